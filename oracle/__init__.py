@@ -1,0 +1,227 @@
+"""CPU oracle for block-scaled FP4 -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never does.
+
+This module is argument marshalling around ``oracle.c`` (plain C, built with
+gcc, no code shared with the CUDA library).  The arithmetic lives in the C
+file; see its header for the definitions and the pages they follow.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+MXFP4 = 0
+NVFP4 = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into a shared library (gcc, OpenMP, strict IEEE fp32)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+               "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        c_i64, c_int, c_f, c_d, c_p = (ctypes.c_int64, ctypes.c_int, ctypes.c_float,
+                                       ctypes.c_double, ctypes.c_void_p)
+        sigs = {
+            "oracle_e2m1_value": (c_d, [c_int]),
+            "oracle_ue8m0_value": (c_d, [c_int]),
+            "oracle_ue4m3_value": (c_d, [c_int]),
+            "oracle_scale_value": (c_d, [c_int, c_int]),
+            "oracle_block_size": (c_int, [c_int]),
+            "oracle_e2m1_round": (c_int, [c_f]),
+            "oracle_ue4m3_round": (c_int, [c_f]),
+            "oracle_ue8m0_round": (c_int, [c_f]),
+            "oracle_scale_round": (c_int, [c_int, c_f]),
+            "oracle_global_scale": (c_f, [c_p, c_i64]),
+            "oracle_global_scale_bf16": (c_f, [c_p, c_i64]),
+            "oracle_quantize_f32": (c_int, [c_int, c_p, c_i64, c_i64, c_f, c_p, c_p]),
+            "oracle_quantize_bf16": (c_int, [c_int, c_p, c_i64, c_i64, c_f, c_p, c_p]),
+            "oracle_dequantize": (c_int, [c_int, c_p, c_p, c_i64, c_i64, c_f, c_p]),
+            "oracle_sf_mma_bytes": (c_i64, [c_i64, c_i64]),
+            "oracle_sf_to_mma": (c_int, [c_p, c_i64, c_i64, c_p]),
+            "oracle_sf_from_mma": (c_int, [c_p, c_i64, c_i64, c_p]),
+            "oracle_gemm_nt": (c_int, [c_int, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_p,
+                                       c_f, c_f, c_p, c_p]),
+            "oracle_gemm_nt_entries": (c_int, [c_int, c_i64, c_p, c_p, c_p, c_p, c_f, c_f,
+                                               c_i64, c_p, c_p, c_p, c_p]),
+            "oracle_num_threads": (c_int, []),
+        }
+        for name, (res, args) in sigs.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def block_size(fmt: int) -> int:
+    return _load().oracle_block_size(fmt)
+
+
+# ---- scalar format functions -------------------------------------------------
+
+def e2m1_value(code: int) -> float:
+    return _load().oracle_e2m1_value(int(code))
+
+
+def ue8m0_value(byte: int) -> float:
+    return _load().oracle_ue8m0_value(int(byte))
+
+
+def ue4m3_value(byte: int) -> float:
+    return _load().oracle_ue4m3_value(int(byte))
+
+
+def scale_value(fmt: int, byte: int) -> float:
+    return _load().oracle_scale_value(int(fmt), int(byte))
+
+
+def e2m1_round(q: float) -> int:
+    return _load().oracle_e2m1_round(float(np.float32(q)))
+
+
+def ue4m3_round(t: float) -> int:
+    return _load().oracle_ue4m3_round(float(np.float32(t)))
+
+
+def ue8m0_round(t: float) -> int:
+    return _load().oracle_ue8m0_round(float(np.float32(t)))
+
+
+def e2m1_round_array(q: np.ndarray) -> np.ndarray:
+    """Vector form of e2m1_round, one C call per element (fp32 input)."""
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.float32).ravel()
+    return np.fromiter((lib.oracle_e2m1_round(float(v)) for v in q), dtype=np.uint8, count=q.size)
+
+
+# ---- tensors -----------------------------------------------------------------
+
+def global_scale(x: np.ndarray) -> np.float32:
+    """gs = amax / (6*448) in fp32.  ``x`` is fp32, or bf16 bits as uint16."""
+    lib = _load()
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        return np.float32(lib.oracle_global_scale_bf16(_ptr(x), x.size))
+    x = x.astype(np.float32, copy=False)
+    return np.float32(lib.oracle_global_scale(_ptr(x), x.size))
+
+
+def quantize(fmt: int, x: np.ndarray, gs: float = 1.0):
+    """x [M, K] fp32, or bf16 bits as uint16 -> (Q uint8 [M, K/2], SF uint8 [M, K/g])."""
+    lib = _load()
+    x = np.ascontiguousarray(x)
+    M, K = x.shape
+    g = block_size(fmt)
+    Q = np.zeros((M, K // 2), dtype=np.uint8)
+    SF = np.zeros((M, K // g), dtype=np.uint8)
+    if x.dtype == np.uint16:
+        rc = lib.oracle_quantize_bf16(fmt, _ptr(x), M, K, float(np.float32(gs)), _ptr(Q), _ptr(SF))
+    else:
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        rc = lib.oracle_quantize_f32(fmt, _ptr(x), M, K, float(np.float32(gs)), _ptr(Q), _ptr(SF))
+    if rc != 0:
+        raise ValueError("oracle quantize rejected its input (shape or non-finite value)")
+    return Q, SF
+
+
+def dequantize(fmt: int, Q: np.ndarray, SF: np.ndarray, gs: float = 1.0) -> np.ndarray:
+    lib = _load()
+    Q = np.ascontiguousarray(Q, dtype=np.uint8)
+    SF = np.ascontiguousarray(SF, dtype=np.uint8)
+    M = Q.shape[0]
+    K = Q.shape[1] * 2
+    X = np.zeros((M, K), dtype=np.float64)
+    if lib.oracle_dequantize(fmt, _ptr(Q), _ptr(SF), M, K, float(np.float32(gs)), _ptr(X)) != 0:
+        raise ValueError("bad shape")
+    return X
+
+
+def sf_mma_bytes(rows: int, cols: int) -> int:
+    return int(_load().oracle_sf_mma_bytes(rows, cols))
+
+
+def sf_to_mma(SF: np.ndarray) -> np.ndarray:
+    lib = _load()
+    SF = np.ascontiguousarray(SF, dtype=np.uint8)
+    rows, cols = SF.shape
+    out = np.zeros(sf_mma_bytes(rows, cols), dtype=np.uint8)
+    lib.oracle_sf_to_mma(_ptr(SF), rows, cols, _ptr(out))
+    return out
+
+
+def sf_from_mma(buf: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    lib = _load()
+    buf = np.ascontiguousarray(buf, dtype=np.uint8)
+    assert buf.size >= sf_mma_bytes(rows, cols)
+    out = np.zeros((rows, cols), dtype=np.uint8)
+    lib.oracle_sf_from_mma(_ptr(buf), rows, cols, _ptr(out))
+    return out
+
+
+def gemm_nt(fmt: int, A: np.ndarray, A_sf: np.ndarray, B: np.ndarray, B_sf: np.ndarray,
+            gs_a: float = 1.0, gs_b: float = 1.0):
+    """Full reference GEMM. Returns (D fp64 [M,N], T fp64 [M,N]); SF row-major."""
+    lib = _load()
+    A, A_sf, B, B_sf = (np.ascontiguousarray(v, dtype=np.uint8) for v in (A, A_sf, B, B_sf))
+    M, N, K = A.shape[0], B.shape[0], A.shape[1] * 2
+    D = np.zeros((M, N), dtype=np.float64)
+    T = np.zeros((M, N), dtype=np.float64)
+    rc = lib.oracle_gemm_nt(fmt, M, N, K, _ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf),
+                            float(np.float32(gs_a)), float(np.float32(gs_b)), _ptr(D), _ptr(T))
+    if rc != 0:
+        raise ValueError("bad shape")
+    return D, T
+
+
+def gemm_nt_entries(fmt: int, A, A_sf, B, B_sf, gs_a, gs_b, mi, ni):
+    """Reference values at sampled (m, n) positions. Returns (D, T) fp64 [count]."""
+    lib = _load()
+    A, A_sf, B, B_sf = (np.ascontiguousarray(v, dtype=np.uint8) for v in (A, A_sf, B, B_sf))
+    K = A.shape[1] * 2
+    mi = np.ascontiguousarray(mi, dtype=np.int64)
+    ni = np.ascontiguousarray(ni, dtype=np.int64)
+    D = np.zeros(mi.size, dtype=np.float64)
+    T = np.zeros(mi.size, dtype=np.float64)
+    rc = lib.oracle_gemm_nt_entries(fmt, K, _ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf),
+                                    float(np.float32(gs_a)), float(np.float32(gs_b)),
+                                    mi.size, _ptr(mi), _ptr(ni), _ptr(D), _ptr(T))
+    if rc != 0:
+        raise ValueError("bad shape")
+    return D, T
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())

@@ -1,0 +1,411 @@
+/*
+ * oracle.c -- plain, slow CPU reference for block-scaled FP4 (MXFP4 / NVFP4).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
+ * calls this file; only the test suite, the smoke check and the CPU-baseline
+ * leg of the benchmark do.  It shares no code, header, table or constant
+ * generator with the CUDA library: every value here is derived from the
+ * format definitions written out below.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [DG]  "Packed MXFP4 & NVFP4 GEMM + mega-MoE (SM100, true 2-CTA multicast)"
+ *         (DeepGEMM pull request), section "Summary": both operands are packed
+ *         E2M1, two elements per byte; MXFP4 carries one UE8M0 scale per 32
+ *         K-elements, NVFP4 one E4M3/UE4M3 scale per 16 K-elements plus
+ *         per-tensor fp32 global scales, dequantised as acc * gs_act * gs_weight;
+ *         the GEMM is [M,K] @ [N,K]^T -> [M,N].
+ *   [MJ]  "fp4_quantization" (Mojo kernel module API), section "Functions":
+ *         dynamic BF16 -> NVFP4/MXFP4 quantisation with per-block scale factors
+ *         (quantize_dynamic_scaled_fp4fp8) and the re-interleave of rank-2
+ *         scale factors into the 5D TCGEN layout (block_scales_interleave).
+ *   [QB]  "quadbit" README, section "Accuracy (real models)": per-16 ue4m3
+ *         local scale with an fp32 global scale (NVFP4), ue8m0 (MXFP4).
+ *   [QG]  "qgemm-mx" project page, section "The gap": MXFP4 moves ~1.88x fewer
+ *         bytes per weight than FP8.
+ * The pages do not print the bit layouts.  Those are taken from the public
+ * OCP Microscaling Formats (MX) v1.0 specification (E2M1 element, E8M0 scale)
+ * and the OCP 8-bit floating point specification (E4M3), as stated at each
+ * function.  Readings of what the pages leave open are marked READING.
+ *
+ * Precision: decoding and the GEMM are done in fp64 (every product is exact);
+ * the quantiser is done in IEEE fp32 with round-to-nearest-even, because the
+ * quantised bytes are defined by fp32 arithmetic.  Build without -ffast-math
+ * and with -ffp-contract=off.
+ *
+ * Parity pins: every function below is checked in the CPU test suite against
+ * closed forms, library conversions, brute-force searches or invariants.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_MXFP4 0
+#define ORACLE_NVFP4 1
+
+/* ------------------------------------------------------------------------ */
+/* Element and scale decoding                                                */
+/* ------------------------------------------------------------------------ */
+
+/* E2M1 (OCP MX v1.0, FP4 E2M1): bits s e1 e0 m, exponent bias 1.
+ * e == 0: subnormal, value m * 0.5; else (1 + m/2) * 2^(e-1).
+ * Codes 0..7 give 0, 0.5, 1, 1.5, 2, 3, 4, 6; codes 8..15 their negatives. */
+double oracle_e2m1_value(int code)
+{
+    int s = (code >> 3) & 1;
+    int e = (code >> 1) & 3;
+    int m = code & 1;
+    double mag = (e == 0) ? 0.5 * m : (1.0 + 0.5 * m) * ldexp(1.0, e - 1);
+    return s ? -mag : mag;
+}
+
+/* UE8M0 (OCP MX v1.0, E8M0 scale): value 2^(e-127) for e in 0..254; 255 is NaN. */
+double oracle_ue8m0_value(int byte)
+{
+    if (byte < 0 || byte > 254) return NAN;
+    return ldexp(1.0, byte - 127);
+}
+
+/* UE4M3: the E4M3 format (OCP 8-bit FP spec, bias 7) with the sign bit fixed
+ * at zero.  e = bits[6:3], m = bits[2:0]; e == 0 is subnormal m * 2^-9,
+ * otherwise (1 + m/8) * 2^(e-7).  0x7F is NaN; bit 7 set is not a UE4M3 code.
+ * Largest finite value 0x7E = 448. */
+double oracle_ue4m3_value(int byte)
+{
+    if (byte < 0 || byte > 0x7E) return NAN;
+    int e = (byte >> 3) & 15;
+    int m = byte & 7;
+    if (e == 0) return ldexp((double)m, -9);
+    return (1.0 + m / 8.0) * ldexp(1.0, e - 7);
+}
+
+/* Scale decoding keyed on the format: MXFP4 -> UE8M0, NVFP4 -> UE4M3 [DG]. */
+double oracle_scale_value(int fmt, int byte)
+{
+    return fmt == ORACLE_MXFP4 ? oracle_ue8m0_value(byte) : oracle_ue4m3_value(byte);
+}
+
+int oracle_block_size(int fmt) { return fmt == ORACLE_MXFP4 ? 32 : 16; }
+
+/* ------------------------------------------------------------------------ */
+/* Rounding to the formats (round to nearest, ties to even code)            */
+/* ------------------------------------------------------------------------ */
+
+/* Nearest entry of a table of ncodes non-negative values that increase with
+ * the code, for a >= 0: the two codes that bracket a are compared (their
+ * distances to a are exact in fp64), ties go to the even code, and anything
+ * at or above the last value gives the last code (saturation). */
+static int nearest_even_code(double a, double (*value)(int), int ncodes)
+{
+    if (a >= value(ncodes - 1)) return ncodes - 1;
+    int hi = 0;
+    while (value(hi) < a) ++hi;            /* first code whose value is >= a */
+    if (hi == 0) return 0;
+    int lo = hi - 1;
+    double dlo = a - value(lo), dhi = value(hi) - a;
+    if (dlo < dhi) return lo;
+    if (dhi < dlo) return hi;
+    return (lo & 1) ? hi : lo;
+}
+
+static double e2m1_magnitude(int code) { return oracle_e2m1_value(code & 7); }
+
+/* E2M1 rounding of an fp32 value q, written as the definition: the nearest
+ * of the eight magnitudes, ties to the code whose mantissa bit is 0 (the even
+ * code), saturating (|q| > 6 -> 6, E2M1 has no Inf/NaN).  The sign bit is
+ * copied from q, so a negative q that rounds to zero gives code 8 (-0).
+ * READING: the pages fix neither the tie rule nor the sign of zero; round to
+ * nearest even is the RNE rule applied to the element, and keeping the sign
+ * matches a sign-preserving conversion. */
+int oracle_e2m1_round(float q)
+{
+    int mag = nearest_even_code(fabs((double)q), e2m1_magnitude, 8);
+    return signbit(q) ? (mag | 8) : mag;
+}
+
+/* UE4M3 rounding of t >= 0: nearest finite UE4M3 value, ties to the even
+ * code, saturating to 0x7E (448) for anything larger ("satfinite"). */
+int oracle_ue4m3_round(float t)
+{
+    double a = (double)t;
+    if (!(a > 0.0)) return 0;          /* zero (and, defensively, negatives) */
+    return nearest_even_code(a, oracle_ue4m3_value, 0x7F);
+}
+
+/* UE8M0 rounding of t >= 0: nearest value 2^(c-127), c in 0..254, ties to
+ * the even code, clamped to 254.  UE8M0 has no zero: t == 0 gives code 0.
+ * READING: the scale rule is round-to-nearest-even of amax/6 (divided by the
+ * global scale); OCP MX v1.0 itself derives the shared exponent as
+ * floor(log2(amax)) - 2, which differs at ties and near the top of a binade. */
+int oracle_ue8m0_round(float t)
+{
+    double a = (double)t;
+    if (!(a > 0.0)) return 0;
+    return nearest_even_code(a, oracle_ue8m0_value, 255);
+}
+
+int oracle_scale_round(int fmt, float t)
+{
+    return fmt == ORACLE_MXFP4 ? oracle_ue8m0_round(t) : oracle_ue4m3_round(t);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Quantiser                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Global scale of a tensor for NVFP4: gs = amax / (6 * 448), one fp32
+ * division (6 * 448 = 2688 is exact).  The largest block amax then lands on
+ * the top of the UE4M3 range.  [DG] "Summary" (per-tensor fp32 global scale);
+ * READING: the value amax/(6*448) is the usual NVFP4 choice. */
+float oracle_global_scale(const float *x, int64_t n)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    return amax / 2688.0f;
+}
+
+static float bf16_bits_to_float(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+float oracle_global_scale_bf16(const uint16_t *x, int64_t n)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fabsf(bf16_bits_to_float(x[i]));
+        if (a > amax) amax = a;
+    }
+    return amax / 2688.0f;
+}
+
+/* One block of g fp32 values -> g nibbles (one per byte, low 4 bits) and the
+ * scale byte.  Steps, in fp32 with round-to-nearest-even at each operation:
+ *   amax = max |x_i|
+ *   t    = (amax / 6) / gs           two divisions, in that order
+ *   sf   = round-to-format(t)        UE8M0 (MXFP4) or UE4M3 (NVFP4)
+ *   s    = decode(sf) * gs           one multiply
+ *   q_i  = x_i / s                   one division per element
+ *   nib_i = E2M1-round(q_i)
+ * READING: if s is zero (UE4M3 code 0, or the product underflows) every
+ * element is encoded as +0 instead of dividing by zero.
+ * [DG] "Summary"; [MJ] quantize_dynamic_scaled_fp4fp8: block amax -> scale
+ * -> E2M1; MXFP4 uses gs = 1. */
+static int quantize_block(int fmt, const float *x, int g, float gs,
+                          uint8_t *nib, uint8_t *sf)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < g; ++i) {
+        if (isnan(x[i]) || isinf(x[i])) return -1;
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    float t = (amax / 6.0f) / gs;
+    int code = oracle_scale_round(fmt, t);
+    float s = (float)oracle_scale_value(fmt, code) * gs;
+    *sf = (uint8_t)code;
+    for (int i = 0; i < g; ++i) {
+        if (s == 0.0f) {
+            nib[i] = 0;
+        } else {
+            float q = x[i] / s;
+            nib[i] = (uint8_t)oracle_e2m1_round(q);
+        }
+    }
+    return 0;
+}
+
+/* X fp32 row-major [M, K] -> Q packed [M, K/2] and SF row-major [M, K/g].
+ * Packing: element k of a row lives in byte k/2, even k in bits [3:0], odd k
+ * in bits [7:4].  READING: the pages say only "2 elems/byte" ([DG]); the
+ * low-nibble-first order is the one the tensor-core GEMM in this library is
+ * pinned to by one-hot probes.  Returns 0, or -1 on bad arguments/inputs. */
+int oracle_quantize_f32(int fmt, const float *X, int64_t M, int64_t K, float gs,
+                        uint8_t *Q, uint8_t *SF)
+{
+    int g = oracle_block_size(fmt);
+    if (M < 0 || K < 0 || K % g != 0) return -1;
+    if (fmt == ORACLE_MXFP4) gs = 1.0f;
+    int64_t kg = K / g;
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t m = 0; m < M; ++m) {
+        uint8_t nib[32];
+        for (int64_t j = 0; j < kg; ++j) {
+            const float *x = X + m * K + j * g;
+            if (quantize_block(fmt, x, g, gs, nib, &SF[m * kg + j]) != 0) {
+                bad = 1;
+                continue;
+            }
+            for (int i = 0; i < g; i += 2)
+                Q[m * (K / 2) + (j * g + i) / 2] = (uint8_t)(nib[i] | (nib[i + 1] << 4));
+        }
+    }
+    return bad ? -1 : 0;
+}
+
+/* Same, from bf16 bit patterns (each converts to fp32 exactly). */
+int oracle_quantize_bf16(int fmt, const uint16_t *X, int64_t M, int64_t K, float gs,
+                         uint8_t *Q, uint8_t *SF)
+{
+    int g = oracle_block_size(fmt);
+    if (M < 0 || K < 0 || K % g != 0) return -1;
+    if (fmt == ORACLE_MXFP4) gs = 1.0f;
+    int64_t kg = K / g;
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t m = 0; m < M; ++m) {
+        float x[32];
+        uint8_t nib[32];
+        for (int64_t j = 0; j < kg; ++j) {
+            for (int i = 0; i < g; ++i) x[i] = bf16_bits_to_float(X[m * K + j * g + i]);
+            if (quantize_block(fmt, x, g, gs, nib, &SF[m * kg + j]) != 0) {
+                bad = 1;
+                continue;
+            }
+            for (int i = 0; i < g; i += 2)
+                Q[m * (K / 2) + (j * g + i) / 2] = (uint8_t)(nib[i] | (nib[i + 1] << 4));
+        }
+    }
+    return bad ? -1 : 0;
+}
+
+/* Dequantise packed codes back to fp64: x[m,k] = E2M1(Q[m,k]) * SF[m,k/g] * gs. */
+int oracle_dequantize(int fmt, const uint8_t *Q, const uint8_t *SF, int64_t M, int64_t K,
+                      float gs, double *X)
+{
+    int g = oracle_block_size(fmt);
+    if (K % g != 0) return -1;
+    double gsd = fmt == ORACLE_MXFP4 ? 1.0 : (double)gs;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) {
+            int byte = Q[m * (K / 2) + k / 2];
+            int code = (k & 1) ? (byte >> 4) : (byte & 15);
+            X[m * K + k] = oracle_e2m1_value(code) *
+                           oracle_scale_value(fmt, SF[m * (K / g) + k / g]) * gsd;
+        }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Scale-factor layout for the tensor cores                                  */
+/* ------------------------------------------------------------------------ */
+
+/* [MJ] block_scales_interleave: rank-2 scale factors [rows, cols] are
+ * re-interleaved into the "5D TCGEN layout".  The pages do not print the
+ * layout; the one used here is the public Blackwell block-scaled layout:
+ * tiles of 128 rows x 4 scale columns, each tile 512 contiguous bytes in
+ * which row r and column c sit at byte (r % 32) * 16 + (r / 32) * 4 + c;
+ * tiles ordered row-tile-major, i.e. a 5D array
+ * [ceil(rows/128)][ceil(cols/4)][32][4][4].  Padding bytes are 0. */
+int64_t oracle_sf_mma_bytes(int64_t rows, int64_t cols)
+{
+    return ((rows + 127) / 128) * ((cols + 3) / 4) * 512;
+}
+
+int oracle_sf_to_mma(const uint8_t *in, int64_t rows, int64_t cols, uint8_t *out)
+{
+    int64_t ctiles = (cols + 3) / 4;
+    memset(out, 0, (size_t)oracle_sf_mma_bytes(rows, cols));
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            int64_t tile = (r / 128) * ctiles + c / 4;
+            int64_t rr = r % 128;
+            int64_t off = tile * 512 + (rr % 32) * 16 + (rr / 32) * 4 + (c % 4);
+            out[off] = in[r * cols + c];
+        }
+    return 0;
+}
+
+int oracle_sf_from_mma(const uint8_t *in, int64_t rows, int64_t cols, uint8_t *out)
+{
+    int64_t ctiles = (cols + 3) / 4;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            int64_t tile = (r / 128) * ctiles + c / 4;
+            int64_t rr = r % 128;
+            out[r * cols + c] = in[tile * 512 + (rr % 32) * 16 + (rr / 32) * 4 + (c % 4)];
+        }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* GEMM                                                                       */
+/* ------------------------------------------------------------------------ */
+
+/* One output element, the definition written out ([DG] "Summary"):
+ *   D[m,n] = gs_a * gs_b * sum_k e2m1(A[m,k]) sfA[m,k/g] * e2m1(B[n,k]) sfB[n,k/g]
+ * Every product is exact in fp64 (at most 12 significant bits, exponents far
+ * inside the fp64 range); the sum is accumulated in fp64 in k order.  Also
+ * returns T = |gs_a gs_b| * sum_k |a_k b_k| for the error bound.
+ * SF are row-major [rows, K/g]. */
+static void gemm_entry(int fmt, int64_t K, const uint8_t *A, const uint8_t *Asf,
+                       const uint8_t *B, const uint8_t *Bsf, double gsab,
+                       int64_t m, int64_t n, double *d_out, double *t_out)
+{
+    int g = oracle_block_size(fmt);
+    int64_t kg = K / g;
+    double acc = 0.0, tacc = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        int ab = A[m * (K / 2) + k / 2];
+        int bb = B[n * (K / 2) + k / 2];
+        int ca = (k & 1) ? (ab >> 4) : (ab & 15);
+        int cb = (k & 1) ? (bb >> 4) : (bb & 15);
+        double a = oracle_e2m1_value(ca) * oracle_scale_value(fmt, Asf[m * kg + k / g]);
+        double b = oracle_e2m1_value(cb) * oracle_scale_value(fmt, Bsf[n * kg + k / g]);
+        acc += a * b;
+        tacc += fabs(a * b);
+    }
+    *d_out = gsab * acc;
+    *t_out = fabs(gsab) * tacc;
+}
+
+/* Full NT GEMM: A packed [M, K/2], B packed [N, K/2], SF row-major; D and T
+ * fp64 [M, N].  MXFP4 ignores gs (1.0).  Returns 0 or -1. */
+int oracle_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K,
+                   const uint8_t *A, const uint8_t *Asf, const uint8_t *B, const uint8_t *Bsf,
+                   float gs_a, float gs_b, double *D, double *T)
+{
+    int g = oracle_block_size(fmt);
+    if (K % g != 0 || K % 2 != 0) return -1;
+    double gsab = fmt == ORACLE_MXFP4 ? 1.0 : (double)gs_a * (double)gs_b;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            gemm_entry(fmt, K, A, Asf, B, Bsf, gsab, m, n, &D[m * N + n], &T[m * N + n]);
+    return 0;
+}
+
+/* Sampled entries (m_i, n_i), for checks at sizes the full product would take
+ * too long on the CPU. */
+int oracle_gemm_nt_entries(int fmt, int64_t K,
+                           const uint8_t *A, const uint8_t *Asf, const uint8_t *B, const uint8_t *Bsf,
+                           float gs_a, float gs_b, int64_t count, const int64_t *mi, const int64_t *ni,
+                           double *D, double *T)
+{
+    int g = oracle_block_size(fmt);
+    if (K % g != 0 || K % 2 != 0) return -1;
+    double gsab = fmt == ORACLE_MXFP4 ? 1.0 : (double)gs_a * (double)gs_b;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t i = 0; i < count; ++i)
+        gemm_entry(fmt, K, A, Asf, B, Bsf, gsab, mi[i], ni[i], &D[i], &T[i]);
+    return 0;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

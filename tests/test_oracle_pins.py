@@ -1,0 +1,434 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each test ties one oracle function to a closed form, a library conversion
+(torch's float8 types), a brute-force search, an invariant of the method, or
+a value printed on the pages / worked by hand from the format definitions
+(fixtures under tests/golden/).  No GPU is used.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_scaled_fp4_tcgen05_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+MX, NV = oracle.MXFP4, oracle.NVFP4
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+def _e2m1_golden():
+    vals = {}
+    for code, val, negzero in _golden_rows("e2m1_values.txt"):
+        vals[int(code)] = (float(val), int(negzero))
+    return vals
+
+
+E2M1 = _e2m1_golden()
+GRID = np.array([E2M1[c][0] for c in range(8)], dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# decoding
+# --------------------------------------------------------------------------
+
+def test_e2m1_decode_matches_format_table():
+    for code in range(16):
+        v = oracle.e2m1_value(code)
+        want, negzero = E2M1[code]
+        assert v == want
+        assert math.copysign(1.0, v) < 0 if negzero else True
+
+
+def test_e2m1_products_bruteforce():
+    """All 256 code x code products equal the table products, exactly."""
+    seen = set()
+    for a in range(16):
+        for b in range(16):
+            p = oracle.e2m1_value(a) * oracle.e2m1_value(b)
+            assert Fraction(p) == Fraction(E2M1[a][0]) * Fraction(E2M1[b][0])
+            seen.add(abs(p))
+    assert max(seen) == 36.0
+    assert len(seen) == len({abs(x * y) for x in GRID for y in GRID})
+
+
+def test_ue4m3_decode_vs_torch_float8():
+    codes = torch.arange(0, 0x7F, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).tolist()
+    for c, r in zip(codes.tolist(), ref):
+        assert oracle.ue4m3_value(c) == r
+    assert oracle.ue4m3_value(0x7E) == 448.0
+    assert oracle.ue4m3_value(0x08) == 2.0 ** -6
+    assert oracle.ue4m3_value(0x01) == 2.0 ** -9
+    assert math.isnan(oracle.ue4m3_value(0x7F))
+    assert math.isnan(oracle.ue4m3_value(0x80))
+
+
+def test_ue8m0_decode_vs_closed_form_and_torch():
+    codes = torch.arange(0, 255, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e8m0fnu).to(torch.float64).tolist()
+    for c, r in zip(codes.tolist(), ref):
+        v = oracle.ue8m0_value(c)
+        assert v == math.ldexp(1.0, c - 127)
+        assert v == r
+    assert math.isnan(oracle.ue8m0_value(255))
+
+
+# --------------------------------------------------------------------------
+# rounding
+# --------------------------------------------------------------------------
+
+def _nearest_even_grid(q):
+    """Brute force: nearest magnitude on the grid, tie -> even code, sign kept."""
+    q = np.asarray(q, dtype=np.float32)
+    # beyond 7 every input is nearest to 6; clamping keeps the fp64 distances exact
+    a = np.minimum(np.abs(q.astype(np.float64)), 7.0)
+    d = np.abs(a[:, None] - GRID[None, :])
+    idx = np.argmin(d, axis=1)                    # first (lower) index on ties
+    nxt = np.minimum(idx + 1, 7)
+    tie = (d[np.arange(a.size), nxt] == d[np.arange(a.size), idx]) & (nxt != idx)
+    idx = np.where(tie & (idx % 2 == 1), nxt, idx)
+    return (idx | np.where(np.signbit(q), 8, 0)).astype(np.uint8)
+
+
+def test_e2m1_round_hand_cases():
+    for inp, code in _golden_rows("e2m1_rounding_cases.txt"):
+        assert oracle.e2m1_round(np.float32(float(inp))) == int(code), inp
+
+
+def test_e2m1_round_bruteforce_random():
+    gen = synth.rng(7)
+    q = np.concatenate([
+        gen.uniform(-7.5, 7.5, 200_000).astype(np.float32),
+        (gen.standard_normal(50_000) * 3).astype(np.float32),
+    ])
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], dtype=np.float32)
+    near = np.concatenate([mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(9))])
+    q = np.concatenate([q, near, -near, np.float32([0.0, -0.0, 6.0, -6.0, 1e30, -1e30])])
+    got = oracle.e2m1_round_array(q)
+    want = _nearest_even_grid(q)
+    assert np.array_equal(got, want)
+
+
+def test_scale_round_hand_cases():
+    for fmt, t, code in _golden_rows("scale_rounding_cases.txt"):
+        fn = oracle.ue8m0_round if fmt == "ue8m0" else oracle.ue4m3_round
+        assert fn(np.float32(float(t))) == int(code), (fmt, t)
+
+
+def test_ue4m3_round_vs_torch_float8():
+    """Below the 448/480 tie torch's float8_e4m3fn conversion is RNE with
+    subnormals, exactly the rounding the scale rule asks for."""
+    gen = synth.rng(11)
+    t = np.concatenate([
+        np.exp(gen.uniform(np.log(1e-5), np.log(463.0), 20_000)).astype(np.float32),
+        gen.uniform(0, 0.02, 5_000).astype(np.float32),
+    ])
+    vals = np.array([oracle.ue4m3_value(c) for c in range(0x7F)], dtype=np.float64)
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)   # exact in fp32
+    t = np.concatenate([t, mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1e9))])
+    t = t[t < 464.0]
+    ref = torch.from_numpy(t).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.ue4m3_round(v) for v in t], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def test_ue8m0_round_vs_torch_away_from_ties():
+    """torch's float8_e8m0fnu conversion rounds to nearest (ties upward); away
+    from the exact 1.5*2^e ties it must agree with round-to-nearest-even."""
+    gen = synth.rng(13)
+    t = np.exp(gen.uniform(np.log(1e-30), np.log(1e30), 20_000)).astype(np.float32)
+    m, _ = np.frexp(t)
+    t = t[m != 0.75]
+    ref = torch.from_numpy(t).to(torch.float8_e8m0fnu).view(torch.uint8).numpy()
+    got = np.array([oracle.ue8m0_round(v) for v in t], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+    # exact ties: the even code
+    for e in range(-20, 21):
+        t = np.float32(1.5 * 2.0 ** e)
+        lo = e + 127
+        assert oracle.ue8m0_round(t) == (lo if lo % 2 == 0 else lo + 1)
+
+
+# --------------------------------------------------------------------------
+# quantiser
+# --------------------------------------------------------------------------
+
+def _grid_blocks(fmt, rows, blocks, seed, gs):
+    """Inputs already on the grid code * scale * gs, with a +-6 in every block
+    so that the block's own scale is recovered exactly."""
+    g = oracle.block_size(fmt)
+    gen = synth.rng(seed)
+    codes = gen.integers(0, 16, size=(rows, blocks, g))
+    pos6 = gen.integers(0, g, size=(rows, blocks))
+    sign6 = gen.integers(0, 2, size=(rows, blocks)) * 8
+    np.put_along_axis(codes, pos6[..., None], (7 + sign6)[..., None], axis=2)
+    if fmt == MX:
+        sfb = gen.integers(110, 145, size=(rows, blocks))
+    else:
+        sfb = gen.integers(1, 0x7F, size=(rows, blocks))
+    x = np.zeros((rows, blocks, g), dtype=np.float64)
+    for r in range(rows):
+        for b in range(blocks):
+            s = (oracle.ue8m0_value(sfb[r, b]) if fmt == MX else oracle.ue4m3_value(sfb[r, b])) * gs
+            x[r, b] = [math.copysign(E2M1[c][0], -1.0 if c >= 8 else 1.0) * s for c in codes[r, b]]
+    return x.reshape(rows, blocks * g).astype(np.float32), codes.reshape(rows, blocks * g), sfb
+
+
+@pytest.mark.parametrize("fmt,gs", [(MX, 1.0), (NV, 1.0), (NV, 2.0 ** -3), (NV, 2.0 ** 5)])
+def test_quantize_roundtrip_exact_on_grid(fmt, gs):
+    x, codes, sfb = _grid_blocks(fmt, 6, 8, 21 + fmt, gs)
+    assert np.array_equal(x.astype(np.float64) / 1.0, x)     # representable
+    Q, SF = oracle.quantize(fmt, x, gs)
+    assert np.array_equal(SF, sfb.astype(np.uint8))
+    lo, hi = Q & 15, Q >> 4
+    got = np.stack([lo, hi], axis=-1).reshape(codes.shape)
+    assert np.array_equal(got, codes.astype(np.uint8))
+    back = oracle.dequantize(fmt, Q, SF, gs)
+    assert np.array_equal(back, x.astype(np.float64))
+
+
+def test_quantize_zero_block_and_saturation():
+    x = np.zeros((1, 32), dtype=np.float32)
+    Q, SF = oracle.quantize(NV, x, 0.5)
+    assert SF.tolist() == [[0, 0]] and Q.max() == 0
+    Q, SF = oracle.quantize(MX, x, 1.0)
+    assert SF.tolist() == [[0]] and Q.max() == 0
+    # NVFP4 scale saturation: t = amax/6/gs of 448, 464, 470, 1e6 -> 0x7E
+    for t in (448.0, 464.0, 470.0, 1e6):
+        x = np.zeros((1, 16), dtype=np.float32)
+        x[0, 3] = np.float32(t * 6)
+        Q, SF = oracle.quantize(NV, x, 1.0)
+        assert SF[0, 0] == 0x7E
+        # q = 6t/448 > 6 for t > 448: saturates to code 7, nibble of element 3
+        assert (Q[0, 1] >> 4) == 7
+
+
+def test_quantize_hand_worked_mx_block():
+    """One MXFP4 block worked by hand: amax = 9 -> t = 1.5 -> tie between
+    2^0 and 2^1 -> even code 128 (scale 2); q = x / 2."""
+    x = np.zeros((1, 32), dtype=np.float32)
+    x[0, :6] = [9.0, -4.5, 1.0, 0.5, -2.5, 3.0]
+    Q, SF = oracle.quantize(MX, x, 1.0)
+    assert SF[0, 0] == 128
+    nib = [Q[0, i // 2] >> (4 * (i % 2)) & 15 for i in range(6)]
+    # q = 4.5 -> 4 (code 6); -2.25 -> -2 (12); 0.5 -> 0.5 (1); 0.25 -> tie -> 0;
+    # -1.25 -> tie -> -1 (10); 1.5 -> 1.5 (3)
+    assert nib == [6, 12, 1, 0, 10, 3]
+
+
+def test_quantize_element_error_property():
+    """Every element lands on the nearest grid point of x/s (or saturates),
+    with s recomputed from the emitted scale byte."""
+    for fmt in (MX, NV):
+        xb = synth.activations_bf16(3 + fmt, 16, 256)
+        x = synth.bf16_bits_to_f32(xb)
+        gs = oracle.global_scale(xb) if fmt == NV else np.float32(1.0)
+        Q, SF = oracle.quantize(fmt, xb, gs)
+        g = oracle.block_size(fmt)
+        codes = np.stack([Q & 15, Q >> 4], axis=-1).reshape(x.shape)
+        for r in range(x.shape[0]):
+            for k in range(x.shape[1]):
+                s = np.float32(np.float32(oracle.scale_value(fmt, SF[r, k // g])) * np.float32(gs))
+                q = np.float32(x[r, k]) / s
+                v = abs(E2M1[int(codes[r, k])][0])
+                if abs(q) >= 6.0:
+                    assert v == 6.0
+                else:
+                    assert abs(abs(q) - v) <= np.min(np.abs(abs(q) - GRID)) + 0.0
+
+
+def test_global_scale_puts_largest_block_at_448():
+    xb = synth.activations_bf16(5, 64, 512)
+    gs = oracle.global_scale(xb)
+    x = synth.bf16_bits_to_f32(xb)
+    assert gs == np.float32(np.float32(np.abs(x).max()) / np.float32(2688.0))
+    Q, SF = oracle.quantize(NV, xb, gs)
+    assert SF.max() == 0x7E
+
+
+def test_byte_accounting_matches_qgemm_page():
+    (row,) = _golden_rows("byte_accounting.txt")
+    printed = float(row[1])
+    x = np.ones((4, 1024), dtype=np.float32)
+    Q, SF = oracle.quantize(MX, x)
+    bits_mx = 8.0 * (Q.nbytes + SF.nbytes) / x.size
+    assert bits_mx == 4.25
+    assert round(8.0 / bits_mx, 2) == printed
+    Q, SF = oracle.quantize(NV, x)
+    assert 8.0 * (Q.nbytes + SF.nbytes) / x.size == 4.5
+
+
+# --------------------------------------------------------------------------
+# GEMM
+# --------------------------------------------------------------------------
+
+def _pack(codes):
+    codes = np.asarray(codes, dtype=np.uint8)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_gemm_all_ones_closed_form(fmt):
+    g = oracle.block_size(fmt)
+    M, N, K = 3, 5, 256
+    A = _pack(np.full((M, K), 2))          # code 2 = 1.0
+    B = _pack(np.full((N, K), 2))
+    sa, sb = (125, 131) if fmt == MX else (0x30, 0x45)
+    Asf = np.full((M, K // g), sa, dtype=np.uint8)
+    Bsf = np.full((N, K // g), sb, dtype=np.uint8)
+    gs_a, gs_b = (1.0, 1.0) if fmt == MX else (0.375, 2.5)
+    D, T = oracle.gemm_nt(fmt, A, Asf, B, Bsf, gs_a, gs_b)
+    dec = oracle.ue8m0_value if fmt == MX else oracle.ue4m3_value
+    want = K * dec(sa) * dec(sb) * gs_a * gs_b
+    assert np.all(D == want) and np.all(T == abs(want))
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_gemm_one_hot_pins_nibble_order(fmt):
+    """A single non-zero element at (m0, k0): the k index <-> nibble mapping
+    (even k low nibble) and the block index k0 // g are both exercised."""
+    g = oracle.block_size(fmt)
+    M, N, K = 4, 3, 128
+    for k0 in (0, 1, 17, 46, 127):
+        codes = np.zeros((M, K), dtype=np.uint8)
+        codes[2, k0] = 7                               # 6.0
+        A = _pack(codes)
+        Asf = np.full((M, K // g), 127 if fmt == MX else 56, dtype=np.uint8)   # 1.0
+        Asf[2, k0 // g] = 129 if fmt == MX else 64                             # 4.0 / 2.0
+        bc = np.zeros((N, K), dtype=np.uint8)
+        bc[:, k0] = [2, 11, 5]                          # 1, -1.5, 3
+        B = _pack(bc)
+        Bsf = np.full((N, K // g), 128 if fmt == MX else 64, dtype=np.uint8)  # 2.0
+        D, _ = oracle.gemm_nt(fmt, A, Asf, B, Bsf, 1.0, 1.0)
+        sa = 4.0 if fmt == MX else 2.0
+        want = np.zeros((M, N))
+        want[2] = np.array([1.0, -1.5, 3.0]) * 6.0 * sa * 2.0
+        assert np.array_equal(D, want), k0
+
+
+def _random_operands(fmt, M, N, K, seed):
+    gen = synth.rng(seed)
+    g = oracle.block_size(fmt)
+    A = gen.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    B = gen.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    lo, hi = (118, 136) if fmt == MX else (1, 0x7F)
+    Asf = gen.integers(lo, hi, size=(M, K // g), dtype=np.uint8)
+    Bsf = gen.integers(lo, hi, size=(N, K // g), dtype=np.uint8)
+    return A, Asf, B, Bsf
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_gemm_vs_numpy_matmul_of_independent_decode(fmt):
+    """Decode with the golden table and torch's float8 decoders, multiply with
+    numpy's matmul (fp64): must match the oracle to fp64 rounding."""
+    M, N, K = 24, 40, 512
+    A, Asf, B, Bsf = _random_operands(fmt, M, N, K, 31 + fmt)
+    gs_a, gs_b = (1.0, 1.0) if fmt == MX else (np.float32(0.0123), np.float32(3.7))
+    g = oracle.block_size(fmt)
+    table = np.array([math.copysign(E2M1[c][0], -1.0 if c >= 8 else 1.0) for c in range(16)])
+    sfdt = torch.float8_e8m0fnu if fmt == MX else torch.float8_e4m3fn
+
+    def deq(Q, SF):
+        codes = np.stack([Q & 15, Q >> 4], axis=-1).reshape(Q.shape[0], -1)
+        sf = torch.from_numpy(SF.copy()).view(sfdt).to(torch.float64).numpy()
+        return table[codes] * np.repeat(sf, g, axis=1)
+
+    ref = (deq(A, Asf) @ deq(B, Bsf).T) * (float(gs_a) * float(gs_b))
+    D, T = oracle.gemm_nt(fmt, A, Asf, B, Bsf, gs_a, gs_b)
+    assert np.allclose(D, ref, rtol=1e-12, atol=1e-12 * np.abs(T).max())
+    Tref = np.abs(deq(A, Asf)) @ np.abs(deq(B, Bsf)).T * abs(float(gs_a) * float(gs_b))
+    assert np.allclose(T, Tref, rtol=1e-12)
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_gemm_tiny_exact_bruteforce(fmt):
+    """2x3 outputs, K = 64, exact rational arithmetic in pure Python."""
+    M, N, K = 2, 3, 64
+    A, Asf, B, Bsf = _random_operands(fmt, M, N, K, 41 + fmt)
+    g = oracle.block_size(fmt)
+    gs_a, gs_b = (1.0, 1.0) if fmt == MX else (0.25, 8.0)
+
+    def val(Q, SF, r, k):
+        byte = int(Q[r, k // 2])
+        code = (byte >> 4) if k % 2 else (byte & 15)
+        mag = Fraction(E2M1[code][0]) if code < 8 else -Fraction(E2M1[code - 8][0])
+        b = int(SF[r, k // g])
+        if fmt == MX:
+            s = Fraction(2) ** (b - 127)
+        else:
+            e, m = b >> 3, b & 7
+            s = Fraction(m, 512) if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+        return mag * s
+
+    D, _ = oracle.gemm_nt(fmt, A, Asf, B, Bsf, gs_a, gs_b)
+    for m in range(M):
+        for n in range(N):
+            exact = sum(val(A, Asf, m, k) * val(B, Bsf, n, k) for k in range(K))
+            exact *= Fraction(gs_a) * Fraction(gs_b)
+            assert Fraction(D[m, n]) == exact
+
+
+def test_gemm_global_scale_identity():
+    A, Asf, B, Bsf = _random_operands(NV, 8, 16, 256, 51)
+    D1, T1 = oracle.gemm_nt(NV, A, Asf, B, Bsf, 1.0, 1.0)
+    D2, T2 = oracle.gemm_nt(NV, A, Asf, B, Bsf, 2.0 ** 3, 2.0 ** -2)
+    assert np.array_equal(D2, 2.0 * D1) and np.array_equal(T2, 2.0 * T1)
+
+
+def test_gemm_ue8m0_increment_doubles_one_block():
+    """Scale byte + 1 on one block of one A row adds exactly that block's
+    contribution once more (it doubles)."""
+    A, Asf, B, Bsf = _random_operands(MX, 4, 6, 256, 61)
+    D0, _ = oracle.gemm_nt(MX, A, Asf, B, Bsf)
+    Asf1 = Asf.copy()
+    Asf1[1, 3] += 1
+    D1, _ = oracle.gemm_nt(MX, A, Asf1, B, Bsf)
+    only = np.zeros_like(A)
+    only[1, 3 * 16:4 * 16] = A[1, 3 * 16:4 * 16]        # block 3 = bytes 48..63
+    Dblk, _ = oracle.gemm_nt(MX, only, Asf, B, Bsf)
+    assert np.array_equal(D1 - D0, Dblk)
+    assert np.array_equal(np.delete(D1, 1, axis=0), np.delete(D0, 1, axis=0))
+
+
+def test_gemm_entries_equal_full():
+    A, Asf, B, Bsf = _random_operands(NV, 32, 48, 256, 71)
+    D, T = oracle.gemm_nt(NV, A, Asf, B, Bsf, 0.5, 0.125)
+
+    mi = np.array([0, 5, 31, 17])
+    ni = np.array([47, 0, 3, 22])
+    d, t = oracle.gemm_nt_entries(NV, A, Asf, B, Bsf, 0.5, 0.125, mi, ni)
+    assert np.array_equal(d, D[mi, ni]) and np.array_equal(t, T[mi, ni])
+
+
+# --------------------------------------------------------------------------
+# scale-factor interleave
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,cols", [(128, 4), (256, 16), (300, 7), (1, 1), (129, 5)])
+def test_sf_interleave_vs_numpy_reshape(rows, cols):
+    """The 5D layout [rows/128][cols/4][32][4][4] built with numpy reshapes."""
+    gen = synth.rng(rows * 100 + cols)
+    sf = gen.integers(1, 255, size=(rows, cols), dtype=np.uint8)
+    R, C = -(-rows // 128) * 128, -(-cols // 4) * 4
+    pad = np.zeros((R, C), dtype=np.uint8)
+    pad[:rows, :cols] = sf
+    # row r = rt*128 + j*32 + i, col c = ct*4 + kk  ->  [rt][ct][i][j][kk]
+    want = pad.reshape(R // 128, 4, 32, C // 4, 4).transpose(0, 3, 2, 1, 4).reshape(-1)
+    got = oracle.sf_to_mma(sf)
+    assert got.size == oracle.sf_mma_bytes(rows, cols) == want.size
+    assert np.array_equal(got, want)
+    assert np.array_equal(oracle.sf_from_mma(got, rows, cols), sf)

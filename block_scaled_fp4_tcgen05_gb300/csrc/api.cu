@@ -1,0 +1,46 @@
+// api.cu -- library-wide entry points of libqfp4: version, status text,
+// device check and the device status poll.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "qfp4_common.cuh"
+
+extern "C" int qfp4_version(void) { return 100; }   // 0.1.0
+
+extern "C" const char *qfp4_status_string(int status)
+{
+    switch (status) {
+    case QFP4_OK: return "ok";
+    case QFP4_ERR_INVALID_ARG: return "invalid argument";
+    case QFP4_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case QFP4_ERR_MISALIGNED: return "pointer not aligned as required";
+    case QFP4_ERR_CUDA: return "CUDA call failed";
+    case QFP4_ERR_TIMEOUT: return "device-side bounded wait ran out";
+    case QFP4_ERR_ARCH: return "current device is not an sm_103 GPU";
+    case QFP4_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+    }
+}
+
+extern "C" int qfp4_device_check(void)
+{
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QFP4_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return QFP4_ERR_CUDA;
+    return (major == 10 && minor == 3) ? QFP4_OK : QFP4_ERR_ARCH;
+}
+
+extern "C" int qfp4_poll_device_status(void *stream)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t q = 0, g = 0;
+    int rc = qfp4::read_clear_status_quant(s, &q);
+    if (rc == QFP4_OK) rc = qfp4::read_clear_status_gemm(s, &g);
+    if (rc != QFP4_OK) return rc;
+    const uint32_t all = q | g;
+    if (all & qfp4::kStatusTimeout) return QFP4_ERR_TIMEOUT;
+    if (all & qfp4::kStatusBadGroup) return QFP4_ERR_INVALID_ARG;
+    return QFP4_OK;
+}

@@ -1,0 +1,38 @@
+// qfp4_common.cuh -- shared host/device helpers of libqfp4 (not part of the ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/qfp4.h"
+
+namespace qfp4 {
+
+// Device status word: one per translation unit that launches kernels.  A
+// kernel that gives up on a bounded wait ORs in a bit; qfp4_poll_device_status
+// reads and clears every unit's word.
+enum : uint32_t { kStatusTimeout = 1u, kStatusBadGroup = 2u };
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+inline int block_elems(int fmt) { return fmt == QFP4_MXFP4 ? 32 : (fmt == QFP4_NVFP4 ? 16 : 0); }
+
+inline int launch_status(cudaError_t e)
+{
+    return e == cudaSuccess ? QFP4_OK : QFP4_ERR_CUDA;
+}
+
+inline int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+// Per-unit status readers (defined in each .cu that owns a status word).
+int read_clear_status_quant(cudaStream_t s, uint32_t *out);
+int read_clear_status_gemm(cudaStream_t s, uint32_t *out);
+
+}  // namespace qfp4

@@ -1,0 +1,170 @@
+"""Thin Python binding of libqfp4.so (see include/qfp4.h).
+
+Argument marshalling only: every function takes torch tensors (or raw
+integers for pointers), passes their device addresses and sizes to the C ABI
+and raises ``Qfp4Error`` on a non-zero status.  All computation happens in
+the CUDA kernels of the library.  There is no fallback: if the library is
+missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+MXFP4 = 0
+NVFP4 = 1
+SF_ROWMAJOR = 0
+SF_MMA = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqfp4.so")
+_lock = threading.Lock()
+_lib = None
+
+# (restype, argtypes) per exported symbol, mirroring include/qfp4.h
+_i32, _i64, _sz, _vp, _cp = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_char_p
+SIGNATURES = {
+    "qfp4_version": (_i32, []),
+    "qfp4_status_string": (_cp, [_i32]),
+    "qfp4_device_check": (_i32, []),
+    "qfp4_poll_device_status": (_i32, [_vp]),
+    "qfp4_block_size": (_i32, [_i32]),
+    "qfp4_sf_mma_bytes": (_sz, [_i64, _i64]),
+    "qfp4_sf_mma_grouped_bytes": (_sz, [_i64, _i64, _i64]),
+    "qfp4_global_scale": (_i32, [_vp, _i64, _i64, _vp, _vp]),
+    "qfp4_global_scale_grouped": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
+    "qfp4_quantize": (_i32, [_i32, _vp, _i64, _i64, _vp, _vp, _vp, _i32, _vp]),
+    "qfp4_quantize_grouped": (_i32, [_i32, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+    "qfp4_sf_interleave": (_i32, [_vp, _i64, _i64, _vp, _i32, _vp]),
+    "qfp4_gemm_workspace_bytes": (_sz, [_i32, _i64, _i64, _i64]),
+    "qfp4_gemm_nt": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "qfp4_gemm_nt_grouped": (_i32, [_i32, _i64, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
+                                    _vp, _vp, _vp, _vp]),
+}
+
+
+class Qfp4Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+def load() -> ctypes.CDLL:
+    """Open libqfp4.so (built by build.py / __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libqfp4.so not built ({LIB_PATH}); run __graft_entry__.build()")
+            lib = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return load().qfp4_status_string(int(status)).decode()
+
+
+def _p(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != 0:
+        raise Qfp4Error(fn, rc)
+
+
+def version() -> int:
+    return load().qfp4_version()
+
+
+def device_check() -> int:
+    return load().qfp4_device_check()
+
+
+def poll_device_status(stream=None) -> int:
+    return load().qfp4_poll_device_status(_stream(stream))
+
+
+def block_size(fmt: int) -> int:
+    return load().qfp4_block_size(fmt)
+
+
+def sf_mma_bytes(rows: int, cols: int) -> int:
+    return int(load().qfp4_sf_mma_bytes(rows, cols))
+
+
+def sf_mma_grouped_bytes(total_rows: int, groups: int, cols: int) -> int:
+    return int(load().qfp4_sf_mma_grouped_bytes(total_rows, groups, cols))
+
+
+def gemm_workspace_bytes(fmt: int, M: int, N: int, K: int) -> int:
+    return int(load().qfp4_gemm_workspace_bytes(fmt, M, N, K))
+
+
+def global_scale(X, gs_out, stream=None) -> None:
+    rows, cols = X.shape
+    _check("qfp4_global_scale",
+           load().qfp4_global_scale(_p(X), rows, cols, _p(gs_out), _stream(stream)))
+
+
+def global_scale_grouped(X, row_offsets, gs_out, stream=None) -> None:
+    rows, cols = X.shape
+    groups = row_offsets.numel() - 1
+    _check("qfp4_global_scale_grouped",
+           load().qfp4_global_scale_grouped(_p(X), rows, cols, groups, _p(row_offsets), _p(gs_out),
+                                            _stream(stream)))
+
+
+def quantize(fmt, X, gs, Q, SF, sf_layout=SF_ROWMAJOR, stream=None) -> None:
+    M, K = X.shape
+    _check("qfp4_quantize",
+           load().qfp4_quantize(fmt, _p(X), M, K, _p(gs), _p(Q), _p(SF), sf_layout, _stream(stream)))
+
+
+def quantize_grouped(fmt, X, row_offsets, gs, Q, SF_mma, stream=None) -> None:
+    rows, K = X.shape
+    groups = row_offsets.numel() - 1
+    _check("qfp4_quantize_grouped",
+           load().qfp4_quantize_grouped(fmt, _p(X), rows, K, groups, _p(row_offsets), _p(gs), _p(Q),
+                                        _p(SF_mma), _stream(stream)))
+
+
+def sf_interleave(SF_in, rows, cols, SF_out, layout=SF_MMA, stream=None) -> None:
+    _check("qfp4_sf_interleave",
+           load().qfp4_sf_interleave(_p(SF_in), rows, cols, _p(SF_out), layout, _stream(stream)))
+
+
+def gemm_nt(fmt, M, N, K, A, A_sf, B, B_sf, gs_a, gs_b, D, workspace=None, ws_bytes=0,
+            stream=None) -> None:
+    _check("qfp4_gemm_nt",
+           load().qfp4_gemm_nt(fmt, M, N, K, _p(A), _p(A_sf), _p(B), _p(B_sf), _p(gs_a), _p(gs_b),
+                               _p(D), _p(workspace), ws_bytes, _stream(stream)))
+
+
+def gemm_nt_grouped(fmt, row_offsets, total_rows, max_group_rows, N, K, A, A_sf, B, B_sf,
+                    gs_a, gs_b, D, stream=None) -> None:
+    groups = row_offsets.numel() - 1
+    _check("qfp4_gemm_nt_grouped",
+           load().qfp4_gemm_nt_grouped(fmt, groups, _p(row_offsets), total_rows, max_group_rows, N, K,
+                                       _p(A), _p(A_sf), _p(B), _p(B_sf), _p(gs_a), _p(gs_b), _p(D),
+                                       _stream(stream)))

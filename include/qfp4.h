@@ -1,0 +1,217 @@
+/*
+ * qfp4.h -- C ABI of libqfp4.so: block-scaled FP4 (MXFP4 / NVFP4) quantiser,
+ * scale-factor interleave and tensor-core GEMM for GB300 (sm_103a).
+ *
+ * Pages this library follows (cited by title and section):
+ *   "Packed MXFP4 & NVFP4 GEMM + mega-MoE (SM100, true 2-CTA multicast)"
+ *     (DeepGEMM pull request), "Summary" and "Key technical details": the GEMM
+ *     [M,K] @ [N,K]^T -> [M,N] in BF16, both operands packed E2M1 two per
+ *     byte, MXFP4 = UE8M0 scale per 32 K-elements, NVFP4 = UE4M3 scale per 16
+ *     K-elements and per-tensor fp32 global scales applied as
+ *     acc * gs_act * gs_weight; the MMA kinds mxf4 (block32) and mxf4nvf4
+ *     (block16); per-expert global scales are listed there as missing.
+ *   "fp4_quantization" (Mojo kernel module API), "Functions": dynamic
+ *     BF16 -> NVFP4/MXFP4 quantisation with per-block scale factors, the
+ *     re-interleave of rank-2 scale factors into the 5D TCGEN layout, and the
+ *     grouped per-expert quantiser and matmul.
+ *   "quadbit" README, "End-to-end serving": the split-K decode kernel that
+ *     fills the GPU at small M, and the one-launch segmented MoE kernel.
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or synchronises inside these calls (except
+ *     qfp4_poll_device_status, which synchronises the given stream).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Work is enqueued asynchronously on `stream`.  Argument errors are
+ *     detected on the host before anything is launched and returned as a
+ *     negative status; nothing is written in that case.
+ *   - Device-side failures (a bounded wait that ran out) are recorded in a
+ *     device status word and reported by qfp4_poll_device_status.
+ *   - Element k of a packed row lives in byte k/2: even k in bits [3:0], odd
+ *     k in bits [7:4].
+ *   - Row-major scale factors SF[rows, cols] hold one byte per block of g
+ *     elements along K (g = 32 for MXFP4, 16 for NVFP4), cols = K / g.
+ *   - The tensor-core ("MMA") scale-factor layout is the 5D layout
+ *     [ceil(rows/128)][ceil(cols/4)][32][4][4]: 512-byte tiles of 128 rows x
+ *     4 columns, row r and column c of a tile at byte
+ *     (r % 32) * 16 + (r / 32) * 4 + c, padded with zero bytes.  Its size is
+ *     qfp4_sf_mma_bytes(rows, cols).
+ */
+#ifndef QFP4_H
+#define QFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Formats. */
+enum { QFP4_MXFP4 = 0, QFP4_NVFP4 = 1 };
+
+/* Scale-factor layouts. */
+enum { QFP4_SF_ROWMAJOR = 0, QFP4_SF_MMA = 1 };
+
+/* Status codes. */
+enum {
+    QFP4_OK = 0,
+    QFP4_ERR_INVALID_ARG = -1,  /* null pointer, bad format/layout, negative size */
+    QFP4_ERR_UNSUPPORTED = -2,  /* shape outside what the kernels handle */
+    QFP4_ERR_MISALIGNED = -3,   /* pointer not 16-byte aligned */
+    QFP4_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed */
+    QFP4_ERR_TIMEOUT = -5,      /* a device-side bounded wait ran out */
+    QFP4_ERR_ARCH = -6,         /* current device is not sm_103 */
+    QFP4_ERR_WORKSPACE = -7     /* workspace missing or too small */
+};
+
+/* Library version (major*10000 + minor*100 + patch). */
+int qfp4_version(void);
+
+/* Human-readable text for a status code.  Never NULL. */
+const char *qfp4_status_string(int status);
+
+/* QFP4_OK if the current CUDA device is a compute-capability 10.3 GPU
+ * (GB300), QFP4_ERR_ARCH otherwise, QFP4_ERR_CUDA if no device is usable. */
+int qfp4_device_check(void);
+
+/* Synchronise `stream`, then return and clear the device status word:
+ * QFP4_OK, or QFP4_ERR_TIMEOUT if any kernel of this library gave up on a
+ * bounded wait since the last poll (its outputs are then undefined). */
+int qfp4_poll_device_status(void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Sizes                                                                    */
+/* ---------------------------------------------------------------------- */
+
+/* Elements per scale block: 32 (MXFP4) or 16 (NVFP4); 0 for a bad fmt. */
+int qfp4_block_size(int fmt);
+
+/* Bytes of the MMA scale-factor layout for a [rows, cols] scale matrix. */
+size_t qfp4_sf_mma_bytes(int64_t rows, int64_t cols);
+
+/* Bytes of the per-group MMA scale-factor layout used by the grouped calls:
+ * every group starts on a 128-row tile, so this is the size for
+ * sum_e ceil(rows_e / 128) <= ceil(total_rows / 128) + groups tiles. */
+size_t qfp4_sf_mma_grouped_bytes(int64_t total_rows, int64_t groups, int64_t cols);
+
+/* ---------------------------------------------------------------------- */
+/* Global scale (NVFP4)                                                     */
+/* ---------------------------------------------------------------------- */
+
+/* gs_out[0] = amax(|X|) / (6 * 448) in fp32 (one IEEE division), where X is
+ * BF16 [rows, cols] row-major.  The block whose |x| reaches amax then gets
+ * the largest UE4M3 scale, 448.  DeepGEMM pull request "Summary" (per-tensor
+ * fp32 global scales).  Requirements: rows, cols >= 0, X 16-byte aligned,
+ * cols % 8 == 0.  An empty X gives gs = 0. */
+int qfp4_global_scale(const void *X_bf16, int64_t rows, int64_t cols, float *gs_out,
+                      void *stream);
+
+/* Per-group version: group e covers rows [row_offsets[e], row_offsets[e+1])
+ * of X (row_offsets is a DEVICE int32 array of groups+1 non-decreasing
+ * entries, row_offsets[0] = 0, row_offsets[groups] = total_rows).
+ * gs_out[e] = amax over group e / (6 * 448).  Same requirements. */
+int qfp4_global_scale_grouped(const void *X_bf16, int64_t total_rows, int64_t cols,
+                              int64_t groups, const int32_t *row_offsets, float *gs_out,
+                              void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Quantiser                                                                */
+/* ---------------------------------------------------------------------- */
+
+/* BF16 X [M, K] -> packed E2M1 Q [M, K/2] and scale bytes SF.
+ * Per block of g elements along K, in IEEE fp32 with round-to-nearest-even:
+ *   amax = max |x|;  t = (amax / 6) / gs;  sf = round-to-format(t)
+ *   (UE8M0: nearest power of two, ties to even code, clamp 254;
+ *    UE4M3: nearest, ties to even, saturate at 448);
+ *   s = decode(sf) * gs;  nibble = E2M1-round(x / s) (nearest even,
+ *   saturate at 6, sign kept); if s == 0 the block encodes as zeros.
+ * Mojo page "fp4_quantization" (quantize_dynamic_scaled_fp4fp8); DeepGEMM
+ * pull request "Summary" (formats).  The output is bit-exact to that rule.
+ *   fmt        QFP4_MXFP4 (gs ignored, 1.0) or QFP4_NVFP4 (gs required)
+ *   gs         DEVICE pointer to one fp32 global scale (NULL allowed for MXFP4)
+ *   sf_layout  QFP4_SF_ROWMAJOR: SF is [M, K/g] row-major;
+ *              QFP4_SF_MMA: SF is written directly in the MMA layout
+ *              (buffer of qfp4_sf_mma_bytes(M, K/g) bytes, padding zeroed).
+ * Requirements: M >= 0, K % 128 == 0, X/Q 16-byte aligned, SF 4-byte aligned. */
+int qfp4_quantize(int fmt, const void *X_bf16, int64_t M, int64_t K, const float *gs,
+                  void *Q_packed, void *SF, int sf_layout, void *stream);
+
+/* Per-group quantiser for MoE-shaped batches (Mojo page "fp4_quantization",
+ * grouped_quantize_dynamic_scaled_fp4_async): rows of group e use gs[e]; the
+ * scale factors are written in the per-group MMA layout, group e starting at
+ * 128-row tile sum_{e' < e} ceil(rows_e' / 128).  Q is [total_rows, K/2].
+ * row_offsets as in qfp4_global_scale_grouped.  SF_mma must hold
+ * qfp4_sf_mma_grouped_bytes(total_rows, groups, K/g) bytes; it is zeroed
+ * by this call before the scale bytes are written. */
+int qfp4_quantize_grouped(int fmt, const void *X_bf16, int64_t total_rows, int64_t K,
+                          int64_t groups, const int32_t *row_offsets, const float *gs,
+                          void *Q_packed, void *SF_mma, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Scale-factor interleave                                                  */
+/* ---------------------------------------------------------------------- */
+
+/* Permute scale bytes between the row-major [rows, cols] layout and the MMA
+ * layout (Mojo page "fp4_quantization", block_scales_interleave: rank-2 scale
+ * factors -> 5D TCGEN layout).
+ *   layout == QFP4_SF_MMA:      SF_in row-major -> SF_out MMA layout
+ *                               (qfp4_sf_mma_bytes bytes, padding zeroed)
+ *   layout == QFP4_SF_ROWMAJOR: SF_in MMA layout -> SF_out row-major
+ * SF_in and SF_out must not overlap.  rows, cols >= 0. */
+int qfp4_sf_interleave(const void *SF_in, int64_t rows, int64_t cols, void *SF_out,
+                       int layout, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* GEMM                                                                     */
+/* ---------------------------------------------------------------------- */
+
+/* Workspace bytes qfp4_gemm_nt needs for this shape (0 when the chosen
+ * kernel needs none).  The split-K decode kernel keeps fp32 partial sums
+ * and tile counters there. */
+size_t qfp4_gemm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K);
+
+/* D[M,N] (BF16, row-major) = bf16_rne(gs_a * gs_b * sum_k a[m,k] * b[n,k]),
+ * a = E2M1(A) * SF_A, b = E2M1(B) * SF_B (DeepGEMM pull request "Summary":
+ * [M,K] @ [N,K]^T -> [M,N], dequant acc * gs_act * gs_weight).
+ *   A_packed  [M, K/2] bytes, K-major;  A_sf  MMA layout for [M, K/g]
+ *   B_packed  [N, K/2] bytes, K-major;  B_sf  MMA layout for [N, K/g]
+ *   gs_a, gs_b DEVICE pointers to one fp32 each (NULL = 1.0; MXFP4 ignores)
+ *   workspace  DEVICE scratch of ws_bytes >= qfp4_gemm_workspace_bytes(...)
+ *              (may be NULL when that is 0); it must not be shared with a
+ *              call running concurrently.
+ * Tensor cores: tcgen05.mma kind::mxf4 (MXFP4) / kind::mxf4nvf4 scale_vec::4X
+ * (NVFP4), fp32 accumulation in tensor memory.
+ * Requirements: M >= 1, N % 128 == 0, K % 128 == 0, all pointers 16-byte
+ * aligned.  Accuracy: |D - exact| <= 2^-8 |exact| + 1e-6 sum_k |a_k b_k|. */
+int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K,
+                 const void *A_packed, const void *A_sf,
+                 const void *B_packed, const void *B_sf,
+                 const float *gs_a, const float *gs_b,
+                 void *D_bf16, void *workspace, size_t ws_bytes, void *stream);
+
+/* Grouped per-expert GEMM in one launch (quadbit README "End-to-end
+ * serving": one-launch segmented MoE kernel; Mojo page: grouped per-expert
+ * block-scaled matmul).  For every group e with rows
+ * [row_offsets[e], row_offsets[e+1]):
+ *   D[rows_e, :] = bf16(gs_a[e] * gs_b[e] * A[rows_e] @ B[e]^T)
+ *   A_packed   [total_rows, K/2];  A_sf  per-group MMA layout (as written by
+ *              qfp4_quantize_grouped)
+ *   B_packed   [groups, N, K/2];   B_sf  [groups] x MMA layout for [N, K/g]
+ *   gs_a, gs_b DEVICE fp32 [groups] (NULL = all 1.0)
+ *   row_offsets DEVICE int32 [groups + 1]; max_group_rows is an upper bound
+ *              on any group's rows (sizes the launch; rows beyond it are an
+ *              error recorded in the device status word).
+ * Requirements as qfp4_gemm_nt; no workspace is needed. */
+int qfp4_gemm_nt_grouped(int fmt, int64_t groups, const int32_t *row_offsets,
+                         int64_t total_rows, int64_t max_group_rows, int64_t N, int64_t K,
+                         const void *A_packed, const void *A_sf,
+                         const void *B_packed, const void *B_sf,
+                         const float *gs_a, const float *gs_b,
+                         void *D_bf16, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QFP4_H */

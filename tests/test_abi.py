@@ -1,0 +1,103 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+declared in include/qfp4.h, and rejects bad arguments on the host before
+launching anything."""
+import os
+import re
+
+import pytest
+
+from block_scaled_fp4_tcgen05_gb300 import qfp4
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qfp4.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qfp4_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(qfp4.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return qfp4.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(qfp4.SIGNATURES), "binding signatures out of sync with the header"
+
+
+def test_version_and_strings(lib):
+    assert qfp4.version() >= 100
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, 12345):
+        assert isinstance(qfp4.status_string(code), str) and qfp4.status_string(code)
+
+
+def test_sizes(lib):
+    assert qfp4.block_size(0) == 32 and qfp4.block_size(1) == 16 and qfp4.block_size(9) == 0
+    assert qfp4.sf_mma_bytes(128, 4) == 512
+    assert qfp4.sf_mma_bytes(129, 5) == 2 * 2 * 512
+    assert qfp4.sf_mma_bytes(0, 8) == 0
+    assert qfp4.sf_mma_grouped_bytes(8192, 8, 256) == (64 + 8) * 64 * 512
+
+
+FAKE = 1 << 40          # a 16-byte aligned address that is never dereferenced
+
+
+def test_quantize_rejects_bad_arguments(lib):
+    L = lib.qfp4_quantize
+    ok_args = dict(fmt=1, X=FAKE, M=16, K=256, gs=FAKE, Q=FAKE, SF=FAKE, layout=0, stream=None)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return L(a["fmt"], a["X"], a["M"], a["K"], a["gs"], a["Q"], a["SF"], a["layout"], a["stream"])
+
+    assert call(fmt=2) == -1
+    assert call(layout=5) == -1
+    assert call(M=-1) == -1
+    assert call(K=200) == -2
+    assert call(X=None) == -1
+    assert call(gs=None) == -1                  # NVFP4 needs a global scale
+    assert call(X=FAKE + 8) == -3
+    assert call(Q=FAKE + 4) == -3
+    assert call(SF=FAKE + 2) == -3
+    assert call(M=0) == 0                       # empty: nothing to do, nothing launched
+
+
+def test_gemm_rejects_bad_arguments(lib):
+    L = lib.qfp4_gemm_nt
+    base = [1, 256, 256, 256, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, None]
+
+    def call(i=None, v=None):
+        a = list(base)
+        if i is not None:
+            a[i] = v
+        return L(*a)
+
+    assert call(0, 3) == -1
+    assert call(1, 0) == -1
+    assert call(2, 100) == -2                   # N % 128
+    assert call(3, 192) == -2                   # K % 128
+    assert call(4, None) == -1
+    assert call(4, FAKE + 8) == -3
+    assert call(10, FAKE + 2) == -3
+
+
+def test_grouped_and_interleave_reject_bad_arguments(lib):
+    assert lib.qfp4_gemm_nt_grouped(1, 0, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE,
+                                    None, None, FAKE, None) == -1
+    assert lib.qfp4_gemm_nt_grouped(1, 300, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE,
+                                    None, None, FAKE, None) == -2
+    assert lib.qfp4_quantize_grouped(1, FAKE, 10, 256, 2, FAKE, None, FAKE, FAKE, None) == -1
+    assert lib.qfp4_sf_interleave(FAKE, 10, 10, FAKE, 7, None) == -1
+    assert lib.qfp4_sf_interleave(FAKE, 10, 10, FAKE + 1, 1, None) == -3
+    assert lib.qfp4_sf_interleave(FAKE, 0, 10, FAKE, 1, None) == 0
+    assert lib.qfp4_global_scale(FAKE, 10, 12, FAKE, None) == -2
+    assert lib.qfp4_global_scale(FAKE + 2, 10, 16, FAKE, None) == -3

@@ -1,0 +1,248 @@
+"""GPU parity of the tensor-core GEMM against the CPU oracle, within
+|D - D_ref| <= 2^-8 |D_ref| + 1e-6 sum_k |a_k b_k| per element."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_scaled_fp4_tcgen05_gb300 import qfp4, synth
+from tests._helpers import (MX, NV, assert_gemm_close, bf16_to_f64, dev_scalar, run_gemm,
+                            to_dev_bf16, to_dev_u8, to_host)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    qfp4.load()
+    assert qfp4.device_check() == 0
+
+
+def pack(codes):
+    codes = np.asarray(codes, dtype=np.uint8)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+
+
+def one_sf(fmt):
+    return 127 if fmt == MX else 0x38          # 1.0
+
+
+# ----------------------------------------------------------------- probes
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_all_ones_closed_form(fmt):
+    M, N, K = 128, 256, 512
+    g = qfp4.block_size(fmt)
+    A, B = pack(np.full((M, K), 2)), pack(np.full((N, K), 2))
+    sa, sb = (126, 129) if fmt == MX else (0x30, 0x40)
+    Asf = np.full((M, K // g), sa, np.uint8)
+    Bsf = np.full((N, K // g), sb, np.uint8)
+    d = run_gemm(fmt, A, Asf, B, Bsf, 1.0, 1.0)
+    want = K * oracle.scale_value(fmt, sa) * oracle.scale_value(fmt, sb)
+    assert np.all(d == want), np.unique(d)[:10]
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_one_hot_elements(fmt):
+    """Single non-zero FP4 element per A row at a distinct k: pins the nibble
+    order and the K position inside the 128-byte swizzled rows."""
+    M, N, K = 128, 256, 512
+    g = qfp4.block_size(fmt)
+    codes = np.zeros((M, K), np.uint8)
+    ks = (np.arange(M) * 37) % K
+    codes[np.arange(M), ks] = 7                          # 6.0
+    A = pack(codes)
+    bc = np.zeros((N, K), np.uint8)
+    bc[:, :] = (np.arange(K)[None, :] % 7) + 1           # distinct per k
+    bc[:, :] += (np.arange(N)[:, None] % 2) * 8          # sign alternates per n
+    B = pack(bc)
+    Asf = np.full((M, K // g), one_sf(fmt), np.uint8)
+    Bsf = np.full((N, K // g), one_sf(fmt), np.uint8)
+    d = run_gemm(fmt, A, Asf, B, Bsf, 1.0, 1.0)
+    d_ref, t_ref = oracle.gemm_nt(fmt, A, Asf, B, Bsf, 1.0, 1.0)
+    assert_gemm_close(d, d_ref, t_ref, "one-hot elements")
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_one_hot_scales(fmt):
+    """All elements 1.0; A's scale bytes distinct per (row, block) and B's per
+    (column, block): pins the scale-factor layout in tensor memory."""
+    M, N, K = 128, 256, 1024
+    g = qfp4.block_size(fmt)
+    kg = K // g
+    A, B = pack(np.full((M, K), 2)), pack(np.full((N, K), 2))
+    gen = synth.rng(3)
+    if fmt == MX:
+        Asf = gen.integers(112, 142, size=(M, kg), dtype=np.uint8)
+        Bsf = gen.integers(112, 142, size=(N, kg), dtype=np.uint8)
+    else:
+        Asf = gen.integers(1, 0x7F, size=(M, kg), dtype=np.uint8)
+        Bsf = gen.integers(1, 0x7F, size=(N, kg), dtype=np.uint8)
+    d = run_gemm(fmt, A, Asf, B, Bsf, 1.0, 1.0)
+    d_ref, t_ref = oracle.gemm_nt(fmt, A, Asf, B, Bsf, 1.0, 1.0)
+    assert_gemm_close(d, d_ref, t_ref, "one-hot scales")
+
+
+# ----------------------------------------------------------------- small cases
+
+def test_small_mxfp4_128x256x256():
+    """The small MXFP4 workload: fp32 N(0,1) operands quantised by the oracle."""
+    case = synth.SMALL_MX
+    gen = synth.rng(case.seed)
+    a = synth.normal_f32(gen, (case.M, case.K))
+    b = synth.normal_f32(gen, (case.N, case.K))
+    A, Asf = oracle.quantize(MX, a)
+    B, Bsf = oracle.quantize(MX, b)
+    d = run_gemm(MX, A, Asf, B, Bsf)
+    d_ref, t_ref = oracle.gemm_nt(MX, A, Asf, B, Bsf)
+    assert_gemm_close(d, d_ref, t_ref, case.name)
+
+
+def random_operands(fmt, M, N, K, seed):
+    gen = synth.rng(seed)
+    g = qfp4.block_size(fmt)
+    A = gen.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    B = gen.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    lo, hi = (118, 136) if fmt == MX else (1, 0x7F)
+    Asf = gen.integers(lo, hi, size=(M, K // g), dtype=np.uint8)
+    Bsf = gen.integers(lo, hi, size=(N, K // g), dtype=np.uint8)
+    return A, Asf, B, Bsf
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (100, 256, 384), (128, 384, 256),
+                                   (300, 640, 1024), (513, 256, 2048), (256, 1280, 640)])
+def test_random_shapes(fmt, M, N, K):
+    A, Asf, B, Bsf = random_operands(fmt, M, N, K, M * 7 + N + K + fmt)
+    gs_a, gs_b = (None, None) if fmt == MX else (0.37, 2.5e-3)
+    d = run_gemm(fmt, A, Asf, B, Bsf, gs_a, gs_b)
+    d_ref, t_ref = oracle.gemm_nt(fmt, A, Asf, B, Bsf, gs_a or 1.0, gs_b or 1.0)
+    assert_gemm_close(d, d_ref, t_ref, f"{M}x{N}x{K}")
+
+
+def test_global_scale_doubles_exactly():
+    A, Asf, B, Bsf = random_operands(NV, 256, 512, 512, 5)
+    d1 = run_gemm(NV, A, Asf, B, Bsf, 0.75, 1.5)
+    d2 = run_gemm(NV, A, Asf, B, Bsf, 1.5, 1.5)
+    assert np.array_equal(d2, 2.0 * d1)
+
+
+# ----------------------------------------------------------------- full pipeline
+
+def device_quantize(fmt, xbits):
+    """gs (NVFP4) -> quantize (row-major SF) -> interleave, all on the device;
+    returns device buffers and the host copies for the oracle."""
+    M, K = xbits.shape
+    g = qfp4.block_size(fmt)
+    X = to_dev_bf16(xbits)
+    gs = torch.ones(1, dtype=torch.float32, device="cuda")
+    if fmt == NV:
+        qfp4.global_scale(X, gs)
+    Q = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+    SF = torch.empty((M, K // g), dtype=torch.uint8, device="cuda")
+    SFm = torch.empty((qfp4.sf_mma_bytes(M, K // g),), dtype=torch.uint8, device="cuda")
+    qfp4.quantize(fmt, X, gs, Q, SF, qfp4.SF_ROWMAJOR)
+    qfp4.sf_interleave(SF, M, K // g, SFm, qfp4.SF_MMA)
+    torch.cuda.synchronize()
+    return Q, SFm, gs, to_host(Q), to_host(SF), np.float32(gs.item())
+
+
+def sampled_check(fmt, qa, qb, D, n_samples, seed, full_rows=(0,)):
+    M, N = D.shape
+    gen = synth.rng(seed)
+    mi = np.concatenate([gen.integers(0, M, n_samples), np.repeat(np.array(full_rows) % M, N)])
+    ni = np.concatenate([gen.integers(0, N, n_samples), np.tile(np.arange(N), len(full_rows))])
+    d_ref, t_ref = oracle.gemm_nt_entries(fmt, qa[3], qa[4], qb[3], qb[4], qa[5], qb[5], mi, ni)
+    d = bf16_to_f64(D)[mi, ni]
+    return assert_gemm_close(d, d_ref, t_ref, "sampled")
+
+
+@pytest.mark.parametrize("case", [synth.PREFILL_NV, synth.DECODE_UP, synth.DECODE_ATTN],
+                         ids=lambda c: c.name)
+def test_pipeline_full_size(case):
+    """Activations and weights quantised on the device (bit-exact against the
+    oracle), then the GEMM at full size, checked on sampled outputs."""
+    xa = synth.activations_bf16(case.seed, case.M, case.K)
+    xw = synth.weights_bf16(case.seed + 1000, case.N, case.K)
+    qa = device_quantize(case.fmt, xa)
+    qb = device_quantize(case.fmt, xw)
+    for q, x in ((qa, xa), (qb, xw)):
+        gs_ref = oracle.global_scale(x) if case.fmt == NV else np.float32(1.0)
+        assert q[5] == gs_ref
+        q_ref, sf_ref = oracle.quantize(case.fmt, x, gs_ref)
+        assert np.array_equal(q[3], q_ref) and np.array_equal(q[4], sf_ref)
+    D = torch.empty((case.M, case.N), dtype=torch.bfloat16, device="cuda")
+    ws_bytes = qfp4.gemm_workspace_bytes(case.fmt, case.M, case.N, case.K)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+    qfp4.gemm_nt(case.fmt, case.M, case.N, case.K, qa[0], qa[1], qb[0], qb[1], qa[2], qb[2], D,
+                 ws, ws_bytes)
+    torch.cuda.synchronize()
+    assert qfp4.poll_device_status() == 0
+    sampled_check(case.fmt, qa, qb, D, 20000, case.seed, full_rows=(0, case.M - 1, 77))
+
+
+@pytest.mark.parametrize("case", synth.COMPUTE_SWEEP, ids=lambda c: c.name)
+def test_compute_sweep_full_size(case):
+    xa = synth.activations_bf16(case.seed, case.M, case.K)
+    xw = synth.weights_bf16(case.seed + 1000, case.N, case.K)
+    qa = device_quantize(case.fmt, xa)
+    qb = device_quantize(case.fmt, xw)
+    D = torch.empty((case.M, case.N), dtype=torch.bfloat16, device="cuda")
+    qfp4.gemm_nt(case.fmt, case.M, case.N, case.K, qa[0], qa[1], qb[0], qb[1], qa[2], qb[2], D)
+    torch.cuda.synchronize()
+    assert qfp4.poll_device_status() == 0
+    sampled_check(case.fmt, qa, qb, D, 8000, case.seed, full_rows=(case.M // 2,))
+
+
+def test_grouped_moe_up_projection():
+    """Per-expert NVFP4 up-projection in one launch: device per-expert global
+    scales and grouped quantisation, then the grouped GEMM."""
+    case = synth.MOE_UP
+    counts = synth.moe_counts(case.seed, case.tokens, case.experts, case.topk)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows = int(offs[-1])
+    E, N, K = case.experts, case.N, case.K
+    g = qfp4.block_size(NV)
+    xa = synth.activations_bf16(case.seed, rows, K)
+    xw = synth.weights_bf16(case.seed + 1000, E * N, K)
+    d_offs = torch.from_numpy(offs).cuda()
+    X = to_dev_bf16(xa)
+    gs_a = torch.empty(E, dtype=torch.float32, device="cuda")
+    qfp4.global_scale_grouped(X, d_offs, gs_a)
+    Qa = torch.empty((rows, K // 2), dtype=torch.uint8, device="cuda")
+    SFa = torch.empty((qfp4.sf_mma_grouped_bytes(rows, E, K // g),), dtype=torch.uint8, device="cuda")
+    qfp4.quantize_grouped(NV, X, d_offs, gs_a, Qa, SFa)
+    # weights: per-expert global scale, quantised per expert, SF interleaved over [E*N, K/g]
+    W = to_dev_bf16(xw)
+    w_offs = torch.arange(0, (E + 1) * N, N, dtype=torch.int32, device="cuda")
+    gs_b = torch.empty(E, dtype=torch.float32, device="cuda")
+    qfp4.global_scale_grouped(W, w_offs, gs_b)
+    Qb = torch.empty((E * N, K // 2), dtype=torch.uint8, device="cuda")
+    SFb = torch.empty((qfp4.sf_mma_grouped_bytes(E * N, E, K // g),), dtype=torch.uint8, device="cuda")
+    qfp4.quantize_grouped(NV, W, w_offs, gs_b, Qb, SFb)
+    D = torch.empty((rows, N), dtype=torch.bfloat16, device="cuda")
+    qfp4.gemm_nt_grouped(NV, d_offs, rows, int(counts.max()), N, K, Qa, SFa, Qb, SFb, gs_a, gs_b, D)
+    torch.cuda.synchronize()
+    assert qfp4.poll_device_status() == 0
+    Qa_h, Qb_h, gsa_h, gsb_h = to_host(Qa), to_host(Qb), to_host(gs_a), to_host(gs_b)
+    Dh = bf16_to_f64(D)
+    gen = synth.rng(case.seed + 7)
+    worst = 0.0
+    for e in range(E):
+        if counts[e] == 0:
+            continue
+        xa_e = xa[offs[e]:offs[e + 1]]
+        xw_e = xw[e * N:(e + 1) * N]
+        assert gsa_h[e] == oracle.global_scale(xa_e) and gsb_h[e] == oracle.global_scale(xw_e)
+        qa_ref, sfa_ref = oracle.quantize(NV, xa_e, gsa_h[e])
+        qb_ref, sfb_ref = oracle.quantize(NV, xw_e, gsb_h[e])
+        assert np.array_equal(Qa_h[offs[e]:offs[e + 1]], qa_ref)
+        assert np.array_equal(Qb_h[e * N:(e + 1) * N], qb_ref)
+        n_s = 3000
+        mi = gen.integers(0, counts[e], n_s)
+        ni = gen.integers(0, N, n_s)
+        d_ref, t_ref = oracle.gemm_nt_entries(NV, qa_ref, sfa_ref, qb_ref, sfb_ref, gsa_h[e], gsb_h[e], mi, ni)
+        worst = max(worst, assert_gemm_close(Dh[offs[e] + mi, ni], d_ref, t_ref, f"expert {e}"))
+    assert worst <= 1.0

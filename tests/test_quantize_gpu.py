@@ -1,0 +1,199 @@
+"""GPU parity of the HBM-bound kernels against the CPU oracle, bit-exact:
+global scale, quantiser (row-major and MMA scale layouts, grouped) and the
+scale-factor interleave."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_scaled_fp4_tcgen05_gb300 import qfp4, synth
+from tests._helpers import MX, NV, dev_scalar, to_dev_bf16, to_dev_u8, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    qfp4.load()
+    assert qfp4.device_check() == 0
+
+
+def quantize_dev(fmt, xbits, gs, layout=qfp4.SF_ROWMAJOR):
+    M, K = xbits.shape
+    g = qfp4.block_size(fmt)
+    X = to_dev_bf16(xbits)
+    Q = torch.full((M, K // 2), 0xAB, dtype=torch.uint8, device="cuda")
+    if layout == qfp4.SF_ROWMAJOR:
+        SF = torch.full((M, K // g), 0xCD, dtype=torch.uint8, device="cuda")
+    else:
+        SF = torch.full((qfp4.sf_mma_bytes(M, K // g),), 0xCD, dtype=torch.uint8, device="cuda")
+    qfp4.quantize(fmt, X, dev_scalar(gs) if gs is not None else None, Q, SF, layout)
+    torch.cuda.synchronize()
+    return to_host(Q), to_host(SF)
+
+
+def check_quantize(fmt, xbits, gs):
+    q_ref, sf_ref = oracle.quantize(fmt, xbits, gs if gs is not None else 1.0)
+    Q, SF = quantize_dev(fmt, xbits, gs, qfp4.SF_ROWMAJOR)
+    bad = np.argwhere(Q != q_ref)
+    assert bad.size == 0, f"{len(bad)} packed bytes differ, first {bad[:5].tolist()}"
+    assert np.array_equal(SF, sf_ref)
+    Q2, SFm = quantize_dev(fmt, xbits, gs, qfp4.SF_MMA)
+    assert np.array_equal(Q2, q_ref)
+    assert np.array_equal(SFm, oracle.sf_to_mma(sf_ref))
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+@pytest.mark.parametrize("M,K", [(1, 128), (37, 384), (130, 1024), (256, 4096)])
+def test_quantize_activations_bitexact(fmt, M, K):
+    x = synth.activations_bf16(1000 + M + K, M, K)
+    gs = oracle.global_scale(x) if fmt == NV else None
+    check_quantize(fmt, x, gs)
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_quantize_weights_bitexact(fmt):
+    x = synth.weights_bf16(77, 512, 2048)
+    check_quantize(fmt, x, oracle.global_scale(x) if fmt == NV else None)
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_quantize_special_values(fmt):
+    """Zero blocks, bf16 subnormals, huge values, signed zeros, mixed scales."""
+    gen = synth.rng(5)
+    rows = []
+    rows.append(np.zeros(256, np.float32))
+    rows.append(np.full(256, -0.0, np.float32))
+    rows.append((gen.standard_normal(256) * 1e-39).astype(np.float32))      # subnormal bf16
+    rows.append((gen.standard_normal(256) * 1e37).astype(np.float32))
+    r = gen.standard_normal(256).astype(np.float32)
+    r[::7] = 0.0
+    r[1::7] = -0.0
+    rows.append(r)
+    rows.append(np.geomspace(1e-30, 1e30, 256).astype(np.float32) * np.where(np.arange(256) % 2, -1, 1))
+    x = synth.f32_to_bf16_bits(np.stack(rows))
+    for gs in ([None] if fmt == MX else [np.float32(1.0), np.float32(3.1e-3), np.float32(1e-30),
+                                          np.float32(7e25), oracle.global_scale(x)]):
+        check_quantize(fmt, x, gs)
+
+
+def test_quantize_on_grid_roundtrip_exact_ties():
+    """Inputs exactly on midpoints of the E2M1 grid times a power-of-two scale:
+    every element is an exact tie and must go to the even code."""
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    for fmt, gs in ((MX, None), (NV, np.float32(0.125))):
+        g = qfp4.block_size(fmt)
+        blocks = []
+        for sc in (2.0 ** -3, 1.0, 2.0 ** 5):
+            for sign in (1.0, -1.0):
+                b = np.zeros(g, np.float32)
+                b[0] = 6.0 * sc * (1.0 if gs is None else gs)
+                b[1:8] = sign * mids * sc * (1.0 if gs is None else gs)
+                blocks.append(b)
+        x = synth.f32_to_bf16_bits(np.concatenate(blocks).reshape(1, -1))
+        pad = (-x.shape[1]) % 128
+        x = np.pad(x, ((0, 0), (0, pad)))
+        check_quantize(fmt, x, gs)
+
+
+def test_quantize_nvfp4_near_ties():
+    """NVFP4 with global scales tuned so x / s lands within a few fp32 ulps of
+    an E2M1 midpoint: the quotient must be the correctly rounded one."""
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    x0 = np.float32(1.0)
+    count = 0
+    for m in mids:
+        for code in (0x30, 0x3B, 0x46, 0x52):
+            dec = np.float32(oracle.ue4m3_value(code))
+            gs0 = np.float32(x0 / (np.float32(m) * dec))
+            for k in range(-3, 4):
+                gs = gs0
+                for _ in range(abs(k)):
+                    gs = np.nextafter(gs, np.float32(np.inf if k > 0 else 0), dtype=np.float32)
+                amax_el = np.float32(6.0) * dec * gs
+                row = np.zeros(128, np.float32)
+                row[0] = amax_el
+                row[1] = x0
+                row[2] = -x0
+                row[3] = np.float32(x0 * 1.5)
+                xb = synth.f32_to_bf16_bits(row.reshape(1, -1))
+                check_quantize(NV, xb, gs)
+                count += 1
+    assert count == 7 * 4 * 7
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_quantize_full_size_16384x4096(fmt):
+    """The decode-batch quantizer workload at full size, bit-exact."""
+    x = synth.activations_bf16(synth.QUANT_SEED, synth.QUANT_ROWS, synth.QUANT_COLS)
+    gs = oracle.global_scale(x) if fmt == NV else None
+    q_ref, sf_ref = oracle.quantize(fmt, x, gs if gs is not None else 1.0)
+    Q, SFm = quantize_dev(fmt, x, gs, qfp4.SF_MMA)
+    assert np.array_equal(Q, q_ref)
+    assert np.array_equal(SFm, oracle.sf_to_mma(sf_ref))
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 4), (16, 16), (200, 64), (4096, 256), (16384, 256)])
+def test_global_scale_bitexact(rows, cols):
+    x = synth.activations_bf16(rows * 7 + cols, rows, cols)
+    gs = torch.empty(1, dtype=torch.float32, device="cuda")
+    qfp4.global_scale(to_dev_bf16(x), gs)
+    torch.cuda.synchronize()
+    assert np.float32(gs.item()) == oracle.global_scale(x)
+
+
+def test_global_scale_grouped_bitexact():
+    counts = synth.moe_counts(5)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    x = synth.activations_bf16(9, int(offs[-1]), 512)
+    gs = torch.empty(len(counts), dtype=torch.float32, device="cuda")
+    qfp4.global_scale_grouped(to_dev_bf16(x), torch.from_numpy(offs).cuda(), gs)
+    torch.cuda.synchronize()
+    got = to_host(gs)
+    for e in range(len(counts)):
+        seg = x[offs[e]:offs[e + 1]]
+        want = oracle.global_scale(seg) if seg.size else np.float32(0.0)
+        assert got[e] == want, e
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_quantize_grouped_bitexact(fmt):
+    counts = np.array([5, 0, 130, 128, 1, 300, 0, 77], dtype=np.int64)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    K = 512
+    g = qfp4.block_size(fmt)
+    x = synth.activations_bf16(11, int(offs[-1]), K)
+    gs_host = np.array([oracle.global_scale(x[offs[e]:offs[e + 1]]) if counts[e] else np.float32(1.0)
+                        for e in range(len(counts))], dtype=np.float32)
+    Q = torch.empty((int(offs[-1]), K // 2), dtype=torch.uint8, device="cuda")
+    SF = torch.full((qfp4.sf_mma_grouped_bytes(int(offs[-1]), len(counts), K // g),), 0xEE,
+                    dtype=torch.uint8, device="cuda")
+    qfp4.quantize_grouped(fmt, to_dev_bf16(x), torch.from_numpy(offs).cuda(),
+                          torch.from_numpy(gs_host).cuda() if fmt == NV else None, Q, SF)
+    torch.cuda.synchronize()
+    Qh, SFh = to_host(Q), to_host(SF)
+    tile = 0
+    for e in range(len(counts)):
+        if counts[e] == 0:
+            continue
+        q_ref, sf_ref = oracle.quantize(fmt, x[offs[e]:offs[e + 1]], gs_host[e] if fmt == NV else 1.0)
+        assert np.array_equal(Qh[offs[e]:offs[e + 1]], q_ref), e
+        ref_mma = oracle.sf_to_mma(sf_ref)
+        start = tile * (K // g // 4) * 512
+        assert np.array_equal(SFh[start:start + ref_mma.size], ref_mma), e
+        tile += -(-int(counts[e]) // 128)
+    assert SFh[tile * (K // g // 4) * 512:].max(initial=0) == 0
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 1), (128, 4), (129, 7), (300, 64), (4096, 256), (8192, 512)])
+def test_sf_interleave_bitexact(rows, cols):
+    sf = synth.rng(rows + cols).integers(0, 255, size=(rows, cols), dtype=np.uint8)
+    out = torch.full((qfp4.sf_mma_bytes(rows, cols),), 0x5A, dtype=torch.uint8, device="cuda")
+    qfp4.sf_interleave(to_dev_u8(sf), rows, cols, out, qfp4.SF_MMA)
+    back = torch.zeros((rows, cols), dtype=torch.uint8, device="cuda")
+    qfp4.sf_interleave(out, rows, cols, back, qfp4.SF_ROWMAJOR)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_host(out), oracle.sf_to_mma(sf))
+    assert np.array_equal(to_host(back), sf)

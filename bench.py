@@ -1,0 +1,573 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-scaled FP4 hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole path over one batch of synthetic input, for
+the NVFP4 prefill-attention GEMM M = N = K = 4096:
+  global scale of the BF16 activations (amax / (6*448))      qfp4_global_scale
+  BF16 -> NVFP4 quantisation, scale factors written straight   qfp4_quantize
+    into the tensor-core layout (the interleave step fused)
+  tensor-core GEMM with the global-scale epilogue -> BF16      qfp4_gemm_nt
+against NVFP4 weights (N(0, 0.02)) quantised once beforehand.  The metric is
+effective TFLOP/s = 2*M*N*K / step time.  L2 is flushed between timed steps.
+
+Also reported on the same JSON line: the roofline of the dominant kernel
+(the GEMM), the CPU oracle timed on a bounded sample ("cpu_baseline"), the
+end-to-end number through host buffers ("e2e"), SM clocks sampled during the
+timed region, and a sweep of the other workloads (decode GEMMs and the
+quantiser in GB/s against HBM, the compute-bound sweep and the grouped MoE
+GEMM in TFLOP/s against the FP4 tensor peak).
+
+Multi-GPU: the path has no exchange step, so N GPUs run N independent
+replicas (weak scaling, no collective on the data path).
+
+--impl reference times the CPU oracle instead (bounded samples per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from block_scaled_fp4_tcgen05_gb300 import synth  # noqa: E402
+
+METRIC = "NVFP4/MXFP4 GEMM eff. TFLOP/s (2MNK) & % FP4 peak; decode/quantize HBM GB/s"
+CASE = synth.PREFILL_NV
+PAGES_BASELINE_TFLOPS = 838.0      # quadbit dense FP4, prefill attn 4096^3, RTX PRO 6000 (SM120)
+FP4_OVER_BF16 = 13.5 / 2.25        # nominal dense FP4 : BF16 tensor rate on GB300
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+GEMM_SRC = os.path.join(ROOT, "block_scaled_fp4_tcgen05_gb300", "csrc", "gemm.cu")
+QUANT_SRC = os.path.join(ROOT, "block_scaled_fp4_tcgen05_gb300", "csrc", "quantize.cu")
+FLUSH_BYTES = 512 << 20
+
+
+# --------------------------------------------------------------------------- helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    """Max over ranks (identity for one process)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def file_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel source changed since the counters were taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            data = json.load(f)
+        ent = data[kernel_key]
+        src = GEMM_SRC if ent.get("source") == "gemm.cu" else QUANT_SRC
+        if ent.get("source_sha") != file_sha(src):
+            return None
+        return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+class Pipeline:
+    """Device buffers and the launches of one step for a GEMM case."""
+
+    def __init__(self, case, device, with_weights=True):
+        import torch
+        from block_scaled_fp4_tcgen05_gb300 import qfp4
+        self.q, self.torch, self.case, self.dev = qfp4, torch, case, device
+        M, N, K, fmt = case.M, case.N, case.K, case.fmt
+        g = qfp4.block_size(fmt)
+        self.g = g
+        xa = synth.activations_bf16(case.seed, M, K)
+        self.X_host = torch.from_numpy(xa.view(np.int16).copy()).view(torch.bfloat16)
+        self.X = self.X_host.to(device)
+        self.X_pinned = self.X_host.pin_memory()
+        self.gs_a = torch.ones(1, dtype=torch.float32, device=device)
+        self.Qa = torch.empty((M, K // 2), dtype=torch.uint8, device=device)
+        self.SFa = torch.empty(qfp4.sf_mma_bytes(M, K // g), dtype=torch.uint8, device=device)
+        self.D = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        self.D_pinned = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+        self.ws_bytes = qfp4.gemm_workspace_bytes(fmt, M, N, K)
+        self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
+        if with_weights:
+            xw = synth.weights_bf16(case.seed + 1000, N, K)
+            W = torch.from_numpy(xw.view(np.int16).copy()).view(torch.bfloat16).to(device)
+            self.gs_b = torch.ones(1, dtype=torch.float32, device=device)
+            self.Qb = torch.empty((N, K // 2), dtype=torch.uint8, device=device)
+            self.SFb = torch.empty(qfp4.sf_mma_bytes(N, K // g), dtype=torch.uint8, device=device)
+            if fmt == qfp4.NVFP4:
+                qfp4.global_scale(W, self.gs_b)
+            qfp4.quantize(fmt, W, self.gs_b, self.Qb, self.SFb, qfp4.SF_MMA)
+            torch.cuda.synchronize()
+            del W
+
+    def prologue(self, X=None):
+        """a1 + a2 (+ a3 fused): global scale and quantisation of the activations."""
+        q, c = self.q, self.case
+        X = self.X if X is None else X
+        if c.fmt == q.NVFP4:
+            q.global_scale(X, self.gs_a)
+        q.quantize(c.fmt, X, self.gs_a, self.Qa, self.SFa, q.SF_MMA)
+
+    def gemm(self, Qb=None, SFb=None, D=None):
+        q, c = self.q, self.case
+        q.gemm_nt(c.fmt, c.M, c.N, c.K, self.Qa, self.SFa, self.Qb if Qb is None else Qb,
+                  self.SFb if SFb is None else SFb, self.gs_a, self.gs_b, self.D if D is None else D,
+                  self.ws, self.ws_bytes)
+
+    def kernels_per_step(self):
+        # amax + finalize (NVFP4), quantise, GEMM
+        return (2 if self.case.fmt == self.q.NVFP4 else 0) + 2
+
+
+def time_main(pipe, steps, warmup, flush, world, device, clocks_gpu):
+    torch = pipe.torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        pipe.prologue()
+        pipe.gemm()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(clocks_gpu)
+    with sampler:
+        time.sleep(0.3)
+        for i in range(steps):
+            flush.zero_()                        # evict L2 (outside the timed events)
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            pipe.prologue()
+            e1.record(stream)
+            pipe.gemm()
+            e2.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    gemm_ms = [b.elapsed_time(c) for _, b, c in ev]
+    pro_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    total_ms = reduce_max(sum(step_ms), world, device)
+    return total_ms, statistics.mean(gemm_ms), statistics.mean(pro_ms), sampler.summary()
+
+
+def time_e2e(pipe, steps, warmup):
+    """Same step through host buffers: pinned H2D of X, the path, D2H of D."""
+    torch = pipe.torch
+    stream = torch.cuda.current_stream()
+
+    def one():
+        pipe.X.copy_(pipe.X_pinned, non_blocking=True)
+        pipe.prologue()
+        pipe.gemm()
+        pipe.D_pinned.copy_(pipe.D, non_blocking=True)
+
+    for _ in range(max(warmup, 1)):
+        one()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return ms, pipe.X_pinned.numel() * 2, pipe.D_pinned.numel() * 2
+
+
+def rotated_gemm_time(case, device, l2_bytes, reps=3):
+    """Mean device time of one GEMM launch over weight copies rotated so that
+    the footprint exceeds twice the L2 (no L2 hits on the weights)."""
+    import torch
+    pipe = Pipeline(case, device)
+    pipe.prologue()
+    wbytes = pipe.Qb.numel() + pipe.SFb.numel()
+    copies = max(1, min(16, int(np.ceil(2 * l2_bytes / max(wbytes, 1))) + 1))
+    Qs = [pipe.Qb] + [pipe.Qb.clone() for _ in range(copies - 1)]
+    SFs = [pipe.SFb] + [pipe.SFb.clone() for _ in range(copies - 1)]
+    for i in range(copies):
+        pipe.gemm(Qs[i], SFs[i])
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = []
+    for _ in range(reps):
+        s.record()
+        for i in range(copies):
+            pipe.gemm(Qs[i], SFs[i])
+        e.record()
+        torch.cuda.synchronize()
+        best.append(s.elapsed_time(e) / copies)
+    ms = statistics.median(best)
+    del Qs, SFs, pipe
+    torch.cuda.empty_cache()
+    return ms
+
+
+def sweep(device, l2_bytes, peaks):
+    import torch
+    from block_scaled_fp4_tcgen05_gb300 import qfp4
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    out = []
+    for case in (synth.DECODE_UP, synth.DECODE_ATTN):
+        ms = rotated_gemm_time(case, device, l2_bytes)
+        g = 16 if case.fmt == 1 else 32
+        byts = case.M * case.K / 2 + case.N * case.K / 2 + (case.M + case.N) * case.K / g + 2 * case.M * case.N
+        gbs = byts / (ms * 1e-3) / 1e9
+        out.append({"workload": case.name, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+                    "frac_hbm": round(gbs / peaks["hbm_gbs"], 3),
+                    "TFLOP/s": round(2 * case.M * case.N * case.K / (ms * 1e-3) / 1e12, 1)})
+    # standalone quantiser X[16384, 4096] (input 134 MB > L2 by itself)
+    for fmt in (qfp4.NVFP4, qfp4.MXFP4):
+        M, K = synth.QUANT_ROWS, synth.QUANT_COLS
+        g = qfp4.block_size(fmt)
+        xa = synth.activations_bf16(synth.QUANT_SEED, M, K)
+        X = torch.from_numpy(xa.view(np.int16).copy()).view(torch.bfloat16).to(device)
+        gs = torch.ones(1, dtype=torch.float32, device=device)
+        qfp4.global_scale(X, gs)
+        Q = torch.empty((M, K // 2), dtype=torch.uint8, device=device)
+        SF = torch.empty(qfp4.sf_mma_bytes(M, K // g), dtype=torch.uint8, device=device)
+        for _ in range(3):
+            qfp4.quantize(fmt, X, gs, Q, SF, qfp4.SF_MMA)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ts = []
+        for _ in range(10):
+            s.record()
+            qfp4.quantize(fmt, X, gs, Q, SF, qfp4.SF_MMA)
+            e.record()
+            torch.cuda.synchronize()
+            ts.append(s.elapsed_time(e))
+        ms = statistics.median(ts)
+        byts = 2 * M * K + M * K / 2 + M * K / g
+        gbs = byts / (ms * 1e-3) / 1e9
+        out.append({"workload": f"{'nv' if fmt else 'mx'}fp4_quantize_{M}x{K}", "us": round(ms * 1e3, 2),
+                    "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 3)})
+        del X, Q, SF
+    # compute-bound sweep
+    for case in synth.COMPUTE_SWEEP:
+        ms = rotated_gemm_time(case, device, l2_bytes, reps=3)
+        tf = 2 * case.M * case.N * case.K / (ms * 1e-3) / 1e12
+        out.append({"workload": case.name, "us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
+                    "frac_fp4_peak": round(tf / fp4_peak, 3)})
+    # grouped MoE up-projection
+    out.append(grouped_time(device, fp4_peak))
+    torch.cuda.empty_cache()
+    return out
+
+
+def grouped_time(device, fp4_peak):
+    import torch
+    from block_scaled_fp4_tcgen05_gb300 import qfp4
+    case = synth.MOE_UP
+    counts = synth.moe_counts(case.seed, case.tokens, case.experts, case.topk)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows, E, N, K = int(offs[-1]), case.experts, case.N, case.K
+    g = qfp4.block_size(case.fmt)
+    X = torch.from_numpy(synth.activations_bf16(case.seed, rows, K).view(np.int16).copy()).view(
+        torch.bfloat16).to(device)
+    W = torch.from_numpy(synth.weights_bf16(case.seed + 1000, E * N, K).view(np.int16).copy()).view(
+        torch.bfloat16).to(device)
+    d_offs = torch.from_numpy(offs).to(device)
+    w_offs = torch.arange(0, (E + 1) * N, N, dtype=torch.int32, device=device)
+    gs_a = torch.empty(E, dtype=torch.float32, device=device)
+    gs_b = torch.empty(E, dtype=torch.float32, device=device)
+    Qa = torch.empty((rows, K // 2), dtype=torch.uint8, device=device)
+    SFa = torch.empty(qfp4.sf_mma_grouped_bytes(rows, E, K // g), dtype=torch.uint8, device=device)
+    Qb = torch.empty((E * N, K // 2), dtype=torch.uint8, device=device)
+    SFb = torch.empty(qfp4.sf_mma_grouped_bytes(E * N, E, K // g), dtype=torch.uint8, device=device)
+    D = torch.empty((rows, N), dtype=torch.bfloat16, device=device)
+    qfp4.global_scale_grouped(W, w_offs, gs_b)
+    qfp4.quantize_grouped(case.fmt, W, w_offs, gs_b, Qb, SFb)
+    del W
+
+    def step():
+        qfp4.global_scale_grouped(X, d_offs, gs_a)
+        qfp4.quantize_grouped(case.fmt, X, d_offs, gs_a, Qa, SFa)
+        qfp4.gemm_nt_grouped(case.fmt, d_offs, rows, int(counts.max()), N, K, Qa, SFa, Qb, SFb,
+                             gs_a, gs_b, D)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    ts, gts = [], []
+    for _ in range(5):
+        flush.zero_()
+        s, m, e = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        s.record()
+        qfp4.global_scale_grouped(X, d_offs, gs_a)
+        qfp4.quantize_grouped(case.fmt, X, d_offs, gs_a, Qa, SFa)
+        m.record()
+        qfp4.gemm_nt_grouped(case.fmt, d_offs, rows, int(counts.max()), N, K, Qa, SFa, Qb, SFb,
+                             gs_a, gs_b, D)
+        e.record()
+        torch.cuda.synchronize()
+        ts.append(s.elapsed_time(e))
+        gts.append(m.elapsed_time(e))
+    flops = 2.0 * rows * N * K
+    ms, gms = statistics.median(ts), statistics.median(gts)
+    return {"workload": case.name, "expert_rows": counts.tolist(), "us_step": round(ms * 1e3, 1),
+            "TFLOP/s_step": round(flops / (ms * 1e-3) / 1e12, 1), "us_gemm": round(gms * 1e3, 1),
+            "TFLOP/s_gemm": round(flops / (gms * 1e-3) / 1e12, 1),
+            "frac_fp4_peak_gemm": round(flops / (gms * 1e-3) / 1e12 / fp4_peak, 3)}
+
+
+# --------------------------------------------------------------------------- CPU oracle arm
+
+def oracle_sample(case, target_s):
+    """Time the oracle on a bounded sample of the step: global scale over the
+    whole activation tensor, quantisation of a slab of rows, and the GEMM of
+    that slab against all N columns.  Returns (TFLOP/s, seconds, rows, threads)."""
+    import oracle
+    xa = synth.activations_bf16(case.seed, case.M, case.K)
+    xw = synth.weights_bf16(case.seed + 1000, case.N, case.K)
+    gw = oracle.global_scale(xw) if case.fmt == 1 else np.float32(1.0)
+    qw, sfw = oracle.quantize(case.fmt, xw, gw)
+
+    def run(rows):
+        t0 = time.perf_counter()
+        gs = oracle.global_scale(xa) if case.fmt == 1 else np.float32(1.0)
+        qa, sfa = oracle.quantize(case.fmt, xa[:rows], gs)
+        mi = np.repeat(np.arange(rows), case.N)
+        ni = np.tile(np.arange(case.N), rows)
+        oracle.gemm_nt_entries(case.fmt, qa, sfa, qw, sfw, gs, gw, mi, ni)
+        return time.perf_counter() - t0
+
+    t1 = run(1)
+    rows = int(max(1, min(case.M, target_s / max(t1, 1e-3))))
+    return rows, run, oracle.num_threads()
+
+
+def cpu_baseline(case, target_s=10.0):
+    rows, run, threads = oracle_sample(case, target_s)
+    dt = run(rows)
+    tf = 2.0 * rows * case.N * case.K / dt / 1e12
+    return {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{case.name}: global scale of all {case.M} rows, quantise {rows} rows, "
+                      f"GEMM of those {rows} rows x {case.N} columns (fp64), {dt:.1f} s"}
+
+
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return                      # the oracle arm runs on rank 0 only
+    case = CASE
+    rows, run, threads = oracle_sample(case, 3.0)
+    for _ in range(args.warmup):
+        run(rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run(rows)
+    dt = (time.perf_counter() - t0) / args.steps
+    tf = 2.0 * rows * case.N * case.K / dt / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": case.name, "M": case.M, "N": case.N, "K": case.K, "format": "NVFP4",
+                       "sample_rows_per_step": rows, "l2": "n/a (host)"},
+            "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{rows} of {case.M} activation rows per step (global scale, "
+                                       f"quantise, GEMM vs all {case.N} columns)"},
+            "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+    from block_scaled_fp4_tcgen05_gb300 import qfp4
+    qfp4.load()
+    if qfp4.device_check() != 0:
+        raise SystemExit("bench.py needs an sm_103 GPU")
+    props = torch.cuda.get_device_properties(device)
+    l2_bytes = getattr(props, "L2_cache_size", 128 << 20)
+    peaks = load_peaks()
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+
+    case = CASE
+    pipe = Pipeline(case, device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else local
+    total_ms, gemm_ms, pro_ms, clocks = time_main(pipe, args.steps, args.warmup, flush, world,
+                                                  device, gpu_index)
+    assert qfp4.poll_device_status() == 0
+    flops = 2.0 * case.M * case.N * case.K
+    ms_per_step = total_ms / args.steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        return
+
+    e2e_ms, h2d, d2h = time_e2e(pipe, max(10, args.steps // 2), args.warmup)
+    gemm_tf = flops / (gemm_ms * 1e-3) / 1e12
+    traffic = ncu_traffic("gemm_nvfp4_4096x4096x4096")
+    roof = {"bound": "tensor", "achieved": round(gemm_tf, 1), "peak": round(fp4_peak, 1),
+            "unit": "TFLOP/s", "frac": round(gemm_tf / fp4_peak, 4), "traffic": traffic,
+            "kernel": "gemm_kernel<NVFP4, BN=256> (qfp4_gemm_nt)", "gemm_us": round(gemm_ms * 1e3, 2),
+            "prologue_us": round(pro_ms * 1e3, 2),
+            "peak_note": f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} TFLOP/s x {FP4_OVER_BF16:g} "
+                         f"(nominal dense FP4:BF16 ratio), of {peaks['source']}"}
+    del pipe
+    torch.cuda.empty_cache()
+    extra = [] if args.no_sweep else sweep(device, l2_bytes, peaks)
+    cpu = None if args.no_cpu else cpu_baseline(case)
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": round(value / PAGES_BASELINE_TFLOPS, 3),
+            "vs_baseline_note": "quadbit dense FP4 prefill attn 4096^3, 838 TF/s on RTX PRO 6000 (SM120)",
+            "dtype": "nvfp4 (e2m1 x ue4m3) -> fp32 accumulate -> bf16", "data": "synthetic",
+            "config": {"workload": case.name, "M": case.M, "N": case.N, "K": case.K, "format": "NVFP4",
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": "flushed between timed steps (512 MiB write)",
+                       "step": "global scale + quantise (SF in MMA layout) + GEMM"},
+            "gpu_launches": pipe_kernels(case) * args.steps,
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "clocks": clocks, "sweep": extra}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+def pipe_kernels(case):
+    return (2 if case.fmt == 1 else 0) + 2
+
+
+if __name__ == "__main__":
+    main()

@@ -31,6 +31,7 @@
 #include <mutex>
 
 #include "qfp4_common.cuh"
+#include "qfp4_gemm_internal.cuh"
 #include "sm103_ptx.cuh"
 
 namespace qfp4 {
@@ -86,17 +87,7 @@ struct Cfg {
     static_assert(SMEM <= 232448, "shared memory overflow");
 };
 
-struct GemmArgs {
-    const uint8_t *A_sf;
-    const uint8_t *B_sf;
-    const float *gs_a;
-    const float *gs_b;
-    __nv_bfloat16 *D;
-    int32_t M, N, K;
-    // grouped
-    int32_t groups;
-    const int32_t *row_offsets;
-};
+using GemmArgs = GemmParams;
 
 struct TileInfo {
     int32_t row0;      // first row of A / D
@@ -383,6 +374,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
     return fn;
 }
 
+}  // namespace
+
 // 2D byte matrix [rows, inner] (row stride = inner bytes), box of
 // box_inner bytes x box_rows rows, 128-byte swizzle, zero fill out of bounds.
 int make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, uint32_t box_inner,
@@ -399,6 +392,8 @@ int make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, 
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? QFP4_OK : QFP4_ERR_CUDA;
 }
+
+namespace {
 
 template <int FMT, int BN, int STAGES, bool GROUPED>
 int launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &a, int32_t tiles,
@@ -446,15 +441,22 @@ extern "C" int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K, const void
     if (!aligned16(A_packed) || !aligned16(A_sf) || !aligned16(B_packed) || !aligned16(B_sf) ||
         !aligned16(D_bf16) || (gs_a && !aligned4(gs_a)) || (gs_b && !aligned4(gs_b)))
         return QFP4_ERR_MISALIGNED;
-    const bool wide = N % 256 == 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    GemmParams a{static_cast<const uint8_t *>(A_sf), static_cast<const uint8_t *>(B_sf), gs_a, gs_b,
+                 static_cast<__nv_bfloat16 *>(D_bf16), static_cast<int32_t>(M), static_cast<int32_t>(N),
+                 static_cast<int32_t>(K), 0, nullptr};
     CUtensorMap ma, mb;
+    if (N % 256 == 0 && M > 128) {
+        // CTA pairs on 256 x 256 tiles
+        int rc = make_map(&ma, A_packed, K / 2, M, kBKBytes, 128);
+        if (rc == QFP4_OK) rc = make_map(&mb, B_packed, K / 2, N, kBKBytes, 128);
+        if (rc != QFP4_OK) return rc;
+        return launch_gemm_pair(fmt, false, ma, mb, a, ((M + 255) / 256) * (N / 256), s);
+    }
+    const bool wide = N % 256 == 0;
     int rc = make_map(&ma, A_packed, K / 2, M, kBKBytes, kBM);
     if (rc == QFP4_OK) rc = make_map(&mb, B_packed, K / 2, N, kBKBytes, wide ? 256 : 128);
     if (rc != QFP4_OK) return rc;
-    GemmArgs a{static_cast<const uint8_t *>(A_sf), static_cast<const uint8_t *>(B_sf), gs_a, gs_b,
-               static_cast<__nv_bfloat16 *>(D_bf16), static_cast<int32_t>(M), static_cast<int32_t>(N),
-               static_cast<int32_t>(K), 0, nullptr};
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int32_t mtiles = static_cast<int32_t>((M + kBM - 1) / kBM);
     if (fmt == QFP4_NVFP4) {
         if (wide) return launch_gemm<QFP4_NVFP4, 256, 4, false>(ma, mb, a, mtiles * (N / 256), s);
@@ -482,24 +484,25 @@ extern "C" int qfp4_gemm_nt_grouped(int fmt, int64_t groups, const int32_t *row_
         (gs_b && !aligned4(gs_b)))
         return QFP4_ERR_MISALIGNED;
     if (total_rows == 0) return QFP4_OK;
-    const bool wide = N % 256 == 0;
-    CUtensorMap ma, mb;
-    int rc = make_map(&ma, A_packed, K / 2, total_rows, kBKBytes, kBM);
-    if (rc == QFP4_OK) rc = make_map(&mb, B_packed, K / 2, groups * N, kBKBytes, wide ? 256 : 128);
-    if (rc != QFP4_OK) return rc;
-    GemmArgs a{static_cast<const uint8_t *>(A_sf), static_cast<const uint8_t *>(B_sf), gs_a, gs_b,
-               static_cast<__nv_bfloat16 *>(D_bf16), static_cast<int32_t>(total_rows),
-               static_cast<int32_t>(N), static_cast<int32_t>(K), static_cast<int32_t>(groups),
-               row_offsets};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // upper bound on row tiles: every group may add one partial tile
-    const int64_t mt_bound = (total_rows + kBM - 1) / kBM + groups;
+    GemmParams a{static_cast<const uint8_t *>(A_sf), static_cast<const uint8_t *>(B_sf), gs_a, gs_b,
+                 static_cast<__nv_bfloat16 *>(D_bf16), static_cast<int32_t>(total_rows),
+                 static_cast<int32_t>(N), static_cast<int32_t>(K), static_cast<int32_t>(groups),
+                 row_offsets};
+    CUtensorMap ma, mb;
     (void)max_group_rows;
-    const int32_t tiles = static_cast<int32_t>(mt_bound * (N / (wide ? 256 : 128)));
-    if (fmt == QFP4_NVFP4) {
-        if (wide) return launch_gemm<QFP4_NVFP4, 256, 4, true>(ma, mb, a, tiles, s);
-        return launch_gemm<QFP4_NVFP4, 128, 6, true>(ma, mb, a, tiles, s);
+    if (N % 256 == 0) {
+        int rc = make_map(&ma, A_packed, K / 2, total_rows, kBKBytes, 128);
+        if (rc == QFP4_OK) rc = make_map(&mb, B_packed, K / 2, groups * N, kBKBytes, 128);
+        if (rc != QFP4_OK) return rc;
+        // upper bound on pair tiles: every group may add one partial tile
+        return launch_gemm_pair(fmt, true, ma, mb, a, ((total_rows + 255) / 256 + groups) * (N / 256), s);
     }
-    if (wide) return launch_gemm<QFP4_MXFP4, 256, 4, true>(ma, mb, a, tiles, s);
+    int rc = make_map(&ma, A_packed, K / 2, total_rows, kBKBytes, kBM);
+    if (rc == QFP4_OK) rc = make_map(&mb, B_packed, K / 2, groups * N, kBKBytes, 128);
+    if (rc != QFP4_OK) return rc;
+    const int64_t mt_bound = (total_rows + kBM - 1) / kBM + groups;
+    const int32_t tiles = static_cast<int32_t>(mt_bound * (N / 128));
+    if (fmt == QFP4_NVFP4) return launch_gemm<QFP4_NVFP4, 128, 6, true>(ma, mb, a, tiles, s);
     return launch_gemm<QFP4_MXFP4, 128, 6, true>(ma, mb, a, tiles, s);
 }

@@ -1,0 +1,504 @@
+// gemm_pair.cu -- block-scaled FP4 GEMM on CTA pairs (tcgen05 cta_group::2).
+//
+// Pages: DeepGEMM pull request "Packed MXFP4 & NVFP4 GEMM + mega-MoE (SM100,
+// true 2-CTA multicast)", "Key technical details": 2-CTA cta_group::2 MMAs
+// with leader-routed barriers and per-CTA scale-factor loads; NVFP4 carries
+// twice the scale-factor traffic of MXFP4 per K-block.
+//
+// A cluster of two CTAs on two SMs computes a 256 x 256 output tile.  CTA r
+// holds rows [m0 + 128 r, +128) of A and rows [n0 + 128 r, +128) of B in its
+// shared memory; the leader (r = 0) issues M=256 x N=256 x K=64 MMAs that read
+// both CTAs' operands, and each CTA's tensor memory receives its own 128 rows
+// of the fp32 accumulator.  Per CTA (20 warps):
+//   warp 0        A/B TMA producer: 256-K slices of A and B into a 5-deep
+//                 (NVFP4) / 6-deep (MXFP4) ring; the leader's mbarrier
+//                 collects the bytes of both CTAs.
+//   warp 1        tensor-memory owner; in the leader, the single MMA issuer.
+//   warp 2        scale-factor producer: the K-block's 512-byte scale tiles
+//                 (A: this CTA's 128 rows; B: all 256 columns) into an 8-deep
+//                 ring of their own, so their latency hides behind more
+//                 K-blocks than the operand ring holds.
+//   warps 4..11   scale-factor warps, two sets of four taking alternate
+//                 K-blocks: move the scale bytes from shared memory into the
+//                 tensor-memory slot paired with the K-block's A/B stage (so
+//                 one MMA commit frees both, and the stage's full barrier also
+//                 counts the scale warps) with tcgen05.st (each warp its own 32-lane
+//                 quarter), then signal the leader.  Writing from registers
+//                 keeps the tensor pipe free of the shared->tensor-memory
+//                 copies NVFP4 would otherwise need (twelve per 256-K block),
+//                 and only B's scales are replicated across the quarters.
+//   warps 12..19  epilogue: drain 128 rows x 256 columns of the accumulator in
+//                 two halves (scaled by gs_a * gs_b and rounded to BF16 on the
+//                 way), release it, and store while the next tile's main loop
+//                 runs.
+// Hand-offs between the CTAs use cluster-scope mbarrier arrivals; the ones
+// that only order tensor-memory writes (already complete after
+// tcgen05.wait::st and fenced) are relaxed, which keeps them off the
+// per-K-block critical path.
+// Every wait is bounded (2 s) and reports QFP4_ERR_TIMEOUT through the device
+// status word.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "qfp4_common.cuh"
+#include "qfp4_gemm_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace qfp4 {
+
+__device__ uint32_t g_status_gemm_pair = 0;
+
+int read_clear_status_gemm_pair(cudaStream_t s, uint32_t *out)
+{
+    uint32_t zero = 0;
+    if (cudaMemcpyFromSymbolAsync(out, g_status_gemm_pair, sizeof(uint32_t), 0,
+                                  cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return QFP4_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return QFP4_ERR_CUDA;
+    if (cudaMemcpyToSymbolAsync(g_status_gemm_pair, &zero, sizeof(uint32_t), 0,
+                                cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return QFP4_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? QFP4_OK : QFP4_ERR_CUDA;
+}
+
+namespace {
+
+constexpr int kThreads = 640;          // 20 warps
+constexpr int kMaxGroups = 256;
+
+template <int FMT>
+struct PairCfg {
+    static constexpr int G = FMT == QFP4_MXFP4 ? 32 : 16;
+    static constexpr int CPS = (256 / G) / 4;          // SF tiles per 128 rows per 256-K block
+    static constexpr int AB_STAGES = FMT == QFP4_MXFP4 ? 6 : 5;
+    static constexpr int SF_STAGES = 8;                // scale-factor ring in shared memory
+    static constexpr int T_SLOTS = AB_STAGES;          // scale-factor slots in tensor memory (one per A/B stage)
+    static constexpr int A_BYTES = 128 * 128;
+    static constexpr int B_BYTES = 128 * 128;
+    static constexpr int AB_BYTES = A_BYTES + B_BYTES;
+    static constexpr int SFA_BYTES = CPS * 512;        // this CTA's 128 rows
+    static constexpr int SFB_BYTES = 2 * CPS * 512;    // all 256 columns of the pair tile
+    static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
+    static constexpr int SFA_COLS = CPS * 4;
+    static constexpr int SFB_COLS = 2 * CPS * 4;
+    static constexpr int SLOT_COLS = SFA_COLS + SFB_COLS;
+    static constexpr int COL_SF = 256;
+    static constexpr int OFF_SF = AB_STAGES * AB_BYTES;
+    static constexpr int OFF_BAR = OFF_SF + SF_STAGES * SF_BYTES;
+    // full/empty[AB], sf_full/sf_empty[SF], acc_full, acc_empty
+    static constexpr int NBAR = 2 * AB_STAGES + 2 * SF_STAGES + 2;
+    static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
+    static_assert(COL_SF + T_SLOTS * SLOT_COLS <= 512, "tensor memory overflow");
+    static_assert(SMEM <= 232448, "shared memory overflow");
+    static_assert(SF_STAGES % 2 == 0, "scale warps alternate K-blocks");
+};
+
+__device__ __forceinline__ void record_timeout()
+{
+    atomicOr(&g_status_gemm_pair, static_cast<uint32_t>(kStatusTimeout));
+}
+
+struct PairTile {
+    int32_t row0;      // first row of the pair's 256-row A tile
+    int32_t row_end;   // rows of this tile's group end here (exclusive)
+    int32_t sf_tile0;  // 128-row SF tile of the pair's first row (CTA r adds r)
+    int32_t n0;
+    int32_t group;
+};
+
+template <int FMT, bool GROUPED>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const GemmParams p)
+{
+    using C = PairCfg<FMT>;
+    constexpr int SAB = C::AB_STAGES, SSF = C::SF_STAGES;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *full = bars;                       // leader: A/B bytes of both CTAs and the
+                                                 // scale slot written by both CTAs
+    uint64_t *empty = full + SAB;                // A/B stage and its tensor-memory scale slot
+                                                 // free again (MMA commit, both CTAs)
+    uint64_t *sf_full = empty + SAB;             // local: scale bytes landed
+    uint64_t *sf_empty = sf_full + SSF;          // local: scale warps done reading
+    uint64_t *acc_full = sf_empty + SSF;
+    uint64_t *acc_empty = acc_full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::NBAR);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    __shared__ int32_t s_offs[GROUPED ? kMaxGroups + 1 : 1];
+    __shared__ int32_t s_ptile[GROUPED ? kMaxGroups + 1 : 1];   // prefix of pair tiles
+    __shared__ int32_t s_sftile[GROUPED ? kMaxGroups + 1 : 1];  // prefix of 128-row SF tiles
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int K = p.K;
+    const int kblocks = (K + 255) / 256;
+    const int kc = (K / C::G) / 4;
+    const int ntiles_n = p.N / 256;
+    const int32_t pair_id = blockIdx.x >> 1;
+    const int32_t npairs = gridDim.x >> 1;
+
+    int32_t total_tiles;
+    if (GROUPED) {
+        for (int i = threadIdx.x; i <= p.groups; i += blockDim.x) s_offs[i] = p.row_offsets[i];
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int32_t pt = 0, st = 0;
+            for (int e = 0; e < p.groups; ++e) {
+                s_ptile[e] = pt;
+                s_sftile[e] = st;
+                const int32_t rows = s_offs[e + 1] - s_offs[e];
+                pt += rows > 0 ? (rows + 255) / 256 : 0;
+                st += rows > 0 ? (rows + 127) / 128 : 0;
+            }
+            s_ptile[p.groups] = pt;
+            s_sftile[p.groups] = st;
+        }
+        __syncthreads();
+        total_tiles = s_ptile[p.groups] * ntiles_n;
+    } else {
+        total_tiles = ((p.M + 255) / 256) * ntiles_n;
+    }
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SAB; ++s) {
+            mbar_init(smem_u32(&full[s]), 1 + 8);   // producer (with the bytes) + 4 scale warps x 2 CTAs
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int s = 0; s < SSF; ++s) {
+            mbar_init(smem_u32(&sf_full[s]), 1);
+            mbar_init(smem_u32(&sf_empty[s]), 4);
+        }
+        mbar_init(smem_u32(acc_full), 1);
+        mbar_init(smem_u32(acc_empty), 2 * 8);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    auto tile_info = [&](int32_t t) {
+        PairTile ti;
+        const int32_t nt = t % ntiles_n;
+        ti.n0 = nt * 256;
+        if (GROUPED) {
+            const int32_t mt_all = t / ntiles_n;
+            int lo = 0, hi = p.groups - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_ptile[mid] <= mt_all) lo = mid; else hi = mid - 1;
+            }
+            const int32_t mt = mt_all - s_ptile[lo];
+            ti.group = lo;
+            ti.row0 = s_offs[lo] + mt * 256;
+            ti.row_end = s_offs[lo + 1];
+            ti.sf_tile0 = s_sftile[lo] + 2 * mt;
+        } else {
+            const int32_t mtiles = (p.M + 255) / 256;
+            constexpr int32_t GM = 8;
+            const int32_t per_group = GM * ntiles_n;
+            const int32_t grp = t / per_group;
+            const int32_t first_m = grp * GM;
+            const int32_t rows_here = min(GM, mtiles - first_m);
+            const int32_t idx = t % per_group;
+            const int32_t mt = first_m + idx % rows_here;
+            ti.n0 = (idx / rows_here) * 256;
+            ti.row0 = mt * 256;
+            ti.row_end = p.M;
+            ti.sf_tile0 = 2 * mt;
+            ti.group = 0;
+        }
+        return ti;
+    };
+
+    // j counts K-blocks over all tiles this pair processes; every ring slot
+    // and phase parity is derived from it.
+    if (warp == 0) {
+        // ------------------------------------------------ A/B TMA producer (both CTAs)
+        if (lane == 0) {
+            const uint32_t full0_leader = mapa_shared(smem_u32(&full[0]), 0);
+            uint32_t j = 0;
+            bool ok = true;
+            for (int32_t t = pair_id; t < total_tiles && ok; t += npairs) {
+                const PairTile ti = tile_info(t);
+                const int32_t arow = ti.row0 + 128 * static_cast<int32_t>(rank);
+                const int32_t brow = (GROUPED ? ti.group * p.N : 0) + ti.n0 + 128 * static_cast<int32_t>(rank);
+                for (int kb = 0; kb < kblocks; ++kb, ++j) {
+                    const uint32_t s = j % SAB;
+                    if (!mbar_wait(smem_u32(&empty[s]), ((j / SAB) & 1) ^ 1)) { ok = false; break; }
+                    if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * C::AB_BYTES);
+                    const uint32_t dst = smem_u32(smem + s * C::AB_BYTES);
+                    const uint32_t fb = full0_leader + s * 8;
+                    tma_load_2d_pair(dst, &tmA, fb, kb * 128, arow);
+                    tma_load_2d_pair(dst + C::A_BYTES, &tmB, fb, kb * 128, brow);
+                }
+            }
+            if (!ok) { record_timeout(); *abort_flag = 1; }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------ scale-factor TMA producer (both CTAs)
+        if (lane == 0) {
+            uint32_t j = 0;
+            bool ok = true;
+            for (int32_t t = pair_id; t < total_tiles && ok; t += npairs) {
+                const PairTile ti = tile_info(t);
+                const bool a_valid = ti.row0 + 128 * static_cast<int32_t>(rank) < ti.row_end;
+                const int32_t bpair = (GROUPED ? ti.group * p.N : 0) + ti.n0;
+                const uint8_t *sfa_g = p.A_sf + static_cast<size_t>(ti.sf_tile0 + rank) * kc * 512;
+                const uint8_t *sfb_g = p.B_sf + static_cast<size_t>(bpair / 128) * kc * 512;
+                for (int kb = 0; kb < kblocks; ++kb, ++j) {
+                    const uint32_t s = j % SSF;
+                    if (!mbar_wait(smem_u32(&sf_empty[s]), ((j / SSF) & 1) ^ 1)) { ok = false; break; }
+                    const int chunks = min(C::CPS, kc - kb * C::CPS);
+                    const uint32_t bar = smem_u32(&sf_full[s]);
+                    mbar_arrive_expect_tx(bar, (a_valid ? 3 : 2) * chunks * 512);
+                    const uint32_t dst = smem_u32(smem + C::OFF_SF + s * C::SF_BYTES);
+                    const size_t koff = static_cast<size_t>(kb) * C::CPS * 512;
+                    if (a_valid) bulk_load(dst, sfa_g + koff, chunks * 512, bar);
+                    bulk_load(dst + C::SFA_BYTES, sfb_g + koff, chunks * 512, bar);
+                    bulk_load(dst + C::SFA_BYTES + C::CPS * 512, sfb_g + static_cast<size_t>(kc) * 512 + koff,
+                              chunks * 512, bar);
+                }
+            }
+            if (!ok) { record_timeout(); *abort_flag = 1; }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (leader)
+        // The per-K-block loop is kept short: descriptors are formed once per
+        // stage (the K=64 steps inside a 128-byte swizzled row advance the
+        // start address by 32 bytes, i.e. +2 in the descriptor) and the ring
+        // position is stepped instead of divided out.
+        if (rank == 0 && lane == 0) {
+            const uint64_t a_desc0 = smem_desc(smem_u32(smem), 16, 1024, kSwizzle128B);
+            const uint64_t b_desc0 = smem_desc(smem_u32(smem) + C::A_BYTES, 16, 1024, kSwizzle128B);
+            constexpr uint64_t kStageDesc = static_cast<uint64_t>(C::AB_BYTES >> 4);
+            const uint32_t sf0 = tmem_base + C::COL_SF;
+            uint32_t s = 0, phase = 0, acc_phase = 0;
+            bool ok = true;
+            const int full_kblocks = K / 256;                  // K-blocks with all four K=64 steps
+            for (int32_t t = pair_id; t < total_tiles && ok; t += npairs) {
+                if (!mbar_wait(smem_u32(acc_empty), acc_phase ^ 1)) { ok = false; break; }
+                tc_fence_after();
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait(smem_u32(&full[s]), phase)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t ad = a_desc0 + s * kStageDesc;
+                    const uint64_t bd = b_desc0 + s * kStageDesc;
+                    const uint32_t sfa_t = sf0 + s * C::SLOT_COLS;
+                    const uint32_t sfb_t = sfa_t + C::SFA_COLS;
+                    const uint32_t acc0 = kb > 0 ? 1u : 0u;
+                    if (kb < full_kblocks) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            if (FMT == QFP4_NVFP4) {
+                                constexpr uint32_t id = idesc_block_scaled(256, 256, false, 0, 0);
+                                tc_mma_nvf4_pair(tmem_base, ad + 2 * kk, bd + 2 * kk, id, sfa_t + kk * 4,
+                                                 sfb_t + kk * 8, kk > 0 ? 1u : acc0);
+                            } else {
+                                constexpr uint32_t id0 = idesc_block_scaled(256, 256, true, 0, 0);
+                                constexpr uint32_t id1 = idesc_block_scaled(256, 256, true, 2, 2);
+                                tc_mma_mxf4_pair(tmem_base, ad + 2 * kk, bd + 2 * kk, (kk & 1) ? id1 : id0,
+                                                 sfa_t + (kk >> 1) * 4, sfb_t + (kk >> 1) * 8, kk > 0 ? 1u : acc0);
+                            }
+                        }
+                    } else {
+                        // trailing half K-block (K % 256 == 128): two K=64 steps
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            if (FMT == QFP4_NVFP4) {
+                                constexpr uint32_t id = idesc_block_scaled(256, 256, false, 0, 0);
+                                tc_mma_nvf4_pair(tmem_base, ad + 2 * kk, bd + 2 * kk, id, sfa_t + kk * 4,
+                                                 sfb_t + kk * 8, kk > 0 ? 1u : acc0);
+                            } else {
+                                constexpr uint32_t id0 = idesc_block_scaled(256, 256, true, 0, 0);
+                                constexpr uint32_t id1 = idesc_block_scaled(256, 256, true, 2, 2);
+                                tc_mma_mxf4_pair(tmem_base, ad + 2 * kk, bd + 2 * kk, (kk & 1) ? id1 : id0,
+                                                 sfa_t, sfb_t, kk > 0 ? 1u : acc0);
+                            }
+                        }
+                    }
+                    tc_commit_pair(smem_u32(&empty[s]), 0x3);
+                    if (++s == SAB) { s = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc_commit_pair(smem_u32(acc_full), 0x3);
+                acc_phase ^= 1;
+            }
+            if (!ok) { record_timeout(); *abort_flag = 1; }
+        }
+    } else if (warp >= 4 && warp < 12) {
+        // ------------------------------------------------ scale-factor warps
+        // Tensor-memory layout of one 512-byte tile at columns [c, c+4):
+        // lane 32q + i, column c + j holds the four scale bytes of row
+        // i + 32 j.  Each 32-lane quarter q of the MMA reads its own rows'
+        // scales of A from column c + q only, but needs all 128 rows of B's
+        // tile, so B's tiles are written in full and A's word q everywhere.
+        // Two sets of four warps take alternate K-blocks.
+        const int quad = warp & 3;
+        const uint32_t set = static_cast<uint32_t>((warp - 4) >> 2);
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t ready0_leader = mapa_shared(smem_u32(&full[0]), 0);
+        uint32_t j = 0;
+        bool ok = true;
+        for (int32_t t = pair_id; t < total_tiles && ok; t += npairs) {
+            for (int kb = 0; kb < kblocks; ++kb, ++j) {
+                if ((j & 1) != set) continue;
+                const uint32_t s = j % SSF, slot = j % SAB;
+                int got = __shfl_sync(0xffffffffu,
+                                      lane == 0 ? (mbar_wait(smem_u32(&sf_full[s]), (j / SSF) & 1) ? 1 : 0) : 0, 0);
+                if (!got) { ok = false; break; }
+                const uint8_t *sf_s = smem + C::OFF_SF + s * C::SF_BYTES;
+                uint32_t va[C::SFA_COLS];
+                uint32_t vb[C::SFB_COLS];
+#pragma unroll
+                for (int c = 0; c < C::CPS; ++c) {
+                    const uint4 a4 = *reinterpret_cast<const uint4 *>(sf_s + c * 512 + lane * 16);
+                    const uint32_t w = quad == 0 ? a4.x : quad == 1 ? a4.y : quad == 2 ? a4.z : a4.w;
+                    va[4 * c + 0] = w; va[4 * c + 1] = w; va[4 * c + 2] = w; va[4 * c + 3] = w;
+                    const uint4 b0 = *reinterpret_cast<const uint4 *>(sf_s + C::SFA_BYTES + c * 512 + lane * 16);
+                    const uint4 b1 = *reinterpret_cast<const uint4 *>(sf_s + C::SFA_BYTES + (C::CPS + c) * 512 + lane * 16);
+                    vb[8 * c + 0] = b0.x; vb[8 * c + 1] = b0.y; vb[8 * c + 2] = b0.z; vb[8 * c + 3] = b0.w;
+                    vb[8 * c + 4] = b1.x; vb[8 * c + 5] = b1.y; vb[8 * c + 6] = b1.z; vb[8 * c + 7] = b1.w;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sf_empty[s]));
+                got = __shfl_sync(0xffffffffu,
+                                  lane == 0 ? (mbar_wait(smem_u32(&empty[slot]), ((j / SAB) & 1) ^ 1) ? 1 : 0) : 0, 0);
+                if (!got) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t col = tmem_base + C::COL_SF + slot * C::SLOT_COLS;
+                tmem_st_32x32b<C::SFA_COLS>(lane_base + col, va);
+                tmem_st_32x32b<C::SFB_COLS>(lane_base + col + C::SFA_COLS, vb);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster_relaxed(ready0_leader + slot * 8);
+            }
+        }
+        if (!ok && lane == 0) { record_timeout(); *abort_flag = 1; }
+    } else if (warp >= 12) {
+        // ------------------------------------------------ epilogue
+        const int quad = warp & 3;
+        const int half = (warp - 12) >> 2;
+        const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int32_t t = pair_id; t < total_tiles; t += npairs) {
+            const PairTile ti = tile_info(t);
+            const int got = __shfl_sync(0xffffffffu,
+                                        lane == 0 ? (mbar_wait(smem_u32(acc_full), acc_phase) ? 1 : 0) : 0, 0);
+            if (!got) { ok = false; break; }
+            tc_fence_after();
+            float gs = 1.0f;
+            if (FMT == QFP4_NVFP4) {
+                const int g = GROUPED ? ti.group : 0;
+                const float ga = p.gs_a ? p.gs_a[g] : 1.0f;
+                const float gb = p.gs_b ? p.gs_b[g] : 1.0f;
+                gs = ga * gb;
+            }
+            const int32_t row = ti.row0 + 128 * static_cast<int32_t>(rank) + quad * 32 + lane;
+            const bool row_ok = row < ti.row_end;
+            __nv_bfloat16 *dst = p.D + static_cast<size_t>(row_ok ? row : 0) * p.N + ti.n0 + half * 128;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + half * 128;
+            // Drain 128 columns in two halves of 64: each 32-column chunk is
+            // scaled and rounded to BF16 pairs as it arrives and stored.
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t packed[2][16];
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr + (2 * h + jj) * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * gs,
+                                                                  __uint_as_float(v[2 * i + 1]) * gs);
+                        packed[jj][i] = *reinterpret_cast<uint32_t *>(&pr);
+                    }
+                }
+                if (h == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
+                }
+                if (row_ok) {
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        __nv_bfloat16 *d = dst + (2 * h + jj) * 32;
+                        const uint32_t(&q)[16] = packed[jj];
+                        st_global_v8(d, *reinterpret_cast<const uint32_t(*)[8]>(&q[0]));
+                        st_global_v8(d + 16, *reinterpret_cast<const uint32_t(*)[8]>(&q[8]));
+                    }
+                }
+            }
+            acc_phase ^= 1;
+        }
+        if (!ok && lane == 0) { record_timeout(); *abort_flag = 1; }
+    }
+
+    // ---- teardown
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    if (*abort_flag) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) { }
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, 512);
+    }
+}
+
+template <int FMT, bool GROUPED>
+int launch(const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &prm, int64_t pair_tiles,
+           cudaStream_t s)
+{
+    using C = PairCfg<FMT>;
+    auto kern = gemm_pair_kernel<FMT, GROUPED>;
+    static int configured_device = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QFP4_ERR_CUDA;
+    if (configured_device != dev) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+            return QFP4_ERR_CUDA;
+        configured_device = dev;
+    }
+    const int sms = sm_count();
+    if (sms < 2) return QFP4_ERR_CUDA;
+    int64_t pairs = sms / 2;
+    if (pair_tiles < pairs) pairs = pair_tiles > 0 ? pair_tiles : 1;
+    kern<<<static_cast<int>(2 * pairs), kThreads, C::SMEM, s>>>(ma, mb, prm);
+    return launch_status(cudaGetLastError());
+}
+
+}  // namespace
+
+int launch_gemm_pair(int fmt, bool grouped, const CUtensorMap &ma, const CUtensorMap &mb,
+                     const GemmParams &prm, int64_t pair_tiles, cudaStream_t s)
+{
+    if (fmt == QFP4_NVFP4)
+        return grouped ? launch<QFP4_NVFP4, true>(ma, mb, prm, pair_tiles, s)
+                       : launch<QFP4_NVFP4, false>(ma, mb, prm, pair_tiles, s);
+    return grouped ? launch<QFP4_MXFP4, true>(ma, mb, prm, pair_tiles, s)
+                   : launch<QFP4_MXFP4, false>(ma, mb, prm, pair_tiles, s);
+}
+
+}  // namespace qfp4

@@ -32,8 +32,9 @@ def one_sf(fmt):
 # ----------------------------------------------------------------- probes
 
 @pytest.mark.parametrize("fmt", [MX, NV])
-def test_all_ones_closed_form(fmt):
-    M, N, K = 128, 256, 512
+@pytest.mark.parametrize("M", [128, 256, 384])
+def test_all_ones_closed_form(fmt, M):
+    N, K = 256, 512
     g = qfp4.block_size(fmt)
     A, B = pack(np.full((M, K), 2)), pack(np.full((N, K), 2))
     sa, sb = (126, 129) if fmt == MX else (0x30, 0x40)
@@ -45,10 +46,12 @@ def test_all_ones_closed_form(fmt):
 
 
 @pytest.mark.parametrize("fmt", [MX, NV])
-def test_one_hot_elements(fmt):
+@pytest.mark.parametrize("M", [128, 256])
+def test_one_hot_elements(fmt, M):
     """Single non-zero FP4 element per A row at a distinct k: pins the nibble
-    order and the K position inside the 128-byte swizzled rows."""
-    M, N, K = 128, 256, 512
+    order and the K position inside the 128-byte swizzled rows (single-CTA
+    tiles at M = 128, CTA-pair tiles at M = 256)."""
+    N, K = 256, 512
     g = qfp4.block_size(fmt)
     codes = np.zeros((M, K), np.uint8)
     ks = (np.arange(M) * 37) % K
@@ -56,7 +59,7 @@ def test_one_hot_elements(fmt):
     A = pack(codes)
     bc = np.zeros((N, K), np.uint8)
     bc[:, :] = (np.arange(K)[None, :] % 7) + 1           # distinct per k
-    bc[:, :] += (np.arange(N)[:, None] % 2) * 8          # sign alternates per n
+    bc[:, :] += ((np.arange(N)[:, None] % 2) * 8).astype(np.uint8)   # sign alternates per n
     B = pack(bc)
     Asf = np.full((M, K // g), one_sf(fmt), np.uint8)
     Bsf = np.full((N, K // g), one_sf(fmt), np.uint8)
@@ -66,10 +69,11 @@ def test_one_hot_elements(fmt):
 
 
 @pytest.mark.parametrize("fmt", [MX, NV])
-def test_one_hot_scales(fmt):
+@pytest.mark.parametrize("M", [128, 256])
+def test_one_hot_scales(fmt, M):
     """All elements 1.0; A's scale bytes distinct per (row, block) and B's per
     (column, block): pins the scale-factor layout in tensor memory."""
-    M, N, K = 128, 256, 1024
+    N, K = 256, 1024
     g = qfp4.block_size(fmt)
     kg = K // g
     A, B = pack(np.full((M, K), 2)), pack(np.full((N, K), 2))

@@ -1,5 +1,7 @@
 // quantize.cu -- BF16 -> NVFP4 / MXFP4 quantiser, global scale and the
-// scale-factor interleave (HBM-bound kernels, no tensor cores).
+// scale-factor interleave (HBM-bound kernels, no tensor cores).  The
+// quantiser streams its input through shared memory with bulk copies (TMA
+// engine) so that enough bytes are in flight per SM to keep HBM busy.
 //
 // Pages: Mojo "fp4_quantization" module, "Functions"
 // (quantize_dynamic_scaled_fp4fp8, grouped_quantize_dynamic_scaled_fp4_async,
@@ -22,6 +24,7 @@
 #include <cuda_runtime.h>
 
 #include "qfp4_common.cuh"
+#include "sm103_ptx.cuh"
 
 namespace qfp4 {
 
@@ -114,18 +117,46 @@ struct BlockScale {
     int mode;       // 0: zero block, 1: fast path, 2: IEEE division
 };
 
+// RN(a / b) from y = RN(1 / b) with two fused corrections (Markstein); the
+// caller guarantees a, b and the quotient stay well inside the normal range.
+// The remainder is formed negated, e = b*q - a, and applied as q - e*y: the
+// same values, but a = -0 keeps its sign (-0 - (+0) = -0) where the
+// a - b*q form would turn it into +0.
+__device__ __forceinline__ float div_markstein(float a, float b, float y)
+{
+    float q = __fmul_rn(a, y);
+    q = __fmaf_rn(-__fmaf_rn(b, q, -a), y, q);
+    q = __fmaf_rn(-__fmaf_rn(b, q, -a), y, q);
+    return q;
+}
+
+__device__ __forceinline__ bool normal_range(float v) { return v >= 0x1p-100f && v <= 0x1p100f; }
+
+// t = (amax / 6) / gs, each division correctly rounded.  inv_gs = RN(1/gs).
+__device__ __forceinline__ float scale_target(float amax, float gs, float inv_gs)
+{
+    constexpr float kInv6 = 0x1.555556p-3f;          // RN(1/6)
+    if (normal_range(amax)) {
+        const float t1 = div_markstein(amax, 6.0f, kInv6);
+        if (gs == 1.0f) return t1;
+        if (normal_range(t1) && gs >= 0x1p-60f && gs <= 0x1p60f) return div_markstein(t1, gs, inv_gs);
+        return __fdiv_rn(t1, gs);
+    }
+    return gs == 1.0f ? __fdiv_rn(amax, 6.0f) : __fdiv_rn(__fdiv_rn(amax, 6.0f), gs);
+}
+
 template <int FMT>
-__device__ __forceinline__ BlockScale block_scale(float amax, float gs)
+__device__ __forceinline__ BlockScale block_scale(float amax, float gs, float inv_gs)
 {
     BlockScale b;
     if (FMT == QFP4_MXFP4) {
-        const float t = __fdiv_rn(amax, 6.0f);
+        const float t = scale_target(amax, 1.0f, 1.0f);
         b.code = ue8m0_encode(t);
         b.inv = ue8m0_inverse(b.code);
         b.s = 0.0f;
         b.mode = 1;
     } else {
-        const float t = __fdiv_rn(__fdiv_rn(amax, 6.0f), gs);
+        const float t = scale_target(amax, gs, inv_gs);
         b.code = ue4m3_encode(t);
         b.s = __fmul_rn(ue4m3_decode(b.code), gs);
         if (b.s == 0.0f) {
@@ -144,13 +175,23 @@ template <int FMT>
 __device__ __forceinline__ float quotient(float x, const BlockScale &b)
 {
     if (FMT == QFP4_MXFP4) return x * b.inv;
-    if (b.mode == 1) {
-        float q = __fmul_rn(x, b.inv);
-        q = __fmaf_rn(__fmaf_rn(-b.s, q, x), b.inv, q);
-        q = __fmaf_rn(__fmaf_rn(-b.s, q, x), b.inv, q);
-        return copysignf(q, x);
-    }
+    if (b.mode == 1) return div_markstein(x, b.s, b.inv);
     return __fdiv_rn(x, b.s);
+}
+
+// Eight fp32 -> four packed bytes: element 2i in the low nibble of byte i.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&q)[8])
+{
+    uint32_t w;
+    asm("{\n.reg .b8 b0, b1, b2, b3;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+        "mov.b32 %0, {b0, b1, b2, b3};\n}"
+        : "=r"(w)
+        : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+    return w;
 }
 
 // 8 consecutive elements -> 4 packed bytes.
@@ -158,14 +199,10 @@ template <int FMT>
 __device__ __forceinline__ uint32_t encode8(const float (&x)[8], const BlockScale &b)
 {
     if (FMT == QFP4_NVFP4 && b.mode == 0) return 0u;
-    uint32_t w = 0;
+    float q[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float q0 = quotient<FMT>(x[2 * i], b);
-        const float q1 = quotient<FMT>(x[2 * i + 1], b);
-        w |= e2m1x2(q1, q0) << (8 * i);
-    }
-    return w;
+    for (int i = 0; i < 8; ++i) q[i] = quotient<FMT>(x[i], b);
+    return e2m1x8(q);
 }
 
 __device__ __forceinline__ int64_t sf_mma_offset(int64_t row_tile, int64_t r_in_tile, int64_t c,
@@ -186,36 +223,57 @@ __device__ __forceinline__ int find_group(const int32_t *offs, int groups, int64
     return lo;
 }
 
-// One pass over X in chunks of 8 elements (16 bytes); TPB = g/8 consecutive
-// lanes share one scale block.  GROUPED: per-row global scale gs[group] and
-// SF written in the per-group MMA layout.
+constexpr int kQStages = 4;
+
+// BF16 bytes per pipeline stage: one scale block per thread (8 KB NVFP4,
+// 16 KB MXFP4), small enough for four CTAs per SM.
+template <int FMT>
+__host__ __device__ constexpr int chunk_bytes() { return kThreads * 2 * (FMT == QFP4_MXFP4 ? 32 : 16); }
+
+// Persistent quantiser fed by bulk copies: each CTA walks 16 KB chunks of the
+// flat BF16 input (rows are contiguous, and a chunk holds whole scale
+// blocks), one thread keeps kQStages chunks in flight through mbarriers, and
+// every thread encodes whole scale blocks from shared memory.  GROUPED:
+// per-row global scale gs[group] and the per-group MMA scale layout.
 template <int FMT, int SF_LAYOUT, bool GROUPED>
-__global__ void __launch_bounds__(kThreads)
-quantize_kernel(const uint4 *__restrict__ X, int64_t total_chunks, int64_t K,
-                const float *__restrict__ gs_ptr, uint32_t *__restrict__ Q,
+__global__ void __launch_bounds__(kThreads, 4)
+quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
+                const float *__restrict__ gs_ptr, uint8_t *__restrict__ Q,
                 uint8_t *__restrict__ SF, int64_t M, int groups,
                 const int32_t *__restrict__ row_offsets)
 {
     constexpr int G = FMT == QFP4_MXFP4 ? 32 : 16;
-    constexpr int TPB = G / 8;
-    constexpr int U = 4;
+    constexpr int kChunkBytes = chunk_bytes<FMT>();
+    constexpr int BPC = kChunkBytes / (2 * G);          // scale blocks per chunk
+    constexpr int BPT = BPC / kThreads;                 // per thread per chunk
+    static_assert(BPC % kThreads == 0 && BPT >= 1, "chunk / thread mismatch");
     const int64_t kg = K / G, kc = kg / 4;
-    const int64_t chunks_per_row = K / 8;
+    extern __shared__ __align__(128) uint8_t qsmem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(qsmem + kQStages * kChunkBytes);
+    uint64_t *empty = full + kQStages;
     __shared__ int32_t s_offs[GROUPED ? kMaxGroups + 1 : 1];
     __shared__ int32_t s_tile0[GROUPED ? kMaxGroups : 1];
     if (GROUPED) {
         for (int i = threadIdx.x; i <= groups; i += blockDim.x) s_offs[i] = row_offsets[i];
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int32_t acc = 0;
-            for (int e = 0; e < groups; ++e) {
-                s_tile0[e] = acc;
-                acc += (s_offs[e + 1] - s_offs[e] + 127) / 128;
-            }
-        }
-        __syncthreads();
     }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kQStages; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), kThreads / 32);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (GROUPED && threadIdx.x == 0) {
+        int32_t acc = 0;
+        for (int e = 0; e < groups; ++e) {
+            s_tile0[e] = acc;
+            acc += (s_offs[e + 1] - s_offs[e] + 127) / 128;
+        }
+    }
+    __syncthreads();
     const float gs_one = (FMT == QFP4_MXFP4 || GROUPED) ? 1.0f : *gs_ptr;
+    const float inv_gs_one = __frcp_rn(gs_one);
 
     // MMA layout without groups: zero the padding rows [M, ceil128(M)).
     if (SF_LAYOUT == QFP4_SF_MMA && !GROUPED) {
@@ -228,54 +286,85 @@ quantize_kernel(const uint4 *__restrict__ X, int64_t total_chunks, int64_t K,
         }
     }
 
+    const int64_t total_bytes = total_blocks * (2 * G);
+    const int64_t nchunks = (total_bytes + kChunkBytes - 1) / kChunkBytes;
     const int lane = threadIdx.x & 31;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    const int64_t first = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-    // Loop bounds are warp-uniform so that every lane joins the shuffles.
-    const int64_t warp_first = first - lane;
-    for (int64_t base = warp_first; base < total_chunks; base += stride * U) {
-        uint4 v[U];
+    bool ok = true;
+
+    // producer: thread 0 issues the first kQStages chunks, then one chunk
+    // per consumed chunk (after the stage's empty barrier completes)
+    auto issue = [&](int64_t c, uint32_t it) {
+        const uint32_t st = it % kQStages;
+        const int64_t off = c * kChunkBytes;
+        const int64_t rem = total_bytes - off;
+        const uint32_t bytes = static_cast<uint32_t>(rem < kChunkBytes ? rem : kChunkBytes);
+        mbar_arrive_expect_tx(smem_u32(&full[st]), bytes);
+        bulk_load(smem_u32(qsmem + st * kChunkBytes), X + off, bytes, smem_u32(&full[st]));
+    };
+    if (threadIdx.x == 0) {
+        uint32_t it = 0;
+        for (int64_t c = blockIdx.x; c < nchunks && it < kQStages; c += gridDim.x, ++it) issue(c, it);
+    }
+    uint32_t it = 0;
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++it) {
+        const uint32_t st = it % kQStages;
+        const uint32_t ph = (it / kQStages) & 1;
+        if (!mbar_wait(smem_u32(&full[st]), ph)) { ok = false; break; }
+        const uint8_t *chunk = qsmem + st * kChunkBytes;
+        const int64_t b0 = c * BPC;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t c = base + u * stride + lane;
-            v[u] = c < total_chunks ? ld_stream_v4(X + c) : make_uint4(0, 0, 0, 0);
-        }
+        for (int u = 0; u < BPT; ++u) {
+            const int local = u * kThreads + threadIdx.x;   // consecutive threads, consecutive blocks
+            const int64_t bu = b0 + local;
+            const bool valid = bu < total_blocks;
+            float x[G];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t c = base + u * stride + lane;
-            const bool valid = c < total_chunks;
-            float x[8];
-            bf16x2_to_f32(v[u].x, x[0], x[1]);
-            bf16x2_to_f32(v[u].y, x[2], x[3]);
-            bf16x2_to_f32(v[u].z, x[4], x[5]);
-            bf16x2_to_f32(v[u].w, x[6], x[7]);
+            for (int h = 0; h < G / 16; ++h) {
+                const uint4 v0 = *reinterpret_cast<const uint4 *>(chunk + local * (2 * G) + h * 32);
+                const uint4 v1 = *reinterpret_cast<const uint4 *>(chunk + local * (2 * G) + h * 32 + 16);
+                bf16x2_to_f32(v0.x, x[16 * h + 0], x[16 * h + 1]);
+                bf16x2_to_f32(v0.y, x[16 * h + 2], x[16 * h + 3]);
+                bf16x2_to_f32(v0.z, x[16 * h + 4], x[16 * h + 5]);
+                bf16x2_to_f32(v0.w, x[16 * h + 6], x[16 * h + 7]);
+                bf16x2_to_f32(v1.x, x[16 * h + 8], x[16 * h + 9]);
+                bf16x2_to_f32(v1.y, x[16 * h + 10], x[16 * h + 11]);
+                bf16x2_to_f32(v1.z, x[16 * h + 12], x[16 * h + 13]);
+                bf16x2_to_f32(v1.w, x[16 * h + 14], x[16 * h + 15]);
+            }
             float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-            if (TPB == 4) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-
-            const int64_t row = c / chunks_per_row;
+            for (int i = 0; i < G; ++i) amax = fmaxf(amax, fabsf(x[i]));
             int grp = 0;
-            float gs = gs_one;
+            float gs = gs_one, inv_gs = inv_gs_one;
             if (GROUPED && valid) {
+                const int64_t row = static_cast<uint32_t>(bu) / static_cast<uint32_t>(kg);
                 grp = find_group(s_offs, groups, row);
-                gs = gs_ptr ? gs_ptr[grp] : 1.0f;
-                if (FMT == QFP4_MXFP4) gs = 1.0f;
+                if (FMT == QFP4_NVFP4 && gs_ptr) {
+                    gs = gs_ptr[grp];
+                    inv_gs = __frcp_rn(gs);
+                }
             }
-            const BlockScale b = block_scale<FMT>(amax, gs);
-            const uint32_t word = encode8<FMT>(x, b);
-            if (valid) Q[c] = word;
-
-            // Scale bytes: lanes 0, TPB, 2TPB, 3TPB hold four consecutive
-            // blocks of one row; the first of them stores the 4-byte word.
-            const uint32_t b1 = __shfl_down_sync(0xffffffffu, b.code, TPB);
-            const uint32_t b2 = __shfl_down_sync(0xffffffffu, b.code, 2 * TPB);
-            const uint32_t b3 = __shfl_down_sync(0xffffffffu, b.code, 3 * TPB);
-            if (valid && (lane % (4 * TPB)) == 0) {
-                const uint32_t sfw = b.code | (b1 << 8) | (b2 << 16) | (b3 << 24);
-                const int64_t blk = c / TPB;                 // flat block index
-                const int64_t col = blk % kg;
+            const BlockScale bs = block_scale<FMT>(amax, gs, inv_gs);
+            uint32_t packed[G / 8];
+#pragma unroll
+            for (int w = 0; w < G / 8; ++w) {
+                float xx[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) xx[i] = x[8 * w + i];
+                packed[w] = encode8<FMT>(xx, bs);
+            }
+            if (valid) {
+                if (G == 16) *reinterpret_cast<uint2 *>(Q + bu * (G / 2)) = make_uint2(packed[0], packed[1]);
+                else *reinterpret_cast<uint4 *>(Q + bu * (G / 2)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            }
+            // Scale bytes: lanes 4i..4i+3 hold four consecutive blocks of one row.
+            const uint32_t c1 = __shfl_down_sync(0xffffffffu, bs.code, 1);
+            const uint32_t c2 = __shfl_down_sync(0xffffffffu, bs.code, 2);
+            const uint32_t c3 = __shfl_down_sync(0xffffffffu, bs.code, 3);
+            if (valid && (lane & 3) == 0) {
+                const uint32_t word = bs.code | (c1 << 8) | (c2 << 16) | (c3 << 24);
+                const uint32_t row = static_cast<uint32_t>(bu) / static_cast<uint32_t>(kg);
+                const uint32_t col = static_cast<uint32_t>(bu) - row * static_cast<uint32_t>(kg);
                 int64_t off;
                 if (GROUPED) {
                     const int64_t rr = row - s_offs[grp];
@@ -283,11 +372,27 @@ quantize_kernel(const uint4 *__restrict__ X, int64_t total_chunks, int64_t K,
                 } else if (SF_LAYOUT == QFP4_SF_MMA) {
                     off = sf_mma_offset(row / 128, row % 128, col, kc);
                 } else {
-                    off = blk;
+                    off = bu;
                 }
-                *reinterpret_cast<uint32_t *>(SF + off) = sfw;
+                *reinterpret_cast<uint32_t *>(SF + off) = word;
             }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
+        if (threadIdx.x == 0) {
+            const int64_t cn = c + static_cast<int64_t>(kQStages) * gridDim.x;
+            if (cn < nchunks) {
+                if (!mbar_wait(smem_u32(&empty[st]), ph)) { ok = false; break; }
+                issue(cn, it + kQStages);
+            }
+        }
+    }
+    if (!ok) atomicOr(&g_status_quant, static_cast<uint32_t>(kStatusTimeout));
+    // no bulk copy may be left in flight: every issued chunk was consumed,
+    // or (after a timeout) give outstanding copies time to land
+    if (!ok) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) { }
     }
 }
 
@@ -403,10 +508,25 @@ template <int FMT, int LAYOUT, bool GROUPED>
 cudaError_t launch_quantize(const void *X, int64_t M, int64_t K, const float *gs, void *Q,
                             void *SF, int groups, const int32_t *offs, cudaStream_t s)
 {
-    const int64_t chunks = M * (K / 8);
-    const int grid = grid_for(chunks, kThreads * 4);
-    quantize_kernel<FMT, LAYOUT, GROUPED><<<grid, kThreads, 0, s>>>(
-        static_cast<const uint4 *>(X), chunks, K, gs, static_cast<uint32_t *>(Q),
+    constexpr int G = FMT == QFP4_MXFP4 ? 32 : 16;
+    const int64_t blocks = M * (K / G);
+    constexpr int kChunkBytes = chunk_bytes<FMT>();
+    const int64_t chunks = (blocks * 2 * G + kChunkBytes - 1) / kChunkBytes;
+    constexpr int smem = kQStages * kChunkBytes + 2 * kQStages * 8;
+    auto kern = quantize_kernel<FMT, LAYOUT, GROUPED>;
+    static int configured_device = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorUnknown;
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    const int sms = sm_count();
+    int64_t grid = static_cast<int64_t>(sms > 0 ? sms : 148) * (FMT == QFP4_MXFP4 ? 3 : 4);
+    if (chunks < grid) grid = chunks > 0 ? chunks : 1;
+    kern<<<static_cast<int>(grid), kThreads, smem, s>>>(
+        static_cast<const uint8_t *>(X), blocks, K, gs, static_cast<uint8_t *>(Q),
         static_cast<uint8_t *>(SF), M, groups, offs);
     return cudaGetLastError();
 }
@@ -481,6 +601,7 @@ extern "C" int qfp4_quantize(int fmt, const void *X_bf16, int64_t M, int64_t K, 
     if (M < 0 || K < 0) return QFP4_ERR_INVALID_ARG;
     if (K % 128 != 0) return QFP4_ERR_UNSUPPORTED;
     if (M == 0 || K == 0) return QFP4_OK;
+    if (M * (K / 16) >= (int64_t{1} << 32)) return QFP4_ERR_UNSUPPORTED;   // 32-bit block index
     if (!X_bf16 || !Q_packed || !SF) return QFP4_ERR_INVALID_ARG;
     if (fmt == QFP4_NVFP4 && !gs) return QFP4_ERR_INVALID_ARG;
     if (!aligned16(X_bf16) || !aligned16(Q_packed) || !aligned4(SF) || (gs && !aligned4(gs)))
@@ -505,6 +626,7 @@ extern "C" int qfp4_quantize_grouped(int fmt, const void *X_bf16, int64_t total_
     if (fmt != QFP4_MXFP4 && fmt != QFP4_NVFP4) return QFP4_ERR_INVALID_ARG;
     if (total_rows < 0 || K < 0 || groups < 1 || !row_offsets) return QFP4_ERR_INVALID_ARG;
     if (groups > kMaxGroups || K % 128 != 0) return QFP4_ERR_UNSUPPORTED;
+    if (total_rows * (K / 16) >= (int64_t{1} << 32)) return QFP4_ERR_UNSUPPORTED;
     if (fmt == QFP4_NVFP4 && !gs) return QFP4_ERR_INVALID_ARG;
     if (!X_bf16 || !Q_packed || !SF_mma) return QFP4_ERR_INVALID_ARG;
     if (!aligned16(X_bf16) || !aligned16(Q_packed) || !aligned4(SF_mma) || !aligned4(row_offsets) ||

@@ -187,7 +187,7 @@ class Pipeline:
         self.D = torch.empty((M, N), dtype=torch.bfloat16, device=device)
         self.D_pinned = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
         self.ws_bytes = qfp4.gemm_workspace_bytes(fmt, M, N, K)
-        self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
         if with_weights:
             xw = synth.weights_bf16(case.seed + 1000, N, K)
             W = torch.from_numpy(xw.view(np.int16).copy()).view(torch.bfloat16).to(device)

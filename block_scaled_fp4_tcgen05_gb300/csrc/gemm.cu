@@ -308,6 +308,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 #pragma unroll
             for (int j = 0; j < NCH; ++j) tmem_ld_32x32b_x32(taddr + j * 32, v[j]);
             tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < NCH; ++j) tmem_regs_after_wait(v[j]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars[2 * STAGES + 1]));
@@ -343,7 +345,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         if (!ok && lane == 0) { record_timeout(); *abort_flag = 1; }
     }
 
-    // ---- teardown: all roles done (or timed out); free tensor memory
+    // ---- teardown: all roles done (or timed out); free tensor memory.
+    // Reconverge each warp first: lanes that skipped a single-lane role must
+    // not reach the block barrier ahead of their warp's working lane.
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (*abort_flag) {
@@ -424,7 +429,7 @@ using namespace qfp4;
 extern "C" size_t qfp4_gemm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K)
 {
     (void)fmt; (void)M; (void)N; (void)K;
-    return 0;
+    return 0;   // every kernel keeps its partial sums on chip
 }
 
 extern "C" int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K, const void *A_packed,
@@ -432,7 +437,6 @@ extern "C" int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K, const void
                             const float *gs_a, const float *gs_b, void *D_bf16, void *workspace,
                             size_t ws_bytes, void *stream)
 {
-    (void)workspace; (void)ws_bytes;
     if (fmt != QFP4_MXFP4 && fmt != QFP4_NVFP4) return QFP4_ERR_INVALID_ARG;
     if (M < 1 || N < 1 || K < 1) return QFP4_ERR_INVALID_ARG;
     if (!A_packed || !A_sf || !B_packed || !B_sf || !D_bf16) return QFP4_ERR_INVALID_ARG;
@@ -446,6 +450,14 @@ extern "C" int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K, const void
                  static_cast<__nv_bfloat16 *>(D_bf16), static_cast<int32_t>(M), static_cast<int32_t>(N),
                  static_cast<int32_t>(K), 0, nullptr};
     CUtensorMap ma, mb;
+    (void)workspace; (void)ws_bytes;
+    if (M <= 128) {
+        // decode shapes: 128-column tiles with K split over a CTA cluster
+        int rc = make_map(&ma, A_packed, K / 2, M, kBKBytes, 128);
+        if (rc == QFP4_OK) rc = make_map(&mb, B_packed, K / 2, N, kBKBytes, 128);
+        if (rc != QFP4_OK) return rc;
+        return launch_gemm_decode(fmt, ma, mb, a, s);
+    }
     if (N % 256 == 0 && M > 128) {
         // CTA pairs on 256 x 256 tiles
         int rc = make_map(&ma, A_packed, K / 2, M, kBKBytes, 128);

@@ -376,8 +376,6 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     vb[8 * c + 0] = b0.x; vb[8 * c + 1] = b0.y; vb[8 * c + 2] = b0.z; vb[8 * c + 3] = b0.w;
                     vb[8 * c + 4] = b1.x; vb[8 * c + 5] = b1.y; vb[8 * c + 6] = b1.z; vb[8 * c + 7] = b1.w;
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sf_empty[s]));
                 got = __shfl_sync(0xffffffffu,
                                   lane == 0 ? (mbar_wait(smem_u32(&empty[slot]), ((j / SAB) & 1) ^ 1) ? 1 : 0) : 0, 0);
                 if (!got) { ok = false; break; }
@@ -388,7 +386,15 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster_relaxed(ready0_leader + slot * 8);
+                // The shared-memory slot is handed back only now: the values
+                // have reached tensor memory, so no read of the slot can still
+                // be outstanding (the compiler is free to sink the loads above
+                // down to their use in tcgen05.st, past any earlier release,
+                // and a refill of the slot would then be read instead).
+                if (lane == 0) {
+                    mbar_arrive(smem_u32(&sf_empty[s]));
+                    mbar_arrive_cluster_relaxed(ready0_leader + slot * 8);
+                }
             }
         }
         if (!ok && lane == 0) { record_timeout(); *abort_flag = 1; }
@@ -426,6 +432,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(taddr + (2 * h + jj) * 32, v);
                     tmem_ld_wait();
+                    tmem_regs_after_wait(v);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * gs,
@@ -453,7 +460,10 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         if (!ok && lane == 0) { record_timeout(); *abort_flag = 1; }
     }
 
-    // ---- teardown
+    // ---- teardown.  Reconverge each warp first: lanes that skipped a
+    // single-lane role must not reach the block barrier ahead of their
+    // warp's working lane.
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();

@@ -31,4 +31,11 @@ int launch_gemm_pair(int fmt, bool grouped, const CUtensorMap &ma, const CUtenso
 
 int read_clear_status_gemm_pair(cudaStream_t s, uint32_t *out);
 
+// Decode GEMM for M <= 128 (N % 128 == 0): one CTA per (128-column tile, K
+// share), K shares of a tile reduced over a thread-block cluster.
+int decode_split(int64_t N, int64_t K);
+int launch_gemm_decode(int fmt, const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &g,
+                       cudaStream_t s);
+int read_clear_status_gemm_decode(cudaStream_t s, uint32_t *out);
+
 }  // namespace qfp4

@@ -191,6 +191,21 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Named barrier that also ANDs a predicate over the participating threads.
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t threads, bool pred)
+{
+    uint32_t out;
+    asm volatile(
+        "{\n.reg .pred P, Q;\n"
+        "setp.ne.u32 P, %3, 0;\n"
+        "bar.red.and.pred Q, %1, %2, P;\n"
+        "selp.u32 %0, 1, 0, Q;\n}\n"
+        : "=r"(out)
+        : "r"(id), "r"(threads), "r"(pred ? 1u : 0u)
+        : "memory");
+    return out != 0;
+}
+
 // ---------------------------------------------------------------- tensor memory
 
 // Allocate `ncols` TMEM columns (power of two, 32..512); whole warp executes.
@@ -285,6 +300,18 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 __device__ __forceinline__ void tmem_ld_wait()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// The registers a tcgen05.ld writes hold valid data only once tcgen05.wait::ld
+// has returned, but nothing in the load's or the wait's asm tells the compiler
+// so: it may schedule a first use of a destination register between the two.
+// Routing every destination register through an empty volatile asm placed
+// after the wait makes each later use depend on a definition that follows it.
+template <int N>
+__device__ __forceinline__ void tmem_regs_after_wait(uint32_t (&r)[N])
+{
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
 // ---------------------------------------------------------------- descriptors
@@ -486,6 +513,14 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&v)[8])
 {
     asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
                  "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+// Vector fp32 reduction into global memory (performed at L2, no return).
+__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d)
+{
+    asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
                  : "memory");
 }
 

@@ -166,9 +166,10 @@ int qfp4_sf_interleave(const void *SF_in, int64_t rows, int64_t cols, void *SF_o
 /* GEMM                                                                     */
 /* ---------------------------------------------------------------------- */
 
-/* Workspace bytes qfp4_gemm_nt needs for this shape (0 when the chosen
- * kernel needs none).  The split-K decode kernel keeps fp32 partial sums
- * and tile counters there. */
+/* Workspace bytes qfp4_gemm_nt uses for this shape.  Every kernel keeps its
+ * partial sums on chip (tensor memory, and distributed shared memory for
+ * split-K), so this is 0; the argument is kept so that a caller written
+ * against it needs no change if a future kernel uses scratch. */
 size_t qfp4_gemm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K);
 
 /* D[M,N] (BF16, row-major) = bf16_rne(gs_a * gs_b * sum_k a[m,k] * b[n,k]),
@@ -177,11 +178,14 @@ size_t qfp4_gemm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K);
  *   A_packed  [M, K/2] bytes, K-major;  A_sf  MMA layout for [M, K/g]
  *   B_packed  [N, K/2] bytes, K-major;  B_sf  MMA layout for [N, K/g]
  *   gs_a, gs_b DEVICE pointers to one fp32 each (NULL = 1.0; MXFP4 ignores)
- *   workspace  DEVICE scratch of ws_bytes >= qfp4_gemm_workspace_bytes(...)
- *              (may be NULL when that is 0); it must not be shared with a
- *              call running concurrently.
+ *   workspace  DEVICE scratch of ws_bytes >= qfp4_gemm_workspace_bytes(...);
+ *              currently unused (NULL is fine).
  * Tensor cores: tcgen05.mma kind::mxf4 (MXFP4) / kind::mxf4nvf4 scale_vec::4X
- * (NVFP4), fp32 accumulation in tensor memory.
+ * (NVFP4), fp32 accumulation in tensor memory.  Kernels: M <= 128: one CTA
+ * per 128-column tile and K share, the K shares of a tile reduced in rank
+ * order over a thread-block cluster (deterministic); M > 128 and
+ * N % 256 == 0: CTA pairs (cta_group::2) on 256 x 256 tiles; otherwise
+ * single-CTA 128 x 128 / 128 x 256 tiles.
  * Requirements: M >= 1, N % 128 == 0, K % 128 == 0, all pointers 16-byte
  * aligned.  Accuracy: |D - exact| <= 2^-8 |exact| + 1e-6 sum_k |a_k b_k|. */
 int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K,

@@ -75,7 +75,7 @@ def run_gemm(fmt, A, A_sf_rm, B, B_sf_rm, gs_a=None, gs_b=None):
     gb = dev_scalar(gs_b) if gs_b is not None else None
     D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     ws_bytes = qfp4.gemm_workspace_bytes(fmt, M, N, K)
-    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda") if ws_bytes else None
+    ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device="cuda") if ws_bytes else None
     qfp4.gemm_nt(fmt, M, N, K, dA, sfa, dB, sfb, ga, gb, D, ws, ws_bytes)
     torch.cuda.synchronize()
     assert qfp4.poll_device_status() == 0

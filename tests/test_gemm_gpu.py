@@ -179,7 +179,7 @@ def test_pipeline_full_size(case):
         assert np.array_equal(q[3], q_ref) and np.array_equal(q[4], sf_ref)
     D = torch.empty((case.M, case.N), dtype=torch.bfloat16, device="cuda")
     ws_bytes = qfp4.gemm_workspace_bytes(case.fmt, case.M, case.N, case.K)
-    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
     qfp4.gemm_nt(case.fmt, case.M, case.N, case.K, qa[0], qa[1], qb[0], qb[1], qa[2], qb[2], D,
                  ws, ws_bytes)
     torch.cuda.synchronize()
@@ -250,3 +250,35 @@ def test_grouped_moe_up_projection():
         d_ref, t_ref = oracle.gemm_nt_entries(NV, qa_ref, sfa_ref, qb_ref, sfb_ref, gsa_h[e], gsb_h[e], mi, ni)
         worst = max(worst, assert_gemm_close(Dh[offs[e] + mi, ni], d_ref, t_ref, f"expert {e}"))
     assert worst <= 1.0
+
+
+# ----------------------------------------------------------------- decode (split-K)
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+@pytest.mark.parametrize("M,N,K", [(1, 128, 256), (37, 384, 1024), (128, 1024, 4096), (100, 2048, 2304),
+                                   (128, 4096, 128), (64, 256, 8192)])
+def test_decode_split_k_shapes(fmt, M, N, K):
+    """M <= 128 runs the decode kernel, K split over a CTA cluster for small
+    N: must match the oracle and be bit-identical across repeated calls (the
+    cluster reduction adds the partial tiles in a fixed order)."""
+    A, Asf, B, Bsf = random_operands(fmt, M, N, K, M + N + K + 3 * fmt)
+    gs_a, gs_b = (None, None) if fmt == MX else (0.125, 3.0)
+    g = qfp4.block_size(fmt)
+    assert qfp4.gemm_workspace_bytes(fmt, M, N, K) == 0
+    dA, dB = to_dev_u8(A), to_dev_u8(B)
+    sfa = torch.zeros(qfp4.sf_mma_bytes(M, K // g), dtype=torch.uint8, device="cuda")
+    sfb = torch.zeros(qfp4.sf_mma_bytes(N, K // g), dtype=torch.uint8, device="cuda")
+    qfp4.sf_interleave(to_dev_u8(Asf), M, K // g, sfa, qfp4.SF_MMA)
+    qfp4.sf_interleave(to_dev_u8(Bsf), N, K // g, sfb, qfp4.SF_MMA)
+    ga = dev_scalar(gs_a) if gs_a else None
+    gb = dev_scalar(gs_b) if gs_b else None
+    outs = []
+    for _ in range(3):
+        D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        qfp4.gemm_nt(fmt, M, N, K, dA, sfa, dB, sfb, ga, gb, D)
+        torch.cuda.synchronize()
+        outs.append(bf16_to_f64(D))
+    assert qfp4.poll_device_status() == 0
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    d_ref, t_ref = oracle.gemm_nt(fmt, A, Asf, B, Bsf, gs_a or 1.0, gs_b or 1.0)
+    assert_gemm_close(outs[0], d_ref, t_ref, f"decode {M}x{N}x{K}")

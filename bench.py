@@ -48,8 +48,7 @@ PAGES_BASELINE_TFLOPS = 838.0      # quadbit dense FP4, prefill attn 4096^3, RTX
 FP4_OVER_BF16 = 13.5 / 2.25        # nominal dense FP4 : BF16 tensor rate on GB300
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
-GEMM_SRC = os.path.join(ROOT, "block_scaled_fp4_tcgen05_gb300", "csrc", "gemm.cu")
-QUANT_SRC = os.path.join(ROOT, "block_scaled_fp4_tcgen05_gb300", "csrc", "quantize.cu")
+CSRC = os.path.join(ROOT, "block_scaled_fp4_tcgen05_gb300", "csrc")
 FLUSH_BYTES = 512 << 20
 
 
@@ -97,8 +96,7 @@ def ncu_traffic(kernel_key):
         with open(TRAFFIC_FILE) as f:
             data = json.load(f)
         ent = data[kernel_key]
-        src = GEMM_SRC if ent.get("source") == "gemm.cu" else QUANT_SRC
-        if ent.get("source_sha") != file_sha(src):
+        if ent.get("source_sha") != file_sha(os.path.join(CSRC, ent["source"])):
             return None
         return float(ent["dram_bytes_per_launch"])
     except Exception:
@@ -277,9 +275,43 @@ def time_e2e(pipe, steps, warmup):
     return ms, pipe.X_pinned.numel() * 2, pipe.D_pinned.numel() * 2
 
 
-def rotated_gemm_time(case, device, l2_bytes, reps=3):
+def graph_time(calls, reps=10):
+    """Mean device time of one call, for kernels of a few microseconds where
+    host launch overhead would otherwise show: the calls are captured once in
+    a CUDA graph (back to back on one stream) and the graph is replayed
+    between CUDA events.  Returns the median over `reps` replays divided by
+    the number of calls."""
+    import torch
+    for c in calls:
+        c()
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for c in calls:
+                c()
+    torch.cuda.synchronize()
+    # replay() launches on the current stream: the events go on that stream too
+    cur = torch.cuda.current_stream()
+    graph.replay()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ts = []
+    for _ in range(reps):
+        s.record(cur)
+        graph.replay()
+        e.record(cur)
+        torch.cuda.synchronize()
+        ts.append(s.elapsed_time(e) / len(calls))
+    del graph
+    return statistics.median(ts)
+
+
+def rotated_gemm_time(case, device, l2_bytes, reps=10):
     """Mean device time of one GEMM launch over weight copies rotated so that
-    the footprint exceeds twice the L2 (no L2 hits on the weights)."""
+    the weights' footprint exceeds twice the L2 (no L2 hits on the weights
+    from the previous launch)."""
     import torch
     pipe = Pipeline(case, device)
     pipe.prologue()
@@ -287,20 +319,9 @@ def rotated_gemm_time(case, device, l2_bytes, reps=3):
     copies = max(1, min(16, int(np.ceil(2 * l2_bytes / max(wbytes, 1))) + 1))
     Qs = [pipe.Qb] + [pipe.Qb.clone() for _ in range(copies - 1)]
     SFs = [pipe.SFb] + [pipe.SFb.clone() for _ in range(copies - 1)]
-    for i in range(copies):
-        pipe.gemm(Qs[i], SFs[i])
-    torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    best = []
-    for _ in range(reps):
-        s.record()
-        for i in range(copies):
-            pipe.gemm(Qs[i], SFs[i])
-        e.record()
-        torch.cuda.synchronize()
-        best.append(s.elapsed_time(e) / copies)
-    ms = statistics.median(best)
-    del Qs, SFs, pipe
+    calls = [(lambda i=i: pipe.gemm(Qs[i], SFs[i])) for i in range(copies)]
+    ms = graph_time(calls, reps)
+    del Qs, SFs, calls, pipe
     torch.cuda.empty_cache()
     return ms
 
@@ -328,18 +349,8 @@ def sweep(device, l2_bytes, peaks):
         qfp4.global_scale(X, gs)
         Q = torch.empty((M, K // 2), dtype=torch.uint8, device=device)
         SF = torch.empty(qfp4.sf_mma_bytes(M, K // g), dtype=torch.uint8, device=device)
-        for _ in range(3):
-            qfp4.quantize(fmt, X, gs, Q, SF, qfp4.SF_MMA)
-        torch.cuda.synchronize()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ts = []
-        for _ in range(10):
-            s.record()
-            qfp4.quantize(fmt, X, gs, Q, SF, qfp4.SF_MMA)
-            e.record()
-            torch.cuda.synchronize()
-            ts.append(s.elapsed_time(e))
-        ms = statistics.median(ts)
+        # X alone (134 MB) exceeds the L2, so back-to-back launches re-read it from HBM
+        ms = graph_time([lambda: qfp4.quantize(fmt, X, gs, Q, SF, qfp4.SF_MMA)] * 8)
         byts = 2 * M * K + M * K / 2 + M * K / g
         gbs = byts / (ms * 1e-3) / 1e9
         out.append({"workload": f"{'nv' if fmt else 'mx'}fp4_quantize_{M}x{K}", "us": round(ms * 1e3, 2),
@@ -347,7 +358,7 @@ def sweep(device, l2_bytes, peaks):
         del X, Q, SF
     # compute-bound sweep
     for case in synth.COMPUTE_SWEEP:
-        ms = rotated_gemm_time(case, device, l2_bytes, reps=3)
+        ms = rotated_gemm_time(case, device, l2_bytes, reps=5)
         tf = 2 * case.M * case.N * case.K / (ms * 1e-3) / 1e12
         out.append({"workload": case.name, "us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
                     "frac_fp4_peak": round(tf / fp4_peak, 3)})
@@ -412,6 +423,46 @@ def grouped_time(device, fp4_peak):
             "TFLOP/s_step": round(flops / (ms * 1e-3) / 1e12, 1), "us_gemm": round(gms * 1e3, 1),
             "TFLOP/s_gemm": round(flops / (gms * 1e-3) / 1e12, 1),
             "frac_fp4_peak_gemm": round(flops / (gms * 1e-3) / 1e12 / fp4_peak, 3)}
+
+
+def single_kernel(args, device):
+    """--kernel NAME: only that kernel, `--warmup` then `--steps` launches
+    (the short runs that ncu captures).  Prints one JSON line with the mean
+    launch time over the timed launches."""
+    import torch
+    from block_scaled_fp4_tcgen05_gb300 import qfp4
+    name = args.kernel
+    if name.startswith("quantize"):
+        fmt = qfp4.NVFP4 if name.endswith("nvfp4") else qfp4.MXFP4
+        M, K = synth.QUANT_ROWS, synth.QUANT_COLS
+        g = qfp4.block_size(fmt)
+        X = torch.from_numpy(synth.activations_bf16(synth.QUANT_SEED, M, K).view(np.int16).copy()).view(
+            torch.bfloat16).to(device)
+        gs = torch.ones(1, dtype=torch.float32, device=device)
+        qfp4.global_scale(X, gs)
+        Q = torch.empty((M, K // 2), dtype=torch.uint8, device=device)
+        SF = torch.empty(qfp4.sf_mma_bytes(M, K // g), dtype=torch.uint8, device=device)
+        run = lambda: qfp4.quantize(fmt, X, gs, Q, SF, qfp4.SF_MMA)
+        workload = f"{name}_{M}x{K}"
+    else:
+        case = {"decode_up": synth.DECODE_UP, "decode_attn": synth.DECODE_ATTN,
+                "prefill": synth.PREFILL_NV}[name]
+        pipe = Pipeline(case, device)
+        pipe.prologue()
+        run = pipe.gemm
+        workload = case.name
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        run()
+    e.record()
+    torch.cuda.synchronize()
+    assert qfp4.poll_device_status() == 0
+    print(json.dumps({"kernel": name, "workload": workload, "launches": args.steps,
+                      "us_per_launch": round(s.elapsed_time(e) * 1e3 / args.steps, 2)}), flush=True)
 
 
 # --------------------------------------------------------------------------- CPU oracle arm
@@ -485,6 +536,9 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--kernel", default=None,
+                    choices=["quantize_nvfp4", "quantize_mxfp4", "decode_up", "decode_attn", "prefill"],
+                    help="launch only this kernel (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -512,6 +566,9 @@ def main():
     l2_bytes = getattr(props, "L2_cache_size", 128 << 20)
     peaks = load_peaks()
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    if args.kernel:
+        single_kernel(args, device)
+        return
 
     case = CASE
     pipe = Pipeline(case, device)
@@ -533,10 +590,10 @@ def main():
 
     e2e_ms, h2d, d2h = time_e2e(pipe, max(10, args.steps // 2), args.warmup)
     gemm_tf = flops / (gemm_ms * 1e-3) / 1e12
-    traffic = ncu_traffic("gemm_nvfp4_4096x4096x4096")
+    traffic = ncu_traffic("gemm_pair_kernel nvfp4 4096x4096x4096")
     roof = {"bound": "tensor", "achieved": round(gemm_tf, 1), "peak": round(fp4_peak, 1),
             "unit": "TFLOP/s", "frac": round(gemm_tf / fp4_peak, 4), "traffic": traffic,
-            "kernel": "gemm_kernel<NVFP4, BN=256> (qfp4_gemm_nt)", "gemm_us": round(gemm_ms * 1e3, 2),
+            "kernel": "gemm_pair_kernel<NVFP4> (qfp4_gemm_nt, CTA pairs on 256x256 tiles)", "gemm_us": round(gemm_ms * 1e3, 2),
             "prologue_us": round(pro_ms * 1e3, 2),
             "peak_note": f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} TFLOP/s x {FP4_OVER_BF16:g} "
                          f"(nominal dense FP4:BF16 ratio), of {peaks['source']}"}

@@ -282,3 +282,49 @@ def test_decode_split_k_shapes(fmt, M, N, K):
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
     d_ref, t_ref = oracle.gemm_nt(fmt, A, Asf, B, Bsf, gs_a or 1.0, gs_b or 1.0)
     assert_gemm_close(outs[0], d_ref, t_ref, f"decode {M}x{N}x{K}")
+
+
+# ----------------------------------------------------------------- grouped vs dense
+
+@pytest.mark.parametrize("N", [14336, 14464])
+def test_grouped_equals_dense_per_group(N):
+    """The grouped launch computes every group with the same kernel and the
+    same K order as a dense launch over that group's rows, so the outputs must
+    be bit-identical, and identical across repeated launches.  Scale factors
+    vary along K, so a K-block combined with another K-block's scales shows.
+    N = 14336 runs the CTA-pair kernel, N = 14464 the single-CTA one."""
+    counts = np.array([2193, 1698, 128, 1553, 1387, 16, 142, 1075])
+    E, K, g = len(counts), 4096, 16
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows = int(offs[-1])
+    gen = torch.Generator(device="cuda").manual_seed(1234 + N)
+    A = torch.randint(0, 256, (rows, K // 2), dtype=torch.uint8, device="cuda", generator=gen)
+    B = torch.randint(0, 256, (E * N, K // 2), dtype=torch.uint8, device="cuda", generator=gen)
+    SFa = torch.randint(40, 60, (qfp4.sf_mma_grouped_bytes(rows, E, K // g),), dtype=torch.uint8,
+                        device="cuda", generator=gen)
+    SFb = torch.randint(40, 60, (qfp4.sf_mma_grouped_bytes(E * N, E, K // g),), dtype=torch.uint8,
+                        device="cuda", generator=gen)
+    gs_a = torch.rand(E, device="cuda", generator=gen) + 0.5
+    gs_b = torch.rand(E, device="cuda", generator=gen) + 0.5
+    d_offs = torch.from_numpy(offs).cuda()
+    outs = []
+    for _ in range(2):
+        D = torch.zeros((rows, N), dtype=torch.bfloat16, device="cuda")
+        qfp4.gemm_nt_grouped(NV, d_offs, rows, int(counts.max()), N, K, A, SFa, B, SFb, gs_a, gs_b, D)
+        torch.cuda.synchronize()
+        outs.append(D)
+    assert qfp4.poll_device_status() == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    kc = K // g // 4
+    tile = 0
+    for e in range(E):
+        m = int(counts[e])
+        sfa_e = SFa[tile * kc * 512:(tile + (m + 127) // 128) * kc * 512]
+        sfb_e = SFb[e * (N // 128) * kc * 512:(e + 1) * (N // 128) * kc * 512]
+        tile += (m + 127) // 128
+        De = torch.empty((m, N), dtype=torch.bfloat16, device="cuda")
+        qfp4.gemm_nt(NV, m, N, K, A[offs[e]:offs[e + 1]], sfa_e, B[e * N:(e + 1) * N], sfb_e,
+                     gs_a[e:e + 1], gs_b[e:e + 1], De)
+        torch.cuda.synchronize()
+        same = torch.equal(De.view(torch.int16), outs[0][offs[e]:offs[e + 1]].view(torch.int16))
+        assert same, f"group {e} ({m} rows) differs from the dense launch"

@@ -398,6 +398,21 @@ int make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, 
     return r == CUDA_SUCCESS ? QFP4_OK : QFP4_ERR_CUDA;
 }
 
+int make_map_bf16(CUtensorMap *map, void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                  uint32_t box_rows)
+{
+    auto enc = get_encode_fn();
+    if (!enc) return QFP4_ERR_CUDA;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? QFP4_OK : QFP4_ERR_CUDA;
+}
+
 namespace {
 
 template <int FMT, int BN, int STAGES, bool GROUPED>
@@ -452,11 +467,13 @@ extern "C" int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K, const void
     CUtensorMap ma, mb;
     (void)workspace; (void)ws_bytes;
     if (M <= 128) {
-        // decode shapes: 128-column tiles with K split over a CTA cluster
-        int rc = make_map(&ma, A_packed, K / 2, M, kBKBytes, 128);
-        if (rc == QFP4_OK) rc = make_map(&mb, B_packed, K / 2, N, kBKBytes, 128);
+        // decode shapes: swap AB on CTA pairs, weights in the MMA's M slot
+        CUtensorMap md;
+        int rc = make_map(&mb, B_packed, K / 2, N, kBKBytes, 128);
+        if (rc == QFP4_OK) rc = make_map(&ma, A_packed, K / 2, M, kBKBytes, 64);
+        if (rc == QFP4_OK) rc = make_map_bf16(&md, D_bf16, N, M, 128, 128);
         if (rc != QFP4_OK) return rc;
-        return launch_gemm_decode(fmt, ma, mb, a, s);
+        return launch_gemm_decode(fmt, mb, ma, md, a, s);
     }
     if (N % 256 == 0 && M > 128) {
         // CTA pairs on 256 x 256 tiles

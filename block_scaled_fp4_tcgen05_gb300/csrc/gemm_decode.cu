@@ -1,25 +1,28 @@
 // gemm_decode.cu -- block-scaled FP4 GEMM for decode-shaped batches (M <= 128).
 //
-// Pages: quadbit README, "End-to-end serving": at decode the weights are
-// streamed from DRAM, and a kernel that launches too few CTAs leaves the GPU
-// idle; splitting K over more CTAs with an fp32 reduction fills the machine.
-// DeepGEMM pull request "Summary" for the operation itself.
+// Pages: quadbit README, "End-to-end serving": at decode the weights stream
+// from DRAM and the kernel must keep enough SMs busy to do that at full
+// bandwidth; DeepGEMM pull request "Key technical details" (swap-AB epilogue,
+// 2-CTA cta_group::2 MMAs with per-CTA scale-factor loads).
 //
-// All M (<= 128) rows fit one MMA tile, so a CTA owns a 128-column tile of N
-// and a contiguous share of K: (N / 128) tiles x S splits CTAs, with S the
-// largest power of two <= 8 that keeps the grid within one wave of SMs (S = 1
-// for N = 14336, where 112 CTAs already outrun HBM; S = 4 for N = 4096).
-// The S CTAs of a tile form one thread-block cluster: each accumulates its
-// K share in tensor memory, writes the fp32 partial tile into its own shared
-// memory, and after a cluster barrier every CTA reduces 128/S rows of the
-// tile by reading all S partials over distributed shared memory, in rank
-// order (deterministic), scales by gs_a * gs_b and stores BF16.  Nothing goes
-// through global memory but the operands and D, and no workspace is needed.
+// Swap AB: the weights B [N, K] take the MMA's M slot and the <= 128 tokens
+// of A take its N slot, so the tensor core computes D^T.  A CTA pair owns 256
+// weight rows (128 per CTA) and all K: ceil(N / 256) pairs, no split-K and no
+// cross-CTA reduction (N = 14336: 56 pairs on 112 SMs).  Per 256-K block the
+// leader issues four M=256 N=128 K=64 MMAs (each CTA's tensor memory
+// receives its 128 weight rows x 128 tokens); each CTA streams 16 KB of
+// weights, 8 KB of tokens (its half of N) and 4 KB of scale factors.
 //
-// Roles (192 threads): warp 0 TMA producer (A, B and scale tiles of each
-// 256-K block into a 6-deep ring); warp 1 tensor-memory owner and MMA issuer
-// (scale tiles copied to tensor memory with tcgen05.cp, four K=64 MMAs per
-// block); warps 2..5 drain the accumulator.  All waits are bounded.
+// Roles (384 threads per CTA): warps 0 and 3 weight and token TMA producers
+// (both CTAs, completion on the leader's barrier); warp 2 scale-factor producer (bulk
+// copies into a local ring); warp 1 tensor-memory owner and, in the leader,
+// the MMA issuer; warps 4..11, two sets of four taking alternate K-blocks,
+// move the scale bytes into tensor memory with tcgen05.st (the tensor pipe
+// then runs MMAs only; one set alone, waiting for each store to complete,
+// would take about a K-block's streaming time per K-block); at the end warps
+// 4..7 drain the accumulator: scale by gs_a * gs_b, round to BF16, transpose
+// through shared memory and write D with one TMA store per CTA.  All waits
+// are bounded.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -48,28 +51,34 @@ int read_clear_status_gemm_decode(cudaStream_t s, uint32_t *out)
 
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kStages = 6;
-constexpr int kBN = 128;
-constexpr int kMaxSplit = 8;
+constexpr int kThreads = 384;          // 12 warps
+constexpr int kTok = 128;              // MMA N: token rows, 64 per CTA
 
 template <int FMT>
 struct DecCfg {
     static constexpr int G = FMT == QFP4_MXFP4 ? 32 : 16;
-    static constexpr int CPS = (256 / G) / 4;           // 512-B SF tiles per 128 rows per K-block
-    static constexpr int A_BYTES = 128 * 128;
-    static constexpr int B_BYTES = kBN * 128;
-    static constexpr int SF_BYTES = 2 * CPS * 512;      // A then B
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
-    static constexpr int PART_BYTES = 128 * kBN * 4;    // fp32 partial tile (reuses the ring)
-    static constexpr int OFF_BAR = kStages * STAGE_BYTES;
-    static constexpr int NBAR = 2 * kStages + 1;        // full, empty, acc_full
-    static constexpr int SMEM = OFF_BAR + NBAR * 8 + 32 + 1024;
-    static constexpr int SF_COLS = 2 * CPS * 4;         // per stage: A then B
-    static constexpr int COL_SF = kBN;
+    static constexpr int CPS = (256 / G) / 4;          // 512-B SF tiles per 128 rows per 256-K block
+    static constexpr int W_BYTES = 128 * 128;          // this CTA's 128 weight rows
+    static constexpr int T_BYTES = (kTok / 2) * 128;   // this CTA's 64 token rows
+    static constexpr int AB_BYTES = W_BYTES + T_BYTES;
+    static constexpr int AB_STAGES = 7;
+    static constexpr int SFW_BYTES = CPS * 512;         // weight rows' scales (MMA A)
+    static constexpr int SFT_BYTES = CPS * 512;         // all 128 token rows' scales (MMA B)
+    static constexpr int SF_BYTES = SFW_BYTES + SFT_BYTES;
+    static constexpr int SF_STAGES = 8;
+    static constexpr int OFF_SF = AB_STAGES * AB_BYTES;
+    static constexpr int OFF_BAR = OFF_SF + SF_STAGES * SF_BYTES;
+    // full/empty[AB], sf_full/sf_empty[SF], acc_full
+    static constexpr int NBAR = 2 * AB_STAGES + 2 * SF_STAGES + 1;
+    static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
+    static constexpr int SFW_COLS = CPS * 4;            // weight word of each quarter, replicated
+    static constexpr int SFT_COLS = CPS * 4;            // all 128 token rows in every quarter
+    static constexpr int SLOT_COLS = SFW_COLS + SFT_COLS;
+    static constexpr int COL_SF = kTok;                 // accumulator: 128 columns
     static constexpr int TMEM_COLS = 512;
-    static_assert(PART_BYTES <= OFF_BAR, "partial tile must fit in the ring");
-    static_assert(COL_SF + kStages * SF_COLS <= TMEM_COLS, "tensor memory overflow");
+    static constexpr int D_BYTES = kTok * 128 * 2;      // BF16 staging of D^T -> D (reuses the ring)
+    static_assert(COL_SF + AB_STAGES * SLOT_COLS <= TMEM_COLS, "tensor memory overflow");
+    static_assert(D_BYTES <= OFF_SF, "output staging must fit in the operand ring");
     static_assert(SMEM <= 232448, "shared memory overflow");
 };
 
@@ -78,247 +87,261 @@ __device__ __forceinline__ void record_timeout()
     atomicOr(&g_status_gemm_decode, static_cast<uint32_t>(kStatusTimeout));
 }
 
-__device__ __forceinline__ uint32_t cluster_nctarank()
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t cluster_addr)
-{
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(cluster_addr)
-                 : "memory");
-    return v;
-}
-
-// Partial tile layout in shared memory: row r, 16-byte chunk j (columns
-// 4j..4j+3) at chunk index r * 32 + (j ^ (r & 31)); the XOR spreads the rows
-// a warp writes at the same chunk over all banks.
-__device__ __forceinline__ uint32_t part_offset(int r, int j)
-{
-    return static_cast<uint32_t>((r * 32 + (j ^ (r & 31))) * 16);
+    __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&pr);
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads, 1)
-gemm_decode_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT,
+                   const __grid_constant__ CUtensorMap tmD, const GemmParams p)
 {
     using C = DecCfg<FMT>;
+    constexpr int SAB = C::AB_STAGES, SSF = C::SF_STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-    uint64_t *full = bars;
-    uint64_t *empty = bars + kStages;
-    uint64_t *acc_full = bars + 2 * kStages;
+    uint64_t *full = bars;                 // leader: operand bytes of both CTAs + 8 scale warps
+    uint64_t *empty = full + SAB;          // stage and its tensor-memory scale slot free (MMA commit)
+    uint64_t *sf_full = empty + SAB;       // local: scale bytes landed
+    uint64_t *sf_empty = sf_full + SSF;    // local: scale warps done with the slot
+    uint64_t *acc_full = sf_empty + SSF;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::NBAR);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int32_t pair = blockIdx.x >> 1;
     const int K = p.K;
     const int kc = (K / C::G) / 4;
     const int kblocks = (K + 255) / 256;
-    const uint32_t S = cluster_nctarank();
-    const uint32_t rank = cluster_ctarank();
-    const int32_t tile = blockIdx.x / S;
-    const int per = (kblocks + static_cast<int>(S) - 1) / static_cast<int>(S);
-    const int kb0 = min(kblocks, static_cast<int>(rank) * per);
-    const int kb1 = min(kblocks, kb0 + per);
+    const int32_t wtile = 2 * pair + static_cast<int32_t>(rank);   // this CTA's 128-row weight tile
+    const bool w_valid = wtile < p.N / 128;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
+        for (int s = 0; s < SAB; ++s) {
+            mbar_init(smem_u32(&full[s]), 1 + 8);     // leader producer (with the bytes) + 4 scale warps x 2 CTAs
             mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int s = 0; s < SSF; ++s) {
+            mbar_init(smem_u32(&sf_full[s]), 1);
+            mbar_init(smem_u32(&sf_empty[s]), 4);     // the four warps of one set
         }
         mbar_init(smem_u32(acc_full), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmW);
+        prefetch_tensormap(&tmT);
+        prefetch_tensormap(&tmD);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer
+    if (warp == 0 || warp == 3) {
+        // ------------------------------------------------ weight (warp 0) / token (warp 3) TMA producers
+        // (two issuing warps: the copy engine serves one issuing thread's
+        // requests one after another)
         if (lane == 0) {
-            uint32_t s = 0, phase = 0;
+            const bool is_w = warp == 0;
+            const uint32_t full0_leader = mapa_shared(smem_u32(&full[0]), 0);
             bool ok = true;
-            for (int kb = kb0; kb < kb1; ++kb) {
-                if (!mbar_wait(smem_u32(&empty[s]), phase ^ 1)) { ok = false; break; }
+            for (int kb = 0; kb < kblocks; ++kb) {
+                const uint32_t s = kb % SAB;
+                if (!mbar_wait(smem_u32(&empty[s]), ((kb / SAB) & 1) ^ 1)) { ok = false; break; }
+                const uint32_t dst = smem_u32(smem + s * C::AB_BYTES);
+                const uint32_t fb = full0_leader + s * 8;
+                if (is_w) {
+                    // the leader's weight thread posts the byte count of both CTAs' loads
+                    if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * C::AB_BYTES);
+                    tma_load_2d_pair(dst, &tmW, fb, kb * 128, wtile * 128);
+                } else {
+                    tma_load_2d_pair(dst + C::W_BYTES, &tmT, fb, kb * 128, static_cast<int32_t>(rank) * (kTok / 2));
+                }
+            }
+            if (!ok) { record_timeout(); *abort_flag = 1; }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------ scale-factor producer (both CTAs)
+        if (lane == 0) {
+            const uint8_t *sfw_g = p.B_sf + static_cast<size_t>(wtile) * kc * 512;
+            bool ok = true;
+            for (int kb = 0; kb < kblocks; ++kb) {
+                const uint32_t s = kb % SSF;
+                if (!mbar_wait(smem_u32(&sf_empty[s]), ((kb / SSF) & 1) ^ 1)) { ok = false; break; }
                 const int chunks = min(C::CPS, kc - kb * C::CPS);
-                const uint32_t fb = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES + 2 * chunks * 512);
-                const uint32_t dst = smem_u32(smem + s * C::STAGE_BYTES);
-                tma_load_2d(dst, &tmA, fb, kb * 128, 0);
-                tma_load_2d(dst + C::A_BYTES, &tmB, fb, kb * 128, tile * kBN);
+                const uint32_t bar = smem_u32(&sf_full[s]);
+                mbar_arrive_expect_tx(bar, (w_valid ? 2 : 1) * chunks * 512);
+                const uint32_t dst = smem_u32(smem + C::OFF_SF + s * C::SF_BYTES);
                 const size_t koff = static_cast<size_t>(kb) * C::CPS * 512;
-                bulk_load(dst + C::A_BYTES + C::B_BYTES, p.A_sf + koff, chunks * 512, fb);
-                bulk_load(dst + C::A_BYTES + C::B_BYTES + C::CPS * 512,
-                          p.B_sf + static_cast<size_t>(tile) * kc * 512 + koff, chunks * 512, fb);
-                if (++s == kStages) { s = 0; phase ^= 1; }
+                if (w_valid) bulk_load(dst, sfw_g + koff, chunks * 512, bar);
+                bulk_load(dst + C::SFW_BYTES, p.A_sf + koff, chunks * 512, bar);
             }
             if (!ok) { record_timeout(); *abort_flag = 1; }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t s = 0, phase = 0;
+        // ------------------------------------------------ MMA issuer (leader)
+        if (rank == 0 && lane == 0) {
+            const uint64_t w_desc0 = smem_desc(smem_u32(smem), 16, 1024, kSwizzle128B);
+            const uint64_t t_desc0 = smem_desc(smem_u32(smem) + C::W_BYTES, 16, 1024, kSwizzle128B);
+            constexpr uint64_t kStageDesc = static_cast<uint64_t>(C::AB_BYTES >> 4);
             bool ok = true;
-            bool first = true;
-            for (int kb = kb0; kb < kb1; ++kb) {
+            uint32_t s = 0, phase = 0;
+            for (int kb = 0; kb < kblocks; ++kb) {
                 if (!mbar_wait(smem_u32(&full[s]), phase)) { ok = false; break; }
                 tc_fence_after();
-                const int chunks = min(C::CPS, kc - kb * C::CPS);
-                const uint32_t sf_t = tmem_base + C::COL_SF + s * C::SF_COLS;
-                const uint32_t stage = smem_u32(smem + s * C::STAGE_BYTES);
-                const uint32_t sf_s = stage + C::A_BYTES + C::B_BYTES;
-                for (int c = 0; c < chunks; ++c) {
-                    tc_cp_32x128b_warpx4(sf_t + c * 4, smem_desc(sf_s + c * 512, 128, 128, kSwizzleNone));
-                    tc_cp_32x128b_warpx4(sf_t + C::CPS * 4 + c * 4,
-                                         smem_desc(sf_s + (C::CPS + c) * 512, 128, 128, kSwizzleNone));
-                }
+                const uint64_t wd = w_desc0 + s * kStageDesc;
+                const uint64_t td = t_desc0 + s * kStageDesc;
+                const uint32_t sfw_t = tmem_base + C::COL_SF + s * C::SLOT_COLS;
+                const uint32_t sft_t = sfw_t + C::SFW_COLS;
                 const int ksteps = min(4, (K - kb * 256) / 64);
-                const uint64_t ad0 = smem_desc(stage, 16, 1024, kSwizzle128B);
-                const uint64_t bd0 = smem_desc(stage + C::A_BYTES, 16, 1024, kSwizzle128B);
                 for (int kk = 0; kk < ksteps; ++kk) {
-                    const uint32_t accum = first ? 0u : 1u;
-                    first = false;
+                    const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
                     if (FMT == QFP4_NVFP4) {
-                        constexpr uint32_t id = idesc_block_scaled(128, kBN, false, 0, 0);
-                        tc_mma_nvf4(tmem_base, ad0 + 2 * kk, bd0 + 2 * kk, id, sf_t + kk * 4,
-                                    sf_t + C::CPS * 4 + kk * 4, accum);
+                        constexpr uint32_t id = idesc_block_scaled(256, kTok, false, 0, 0);
+                        tc_mma_nvf4_pair(tmem_base, wd + 2 * kk, td + 2 * kk, id, sfw_t + kk * 4, sft_t + kk * 4,
+                                         acc);
                     } else {
-                        constexpr uint32_t id0 = idesc_block_scaled(128, kBN, true, 0, 0);
-                        constexpr uint32_t id1 = idesc_block_scaled(128, kBN, true, 2, 2);
-                        tc_mma_mxf4(tmem_base, ad0 + 2 * kk, bd0 + 2 * kk, (kk & 1) ? id1 : id0,
-                                    sf_t + (kk >> 1) * 4, sf_t + C::CPS * 4 + (kk >> 1) * 4, accum);
+                        constexpr uint32_t id0 = idesc_block_scaled(256, kTok, true, 0, 0);
+                        constexpr uint32_t id1 = idesc_block_scaled(256, kTok, true, 2, 2);
+                        tc_mma_mxf4_pair(tmem_base, wd + 2 * kk, td + 2 * kk, (kk & 1) ? id1 : id0,
+                                         sfw_t + (kk >> 1) * 4, sft_t + (kk >> 1) * 4, acc);
                     }
                 }
-                tc_commit(smem_u32(&empty[s]));
-                if (++s == kStages) { s = 0; phase ^= 1; }
+                tc_commit_pair(smem_u32(&empty[s]), 0x3);
+                if (++s == SAB) { s = 0; phase ^= 1; }
             }
-            // an empty K share issues no MMA; the commit still arrives
-            if (ok) tc_commit(smem_u32(acc_full));
+            if (ok) tc_commit_pair(smem_u32(acc_full), 0x3);
             else { record_timeout(); *abort_flag = 1; }
         }
-    } else {
-        // ------------------------------------------------ accumulator drain (warps 2..5)
+    } else if (warp >= 4) {
         const int quad = warp & 3;
-        const int row = quad * 32 + lane;
-        const int got = __shfl_sync(0xffffffffu, lane == 0 ? (mbar_wait(smem_u32(acc_full), 0) ? 1 : 0) : 0, 0);
+        const int set = (warp - 4) >> 2;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t ready0_leader = mapa_shared(smem_u32(&full[0]), 0);
+        bool ok = true;
+        // -------------------------------------------- scale factors -> tensor memory
+        // Tensor-memory layout of one 512-byte tile at columns [c, c+4):
+        // lane 32q + i, column c + j holds the four scale bytes of row
+        // i + 32 j.  Quarter q of the MMA reads its weight rows' scales from
+        // column c + q only, but needs all 128 token rows, so the token
+        // tile is written in full and the weight word q into all four
+        // columns.  The shared-memory slot is handed back only after the
+        // values reached tensor memory.
+        for (int kb = set; kb < kblocks; kb += 2) {
+            const uint32_t s = kb % SSF, slot = kb % SAB;
+            int got = __shfl_sync(0xffffffffu,
+                                  lane == 0 ? (mbar_wait(smem_u32(&sf_full[s]), (kb / SSF) & 1) ? 1 : 0) : 0, 0);
+            if (!got) { ok = false; break; }
+            const uint8_t *sf_s = smem + C::OFF_SF + s * C::SF_BYTES;
+            uint32_t vw[C::SFW_COLS];
+            uint32_t vt[C::SFT_COLS];
+#pragma unroll
+            for (int c = 0; c < C::CPS; ++c) {
+                const uint4 w4 = *reinterpret_cast<const uint4 *>(sf_s + c * 512 + lane * 16);
+                const uint32_t w = quad == 0 ? w4.x : quad == 1 ? w4.y : quad == 2 ? w4.z : w4.w;
+                vw[4 * c + 0] = w; vw[4 * c + 1] = w; vw[4 * c + 2] = w; vw[4 * c + 3] = w;
+                const uint4 t4 = *reinterpret_cast<const uint4 *>(sf_s + C::SFW_BYTES + c * 512 + lane * 16);
+                vt[4 * c + 0] = t4.x; vt[4 * c + 1] = t4.y; vt[4 * c + 2] = t4.z; vt[4 * c + 3] = t4.w;
+            }
+            got = __shfl_sync(0xffffffffu,
+                              lane == 0 ? (mbar_wait(smem_u32(&empty[slot]), ((kb / SAB) & 1) ^ 1) ? 1 : 0) : 0, 0);
+            if (!got) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t col = tmem_base + C::COL_SF + slot * C::SLOT_COLS;
+            tmem_st_32x32b<C::SFW_COLS>(lane_base + col, vw);
+            tmem_st_32x32b<C::SFT_COLS>(lane_base + col + C::SFW_COLS, vt);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(smem_u32(&sf_empty[s]));
+                mbar_arrive_cluster_relaxed(ready0_leader + slot * 8);
+            }
+        }
+        // -------------------------------------------- accumulator drain
+        // Lane 32q + i of tensor memory is weight row n = 32q + i of this
+        // CTA; column m is token m.  Each thread writes D[m][n] for its n
+        // into a row-major [128 tokens][128 columns] BF16 tile in shared
+        // memory (a warp writes 64 consecutive bytes per token), and one
+        // TMA store moves the tile to D; rows m >= M are clipped by it.
+        if (set == 0) {
+        const int got = ok ? __shfl_sync(0xffffffffu,
+                                         lane == 0 ? (mbar_wait(smem_u32(acc_full), 0) ? 1 : 0) : 0, 0)
+                           : 0;
         if (got) {
             tc_fence_after();
-            uint32_t v[4][32];
+            float gs = 1.0f;
+            if (FMT == QFP4_NVFP4) gs = (p.gs_a ? *p.gs_a : 1.0f) * (p.gs_b ? *p.gs_b : 1.0f);
+            const int n = quad * 32 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+            // Neighbouring lanes (rows n, n^1) swap one value per pair of
+            // tokens so that each writes two adjacent columns of one token
+            // row as a 4-byte word: the even lane token m, the odd lane m+1.
+            uint32_t *stage = reinterpret_cast<uint32_t *>(smem);
+            const bool odd = lane & 1;
+            const int n0 = n & ~1;
+            const int nchunks = (p.M + 31) / 32;
+            for (int j = 0; j < nchunks; ++j) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(taddr + j * 32, v);
+                tmem_ld_wait();
+                tmem_regs_after_wait(v);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tmem_ld_32x32b_x32(taddr + j * 32, v[j]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 4; ++j) tmem_regs_after_wait(v[j]);
-            if (kb1 <= kb0) {
-                // empty K share (more splits than K-blocks): contributes zeros
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[j][i] = 0u;
-            }
-            if (S == 1) {
-                float gs = 1.0f;
-                if (FMT == QFP4_NVFP4) gs = (p.gs_a ? *p.gs_a : 1.0f) * (p.gs_b ? *p.gs_b : 1.0f);
-                if (row < p.M) {
-                    __nv_bfloat16 *drow = p.D + static_cast<size_t>(row) * p.N + tile * kBN;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t packed[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(v[j][2 * i]) * gs,
-                                                                      __uint_as_float(v[j][2 * i + 1]) * gs);
-                            packed[i] = *reinterpret_cast<uint32_t *>(&pr);
-                        }
-                        st_global_v8(drow + j * 32, *reinterpret_cast<const uint32_t(*)[8]>(&packed[0]));
-                        st_global_v8(drow + j * 32 + 16, *reinterpret_cast<const uint32_t(*)[8]>(&packed[8]));
-                    }
+                for (int i = 0; i < 32; i += 2) {
+                    const float a = __uint_as_float(v[i]) * gs, b = __uint_as_float(v[i + 1]) * gs;
+                    const float other = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+                    const int m = j * 32 + i + (odd ? 1 : 0);
+                    // columns n0 (low half) and n0 + 1 (high half) of token row m
+                    stage[(m * 128 + n0) >> 1] = odd ? pack_bf16x2(other, b) : pack_bf16x2(a, other);
                 }
-            } else {
-                // the ring is idle now (every load was consumed): keep the
-                // fp32 partial tile in shared memory for the cluster reduction
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4 *>(smem + part_offset(row, j * 8 + c)) =
-                            make_uint4(v[j][4 * c], v[j][4 * c + 1], v[j][4 * c + 2], v[j][4 * c + 3]);
             }
+            fence_proxy_async_smem();
         } else if (lane == 0) {
             record_timeout();
             *abort_flag = 1;
         }
+        __syncwarp();
+        named_barrier_sync(1, 4 * 32);
+        if (warp == 4 && lane == 0 && !*abort_flag && w_valid) {
+            tma_store_2d(&tmD, smem_u32(smem), wtile * 128, 0);
+            bulk_commit_group();
+            bulk_wait_group<0>();
+        }
+        }
     }
 
-    // ---- all roles done.  Reconverge each warp first: lanes that skipped a
+    // ---- teardown.  Reconverge each warp first: lanes that skipped a
     // single-lane role must not reach the block barrier ahead of their warp's
     // working lane.
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();
     if (*abort_flag) {
         const uint64_t t0 = globaltimer_ns();
         while (globaltimer_ns() - t0 < 1000000ull) { }
     }
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
-    }
-    if (S > 1) {
-        // every CTA of the cluster holds its partial tile in shared memory
-        cluster_sync_all();
-        float gs = 1.0f;
-        if (FMT == QFP4_NVFP4) gs = (p.gs_a ? *p.gs_a : 1.0f) * (p.gs_b ? *p.gs_b : 1.0f);
-        const int rows = 128 / static_cast<int>(S);
-        const int r0 = static_cast<int>(rank) * rows;
-        const uint32_t base = smem_u32(smem);
-        // one 16-byte chunk (4 columns) of one row per thread and step; the
-        // partials are added in cluster-rank order whichever CTA reads them
-        for (int idx = threadIdx.x; idx < rows * 32; idx += kThreads) {
-            const int r = r0 + idx / 32, j = idx % 32;
-            const uint32_t off = part_offset(r, j);
-            float4 a = ld_dsmem_v4(mapa_shared(base + off, 0));
-            for (uint32_t q = 1; q < S; ++q) {
-                const float4 b = ld_dsmem_v4(mapa_shared(base + off, q));
-                a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-            }
-            if (r < p.M) {
-                __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * gs, a.y * gs);
-                __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * gs, a.w * gs);
-                uint2 w;
-                w.x = *reinterpret_cast<uint32_t *>(&lo);
-                w.y = *reinterpret_cast<uint32_t *>(&hi);
-                *reinterpret_cast<uint2 *>(p.D + static_cast<size_t>(r) * p.N + tile * kBN + j * 4) = w;
-            }
-        }
-        // keep this CTA's shared memory alive until every peer has read it
-        cluster_sync_all();
+        tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
     }
 }
 
 template <int FMT>
-int launch_decode(const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &g, int tiles, int split,
+int launch_decode(const CUtensorMap &mw, const CUtensorMap &mt, const CUtensorMap &md, const GemmParams &g,
                   cudaStream_t s)
 {
     using C = DecCfg<FMT>;
@@ -331,42 +354,18 @@ int launch_decode(const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams
             return QFP4_ERR_CUDA;
         configured_device = dev;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(tiles * split));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::SMEM;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return launch_status(cudaLaunchKernelEx(&cfg, kern, ma, mb, g));
+    const int pairs = (g.N + 255) / 256;
+    kern<<<2 * pairs, kThreads, C::SMEM, s>>>(mw, mt, md, g);
+    return launch_status(cudaGetLastError());
 }
 
 }  // namespace
 
-// K splits per 128-column tile: the largest power of two <= 8 (and <= the
-// number of 256-K blocks) for which the grid still fits one wave of SMs.
-int decode_split(int64_t N, int64_t K)
+int launch_gemm_decode(int fmt, const CUtensorMap &mw, const CUtensorMap &mt, const CUtensorMap &md,
+                       const GemmParams &g, cudaStream_t s)
 {
-    const int64_t tiles = N / kBN, kblocks = (K + 255) / 256;
-    int sms = sm_count();
-    if (sms <= 0) sms = 148;
-    int split = 1;
-    while (split * 2 <= kMaxSplit && split * 2 <= kblocks && tiles * split * 2 <= sms) split *= 2;
-    return split;
-}
-
-int launch_gemm_decode(int fmt, const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &g,
-                       cudaStream_t s)
-{
-    const int tiles = g.N / kBN;
-    const int split = decode_split(g.N, g.K);
-    return fmt == QFP4_NVFP4 ? launch_decode<QFP4_NVFP4>(ma, mb, g, tiles, split, s)
-                             : launch_decode<QFP4_MXFP4>(ma, mb, g, tiles, split, s);
+    return fmt == QFP4_NVFP4 ? launch_decode<QFP4_NVFP4>(mw, mt, md, g, s)
+                             : launch_decode<QFP4_MXFP4>(mw, mt, md, g, s);
 }
 
 }  // namespace qfp4

@@ -10,9 +10,9 @@
 // shared memory; the leader (r = 0) issues M=256 x N=256 x K=64 MMAs that read
 // both CTAs' operands, and each CTA's tensor memory receives its own 128 rows
 // of the fp32 accumulator.  Per CTA (20 warps):
-//   warp 0        A/B TMA producer: 256-K slices of A and B into a 5-deep
-//                 (NVFP4) / 6-deep (MXFP4) ring; the leader's mbarrier
-//                 collects the bytes of both CTAs.
+//   warps 0, 3    A and B TMA producers: 256-K slices of A (warp 0) and B
+//                 (warp 3) into a 5-deep (NVFP4) / 6-deep (MXFP4) ring; the
+//                 leader's mbarrier collects the bytes of both CTAs.
 //   warp 1        tensor-memory owner; in the leader, the single MMA issuer.
 //   warp 2        scale-factor producer: the K-block's 512-byte scale tiles
 //                 (A: this CTA's 128 rows; B: all 256 columns) into an 8-deep
@@ -229,9 +229,13 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
     // j counts K-blocks over all tiles this pair processes; every ring slot
     // and phase parity is derived from it.
-    if (warp == 0) {
-        // ------------------------------------------------ A/B TMA producer (both CTAs)
+    if (warp == 0 || warp == 3) {
+        // ------------------------------------------------ A (warp 0) and B (warp 3) TMA producers
+        // Two issuing warps: the copy engine works through the requests of
+        // one issuing thread one after another, so A and B boxes issued from
+        // separate warps stream concurrently (about twice the bytes per SM).
         if (lane == 0) {
+            const bool is_a = warp == 0;
             const uint32_t full0_leader = mapa_shared(smem_u32(&full[0]), 0);
             uint32_t j = 0;
             bool ok = true;
@@ -242,11 +246,15 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 for (int kb = 0; kb < kblocks; ++kb, ++j) {
                     const uint32_t s = j % SAB;
                     if (!mbar_wait(smem_u32(&empty[s]), ((j / SAB) & 1) ^ 1)) { ok = false; break; }
-                    if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * C::AB_BYTES);
                     const uint32_t dst = smem_u32(smem + s * C::AB_BYTES);
                     const uint32_t fb = full0_leader + s * 8;
-                    tma_load_2d_pair(dst, &tmA, fb, kb * 128, arow);
-                    tma_load_2d_pair(dst + C::A_BYTES, &tmB, fb, kb * 128, brow);
+                    if (is_a) {
+                        // the leader's A thread posts the byte count of both CTAs' A and B
+                        if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * C::AB_BYTES);
+                        tma_load_2d_pair(dst, &tmA, fb, kb * 128, arow);
+                    } else {
+                        tma_load_2d_pair(dst + C::A_BYTES, &tmB, fb, kb * 128, brow);
+                    }
                 }
             }
             if (!ok) { record_timeout(); *abort_flag = 1; }
@@ -422,38 +430,48 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const bool row_ok = row < ti.row_end;
             __nv_bfloat16 *dst = p.D + static_cast<size_t>(row_ok ? row : 0) * p.N + ti.n0 + half * 128;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + half * 128;
-            // Drain 128 columns in two halves of 64: each 32-column chunk is
-            // scaled and rounded to BF16 pairs as it arrives and stored.
+            // Drain this warp's 128 columns completely before releasing the
+            // accumulator (the next tile's MMAs wait for that): the first
+            // three 32-column chunks are scaled and rounded to BF16 pairs as
+            // they arrive, the fourth is held as loaded; the global stores
+            // only start after the release.
+            uint32_t packed[3][16];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t packed[2][16];
+            for (int j = 0; j < 3; ++j) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(taddr + j * 32, v);
+                tmem_ld_wait();
+                tmem_regs_after_wait(v);
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(taddr + (2 * h + jj) * 32, v);
-                    tmem_ld_wait();
-                    tmem_regs_after_wait(v);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * gs,
-                                                                  __uint_as_float(v[2 * i + 1]) * gs);
-                        packed[jj][i] = *reinterpret_cast<uint32_t *>(&pr);
-                    }
+                for (int i = 0; i < 16; ++i) {
+                    __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * gs,
+                                                              __uint_as_float(v[2 * i + 1]) * gs);
+                    packed[j][i] = *reinterpret_cast<uint32_t *>(&pr);
                 }
-                if (h == 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
-                }
-                if (row_ok) {
+            }
+            uint32_t last[32];
+            tmem_ld_32x32b_x32(taddr + 3 * 32, last);
+            tmem_ld_wait();
+            tmem_regs_after_wait(last);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
+            if (row_ok) {
 #pragma unroll
-                    for (int jj = 0; jj < 2; ++jj) {
-                        __nv_bfloat16 *d = dst + (2 * h + jj) * 32;
-                        const uint32_t(&q)[16] = packed[jj];
-                        st_global_v8(d, *reinterpret_cast<const uint32_t(*)[8]>(&q[0]));
-                        st_global_v8(d + 16, *reinterpret_cast<const uint32_t(*)[8]>(&q[8]));
-                    }
+                for (int j = 0; j < 3; ++j) {
+                    __nv_bfloat16 *d = dst + j * 32;
+                    st_global_v8(d, *reinterpret_cast<const uint32_t(*)[8]>(&packed[j][0]));
+                    st_global_v8(d + 16, *reinterpret_cast<const uint32_t(*)[8]>(&packed[j][8]));
                 }
+                uint32_t q3[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(last[2 * i]) * gs,
+                                                              __uint_as_float(last[2 * i + 1]) * gs);
+                    q3[i] = *reinterpret_cast<uint32_t *>(&pr);
+                }
+                st_global_v8(dst + 96, *reinterpret_cast<const uint32_t(*)[8]>(&q3[0]));
+                st_global_v8(dst + 112, *reinterpret_cast<const uint32_t(*)[8]>(&q3[8]));
             }
             acc_phase ^= 1;
         }

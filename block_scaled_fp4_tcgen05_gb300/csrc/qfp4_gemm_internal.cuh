@@ -31,11 +31,16 @@ int launch_gemm_pair(int fmt, bool grouped, const CUtensorMap &ma, const CUtenso
 
 int read_clear_status_gemm_pair(cudaStream_t s, uint32_t *out);
 
-// Decode GEMM for M <= 128 (N % 128 == 0): one CTA per (128-column tile, K
-// share), K shares of a tile reduced over a thread-block cluster.
-int decode_split(int64_t N, int64_t K);
-int launch_gemm_decode(int fmt, const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &g,
-                       cudaStream_t s);
+// Decode GEMM for M <= 128 (N % 128 == 0), swap AB on CTA pairs: the
+// weights (B, map mw with 128-row boxes) fill the MMA's M slot, the tokens
+// (A, map mt with 64-row boxes) its N slot; D is written through md (BF16,
+// 128 x 128 boxes, no swizzle).
+int launch_gemm_decode(int fmt, const CUtensorMap &mw, const CUtensorMap &mt, const CUtensorMap &md,
+                       const GemmParams &g, cudaStream_t s);
+// 2D BF16 matrix [rows, cols] (row stride cols * 2 bytes), box of
+// box_cols x box_rows elements, no swizzle: the TMA store map of D.
+int make_map_bf16(CUtensorMap *map, void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                  uint32_t box_rows);
 int read_clear_status_gemm_decode(cudaStream_t s, uint32_t *out);
 
 }  // namespace qfp4

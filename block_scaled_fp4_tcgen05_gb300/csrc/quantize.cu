@@ -99,17 +99,6 @@ __device__ __forceinline__ float ue8m0_inverse(uint32_t c)
                      : __uint_as_float(0x00400000u);          // 2^-127
 }
 
-// Two fp32 -> packed E2M1 byte (first argument in the high nibble), round to
-// nearest even, saturating at +-6, sign kept.
-__device__ __forceinline__ uint32_t e2m1x2(float hi, float lo)
-{
-    uint32_t r;
-    asm("{\n.reg .b8 t;\ncvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\ncvt.u32.u8 %0, t;\n}"
-        : "=r"(r)
-        : "f"(hi), "f"(lo));
-    return r;
-}
-
 struct BlockScale {
     float inv;      // MXFP4: exact 2^-e; NVFP4: RN(1/s)
     float s;        // NVFP4 scale s = decode(sf) * gs
@@ -171,12 +160,74 @@ __device__ __forceinline__ BlockScale block_scale(float amax, float gs, float in
     return b;
 }
 
-template <int FMT>
-__device__ __forceinline__ float quotient(float x, const BlockScale &b)
+// ---- packed fp32 pairs: one f32x2 instruction works on both halves of a
+// 64-bit register pair, halving the arithmetic issue slots of the quotient.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
 {
-    if (FMT == QFP4_MXFP4) return x * b.inv;
-    if (b.mode == 1) return div_markstein(x, b.s, b.inv);
-    return __fdiv_rn(x, b.s);
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// bf16 pair in a 32-bit word -> both values as one fp32 pair (exact).
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w)
+{
+    return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// RN(-x / s) on both halves of x2, from s2 = (s, s) and ny2 = (-y, -y) with
+// y = RN(1/s): the two Markstein corrections of div_markstein applied to the
+// dividend -x.  q0 = x*(-y) = (-x)*y, e = s*q + x = s*q - (-x) and
+// q + e*(-y) = q - e*y are the same roundings as for -x, so the result is
+// div_markstein(-x, s, y) = -RN(x/s), and no negation is ever issued.  Signed
+// zeros come out right: x = +0 gives -0 and x = -0 gives +0.
+__device__ __forceinline__ uint64_t f2_neg_quotient(uint64_t x2, uint64_t s2, uint64_t ny2)
+{
+    uint64_t q = f2_mul(x2, ny2);
+    uint64_t e = f2_fma(s2, q, x2);
+    q = f2_fma(e, ny2, q);
+    e = f2_fma(s2, q, x2);
+    return f2_fma(e, ny2, q);
+}
+
+// E2M1 rounding is symmetric (round to nearest even, saturation at +-6), so
+// the codes of -q are the codes of q with the sign bit of every nibble set
+// the other way.
+constexpr uint32_t kNibbleSigns = 0x88888888u;
+
+// Largest |x| of a block as fp32 (exact): pairwise max of magnitudes on the
+// packed bf16 words (the sign of the result is meaningless and dropped).
+template <int W>
+__device__ __forceinline__ float block_amax(const uint32_t (&w)[W])
+{
+    uint32_t m[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) m[i] = w[i];
+#pragma unroll
+    for (int n = W; n > 1; n >>= 1)
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i)
+            asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[i]) : "r"(m[2 * i]), "r"(m[2 * i + 1]));
+    return fmaxf(fabsf(__uint_as_float(m[0] << 16)), fabsf(__uint_as_float(m[0] & 0xFFFF0000u)));
 }
 
 // Eight fp32 -> four packed bytes: element 2i in the low nibble of byte i.
@@ -194,22 +245,38 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&q)[8])
     return w;
 }
 
-// 8 consecutive elements -> 4 packed bytes.
+// Four bf16 words (8 elements, element 2i in the low half of word i) -> four
+// packed E2M1 bytes (element 2i in the low nibble of byte i).
 template <int FMT>
-__device__ __forceinline__ uint32_t encode8(const float (&x)[8], const BlockScale &b)
+__device__ __forceinline__ uint32_t encode8(const uint32_t *w, const BlockScale &b)
 {
-    if (FMT == QFP4_NVFP4 && b.mode == 0) return 0u;
     float q[8];
+    if (FMT == QFP4_MXFP4) {
+        const uint64_t inv2 = f2_pack(b.inv, b.inv);       // a power of two: exact
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = quotient<FMT>(x[i], b);
+        for (int i = 0; i < 4; ++i) f2_unpack(f2_mul(bf16x2_to_f2(w[i]), inv2), q[2 * i], q[2 * i + 1]);
+        return e2m1x8(q);
+    }
+    if (b.mode == 1) {
+        const uint64_t s2 = f2_pack(b.s, b.s), ny2 = f2_pack(-b.inv, -b.inv);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            f2_unpack(f2_neg_quotient(bf16x2_to_f2(w[i]), s2, ny2), q[2 * i], q[2 * i + 1]);
+        return e2m1x8(q) ^ kNibbleSigns;
+    }
+    if (b.mode == 0) return 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        q[2 * i] = __fdiv_rn(__uint_as_float(w[i] << 16), b.s);
+        q[2 * i + 1] = __fdiv_rn(__uint_as_float(w[i] & 0xFFFF0000u), b.s);
+    }
     return e2m1x8(q);
 }
 
-__device__ __forceinline__ int64_t sf_mma_offset(int64_t row_tile, int64_t r_in_tile, int64_t c,
-                                                 int64_t kc)
+__device__ __forceinline__ uint32_t sf_mma_offset(uint32_t row_tile, uint32_t r_in_tile, uint32_t c,
+                                                  uint32_t kc)
 {
-    return (row_tile * kc + (c >> 2)) * 512 + (r_in_tile & 31) * 16 + (r_in_tile >> 5) * 4 +
-           (c & 3);
+    return (row_tile * kc + (c >> 2)) * 512u + (r_in_tile & 31u) * 16u + (r_in_tile >> 5) * 4u + (c & 3u);
 }
 
 // Group of a row (row_offsets sorted; offs has groups+1 entries in smem).
@@ -225,29 +292,44 @@ __device__ __forceinline__ int find_group(const int32_t *offs, int groups, int64
 
 constexpr int kQStages = 4;
 
-// BF16 bytes per pipeline stage: one scale block per thread (8 KB NVFP4,
-// 16 KB MXFP4), small enough for four CTAs per SM.
+// Scale blocks per thread per pipeline stage.  NVFP4 takes two (16 KB
+// stages): the per-stage wait, release and refill are then paid once per two
+// blocks; MXFP4 blocks are twice as long, one per thread fills 16 KB.
 template <int FMT>
-__host__ __device__ constexpr int chunk_bytes() { return kThreads * 2 * (FMT == QFP4_MXFP4 ? 32 : 16); }
+__host__ __device__ constexpr int blocks_per_thread() { return FMT == QFP4_MXFP4 ? 1 : 2; }
+
+template <int FMT>
+__host__ __device__ constexpr int chunk_bytes()
+{
+    return kThreads * blocks_per_thread<FMT>() * 2 * (FMT == QFP4_MXFP4 ? 32 : 16);
+}
+
+// floor(n / d) for n < 2^32 as the high half of n * m with m = floor(2^64/d) + 1
+// (d >= 2): n*m/2^64 = n/d + n*(m - 2^64/d)/2^64, and the second term is below
+// 2^-32 <= 1/d, less than the distance from n/d to the next integer.
+__host__ __device__ constexpr uint64_t div_magic(uint64_t d) { return ~0ull / d + 1; }
 
 // Persistent quantiser fed by bulk copies: each CTA walks 16 KB chunks of the
 // flat BF16 input (rows are contiguous, and a chunk holds whole scale
 // blocks), one thread keeps kQStages chunks in flight through mbarriers, and
-// every thread encodes whole scale blocks from shared memory.  GROUPED:
-// per-row global scale gs[group] and the per-group MMA scale layout.
+// every thread encodes whole scale blocks from shared memory.  Consecutive
+// threads take consecutive blocks, so the four scale bytes of one 32-bit word
+// of the scale layout come from four neighbouring lanes.  GROUPED: per-row
+// global scale gs[group] and the per-group MMA scale layout.
 template <int FMT, int SF_LAYOUT, bool GROUPED>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, 3)
 quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
                 const float *__restrict__ gs_ptr, uint8_t *__restrict__ Q,
                 uint8_t *__restrict__ SF, int64_t M, int groups,
-                const int32_t *__restrict__ row_offsets)
+                const int32_t *__restrict__ row_offsets, uint64_t kg_magic)
 {
     constexpr int G = FMT == QFP4_MXFP4 ? 32 : 16;
+    constexpr int W = G / 2;                            // bf16 words per block
+    constexpr int BPT = blocks_per_thread<FMT>();
     constexpr int kChunkBytes = chunk_bytes<FMT>();
     constexpr int BPC = kChunkBytes / (2 * G);          // scale blocks per chunk
-    constexpr int BPT = BPC / kThreads;                 // per thread per chunk
-    static_assert(BPC % kThreads == 0 && BPT >= 1, "chunk / thread mismatch");
-    const int64_t kg = K / G, kc = kg / 4;
+    static_assert(BPC == BPT * kThreads, "chunk / thread mismatch");
+    const uint32_t kg = static_cast<uint32_t>(K / G), kc = kg / 4;
     extern __shared__ __align__(128) uint8_t qsmem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(qsmem + kQStages * kChunkBytes);
     uint64_t *empty = full + kQStages;
@@ -282,7 +364,9 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
         for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < pad;
              i += (int64_t)gridDim.x * blockDim.x) {
             const int64_t r = M + i / kc, c4 = i % kc;
-            *reinterpret_cast<uint32_t *>(SF + sf_mma_offset(r / 128, r % 128, c4 * 4, kc)) = 0u;
+            *reinterpret_cast<uint32_t *>(SF + sf_mma_offset(static_cast<uint32_t>(r / 128),
+                                                             static_cast<uint32_t>(r % 128),
+                                                             static_cast<uint32_t>(c4 * 4), kc)) = 0u;
         }
     }
 
@@ -311,33 +395,24 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
         const uint32_t ph = (it / kQStages) & 1;
         if (!mbar_wait(smem_u32(&full[st]), ph)) { ok = false; break; }
         const uint8_t *chunk = qsmem + st * kChunkBytes;
-        const int64_t b0 = c * BPC;
+        // block indices fit 32 bits (checked on the host)
+        const uint32_t b0 = static_cast<uint32_t>(c * BPC);
 #pragma unroll
         for (int u = 0; u < BPT; ++u) {
             const int local = u * kThreads + threadIdx.x;   // consecutive threads, consecutive blocks
-            const int64_t bu = b0 + local;
-            const bool valid = bu < total_blocks;
-            float x[G];
+            const uint32_t bu = b0 + static_cast<uint32_t>(local);
+            const bool valid = bu < static_cast<uint64_t>(total_blocks);
+            uint32_t w[W];
 #pragma unroll
-            for (int h = 0; h < G / 16; ++h) {
-                const uint4 v0 = *reinterpret_cast<const uint4 *>(chunk + local * (2 * G) + h * 32);
-                const uint4 v1 = *reinterpret_cast<const uint4 *>(chunk + local * (2 * G) + h * 32 + 16);
-                bf16x2_to_f32(v0.x, x[16 * h + 0], x[16 * h + 1]);
-                bf16x2_to_f32(v0.y, x[16 * h + 2], x[16 * h + 3]);
-                bf16x2_to_f32(v0.z, x[16 * h + 4], x[16 * h + 5]);
-                bf16x2_to_f32(v0.w, x[16 * h + 6], x[16 * h + 7]);
-                bf16x2_to_f32(v1.x, x[16 * h + 8], x[16 * h + 9]);
-                bf16x2_to_f32(v1.y, x[16 * h + 10], x[16 * h + 11]);
-                bf16x2_to_f32(v1.z, x[16 * h + 12], x[16 * h + 13]);
-                bf16x2_to_f32(v1.w, x[16 * h + 14], x[16 * h + 15]);
+            for (int h = 0; h < W / 4; ++h) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(chunk + local * (2 * G) + h * 16);
+                w[4 * h] = v.x; w[4 * h + 1] = v.y; w[4 * h + 2] = v.z; w[4 * h + 3] = v.w;
             }
-            float amax = 0.0f;
-#pragma unroll
-            for (int i = 0; i < G; ++i) amax = fmaxf(amax, fabsf(x[i]));
+            const float amax = block_amax(w);
+            const uint32_t row = static_cast<uint32_t>(__umul64hi(bu, kg_magic));
             int grp = 0;
             float gs = gs_one, inv_gs = inv_gs_one;
             if (GROUPED && valid) {
-                const int64_t row = static_cast<uint32_t>(bu) / static_cast<uint32_t>(kg);
                 grp = find_group(s_offs, groups, row);
                 if (FMT == QFP4_NVFP4 && gs_ptr) {
                     gs = gs_ptr[grp];
@@ -345,17 +420,12 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
                 }
             }
             const BlockScale bs = block_scale<FMT>(amax, gs, inv_gs);
-            uint32_t packed[G / 8];
+            uint32_t packed[W / 4];
 #pragma unroll
-            for (int w = 0; w < G / 8; ++w) {
-                float xx[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) xx[i] = x[8 * w + i];
-                packed[w] = encode8<FMT>(xx, bs);
-            }
+            for (int v = 0; v < W / 4; ++v) packed[v] = encode8<FMT>(&w[4 * v], bs);
             if (valid) {
-                if (G == 16) *reinterpret_cast<uint2 *>(Q + bu * (G / 2)) = make_uint2(packed[0], packed[1]);
-                else *reinterpret_cast<uint4 *>(Q + bu * (G / 2)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                if (G == 16) *reinterpret_cast<uint2 *>(Q + static_cast<size_t>(bu) * (G / 2)) = make_uint2(packed[0], packed[1]);
+                else *reinterpret_cast<uint4 *>(Q + static_cast<size_t>(bu) * (G / 2)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             }
             // Scale bytes: lanes 4i..4i+3 hold four consecutive blocks of one row.
             const uint32_t c1 = __shfl_down_sync(0xffffffffu, bs.code, 1);
@@ -363,12 +433,11 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
             const uint32_t c3 = __shfl_down_sync(0xffffffffu, bs.code, 3);
             if (valid && (lane & 3) == 0) {
                 const uint32_t word = bs.code | (c1 << 8) | (c2 << 16) | (c3 << 24);
-                const uint32_t row = static_cast<uint32_t>(bu) / static_cast<uint32_t>(kg);
-                const uint32_t col = static_cast<uint32_t>(bu) - row * static_cast<uint32_t>(kg);
-                int64_t off;
+                const uint32_t col = bu - row * kg;
+                size_t off;
                 if (GROUPED) {
-                    const int64_t rr = row - s_offs[grp];
-                    off = sf_mma_offset(s_tile0[grp] + rr / 128, rr % 128, col, kc);
+                    const uint32_t rr = row - static_cast<uint32_t>(s_offs[grp]);
+                    off = sf_mma_offset(static_cast<uint32_t>(s_tile0[grp]) + rr / 128, rr % 128, col, kc);
                 } else if (SF_LAYOUT == QFP4_SF_MMA) {
                     off = sf_mma_offset(row / 128, row % 128, col, kc);
                 } else {
@@ -397,15 +466,19 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
 }
 
 // amax over rows of X, one warp per row; per group via atomicMax on the bit
-// pattern (non-negative floats order like unsigned integers).
+// pattern (non-negative floats order like unsigned integers).  Without
+// groups the warps of a CTA first fold their maxima in shared memory, so
+// that one atomic per CTA (not per row) reaches the single global word.
 __global__ void __launch_bounds__(kThreads)
 amax_rows_kernel(const uint4 *__restrict__ X, int64_t rows, int64_t chunks_per_row, int groups,
                  const int32_t *__restrict__ row_offsets, uint32_t *__restrict__ amax_bits)
 {
     __shared__ int32_t s_offs[kMaxGroups + 1];
+    __shared__ uint32_t s_max;
     if (row_offsets) {
         for (int i = threadIdx.x; i <= groups; i += blockDim.x) s_offs[i] = row_offsets[i];
     }
+    if (threadIdx.x == 0) s_max = 0u;
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
@@ -451,7 +524,13 @@ amax_rows_kernel(const uint4 *__restrict__ X, int64_t rows, int64_t chunks_per_r
         }
         run = fmaxf(run, m);
     }
-    if (cur >= 0 && lane == 0) atomicMax(amax_bits + cur, __float_as_uint(run));
+    if (row_offsets) {
+        if (cur >= 0 && lane == 0) atomicMax(amax_bits + cur, __float_as_uint(run));
+        return;
+    }
+    if (cur >= 0 && lane == 0) atomicMax(&s_max, __float_as_uint(run));
+    __syncthreads();
+    if (threadIdx.x == 0 && s_max != 0u) atomicMax(amax_bits, s_max);
 }
 
 // gs = amax / (6 * 448), in place over the amax bit patterns.
@@ -523,11 +602,11 @@ cudaError_t launch_quantize(const void *X, int64_t M, int64_t K, const float *gs
         configured_device = dev;
     }
     const int sms = sm_count();
-    int64_t grid = static_cast<int64_t>(sms > 0 ? sms : 148) * (FMT == QFP4_MXFP4 ? 3 : 4);
+    int64_t grid = static_cast<int64_t>(sms > 0 ? sms : 148) * 3;
     if (chunks < grid) grid = chunks > 0 ? chunks : 1;
     kern<<<static_cast<int>(grid), kThreads, smem, s>>>(
         static_cast<const uint8_t *>(X), blocks, K, gs, static_cast<uint8_t *>(Q),
-        static_cast<uint8_t *>(SF), M, groups, offs);
+        static_cast<uint8_t *>(SF), M, groups, offs, div_magic(static_cast<uint64_t>(K / G)));
     return cudaGetLastError();
 }
 
@@ -601,7 +680,9 @@ extern "C" int qfp4_quantize(int fmt, const void *X_bf16, int64_t M, int64_t K, 
     if (M < 0 || K < 0) return QFP4_ERR_INVALID_ARG;
     if (K % 128 != 0) return QFP4_ERR_UNSUPPORTED;
     if (M == 0 || K == 0) return QFP4_OK;
-    if (M * (K / 16) >= (int64_t{1} << 32)) return QFP4_ERR_UNSUPPORTED;   // 32-bit block index
+    // 32-bit block indices and scale offsets, with room for the last chunk
+    // and the padded scale rows
+    if ((M + 128) * (K / 16) >= (int64_t{1} << 32) - 4096) return QFP4_ERR_UNSUPPORTED;
     if (!X_bf16 || !Q_packed || !SF) return QFP4_ERR_INVALID_ARG;
     if (fmt == QFP4_NVFP4 && !gs) return QFP4_ERR_INVALID_ARG;
     if (!aligned16(X_bf16) || !aligned16(Q_packed) || !aligned4(SF) || (gs && !aligned4(gs)))
@@ -626,7 +707,7 @@ extern "C" int qfp4_quantize_grouped(int fmt, const void *X_bf16, int64_t total_
     if (fmt != QFP4_MXFP4 && fmt != QFP4_NVFP4) return QFP4_ERR_INVALID_ARG;
     if (total_rows < 0 || K < 0 || groups < 1 || !row_offsets) return QFP4_ERR_INVALID_ARG;
     if (groups > kMaxGroups || K % 128 != 0) return QFP4_ERR_UNSUPPORTED;
-    if (total_rows * (K / 16) >= (int64_t{1} << 32)) return QFP4_ERR_UNSUPPORTED;
+    if ((total_rows + 128 * (groups + 1)) * (K / 16) >= (int64_t{1} << 32) - 4096) return QFP4_ERR_UNSUPPORTED;
     if (fmt == QFP4_NVFP4 && !gs) return QFP4_ERR_INVALID_ARG;
     if (!X_bf16 || !Q_packed || !SF_mma) return QFP4_ERR_INVALID_ARG;
     if (!aligned16(X_bf16) || !aligned16(Q_packed) || !aligned4(SF_mma) || !aligned4(row_offsets) ||

@@ -181,9 +181,9 @@ size_t qfp4_gemm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K);
  *   workspace  DEVICE scratch of ws_bytes >= qfp4_gemm_workspace_bytes(...);
  *              currently unused (NULL is fine).
  * Tensor cores: tcgen05.mma kind::mxf4 (MXFP4) / kind::mxf4nvf4 scale_vec::4X
- * (NVFP4), fp32 accumulation in tensor memory.  Kernels: M <= 128: one CTA
- * per 128-column tile and K share, the K shares of a tile reduced in rank
- * order over a thread-block cluster (deterministic); M > 128 and
+ * (NVFP4), fp32 accumulation in tensor memory.  Kernels: M <= 128: CTA
+ * pairs with A and B swapped (256 weight rows per pair in the MMA's M slot,
+ * the tokens in its N slot, all of K per pair, no split-K); M > 128 and
  * N % 256 == 0: CTA pairs (cta_group::2) on 256 x 256 tiles; otherwise
  * single-CTA 128 x 128 / 128 x 256 tiles.
  * Requirements: M >= 1, N % 128 == 0, K % 128 == 0, all pointers 16-byte

@@ -252,15 +252,16 @@ def test_grouped_moe_up_projection():
     assert worst <= 1.0
 
 
-# ----------------------------------------------------------------- decode (split-K)
+# ----------------------------------------------------------------- decode (M <= 128)
 
 @pytest.mark.parametrize("fmt", [MX, NV])
 @pytest.mark.parametrize("M,N,K", [(1, 128, 256), (37, 384, 1024), (128, 1024, 4096), (100, 2048, 2304),
                                    (128, 4096, 128), (64, 256, 8192)])
-def test_decode_split_k_shapes(fmt, M, N, K):
-    """M <= 128 runs the decode kernel, K split over a CTA cluster for small
-    N: must match the oracle and be bit-identical across repeated calls (the
-    cluster reduction adds the partial tiles in a fixed order)."""
+def test_decode_shapes(fmt, M, N, K):
+    """M <= 128 runs the decode kernel (A and B swapped on CTA pairs; ragged
+    token counts, a weight tile of only 128 rows, and a trailing half K-block
+    among the shapes): must match the oracle and be bit-identical across
+    repeated calls."""
     A, Asf, B, Bsf = random_operands(fmt, M, N, K, M + N + K + 3 * fmt)
     gs_a, gs_b = (None, None) if fmt == MX else (0.125, 3.0)
     g = qfp4.block_size(fmt)

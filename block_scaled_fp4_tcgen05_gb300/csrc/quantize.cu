@@ -290,7 +290,7 @@ __device__ __forceinline__ int find_group(const int32_t *offs, int groups, int64
     return lo;
 }
 
-constexpr int kQStages = 4;
+constexpr int kQStages = 3;
 
 // Scale blocks per thread per pipeline stage.  NVFP4 takes two (16 KB
 // stages): the per-stage wait, release and refill are then paid once per two
@@ -317,7 +317,7 @@ __host__ __device__ constexpr uint64_t div_magic(uint64_t d) { return ~0ull / d 
 // of the scale layout come from four neighbouring lanes.  GROUPED: per-row
 // global scale gs[group] and the per-group MMA scale layout.
 template <int FMT, int SF_LAYOUT, bool GROUPED>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, 4)
 quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
                 const float *__restrict__ gs_ptr, uint8_t *__restrict__ Q,
                 uint8_t *__restrict__ SF, int64_t M, int groups,
@@ -602,7 +602,9 @@ cudaError_t launch_quantize(const void *X, int64_t M, int64_t K, const float *gs
         configured_device = dev;
     }
     const int sms = sm_count();
-    int64_t grid = static_cast<int64_t>(sms > 0 ? sms : 148) * 3;
+    // four CTAs (32 warps) per SM: the per-block scale arithmetic is a
+    // dependent chain, and more warps hide it
+    int64_t grid = static_cast<int64_t>(sms > 0 ? sms : 148) * 4;
     if (chunks < grid) grid = chunks > 0 ? chunks : 1;
     kern<<<static_cast<int>(grid), kThreads, smem, s>>>(
         static_cast<const uint8_t *>(X), blocks, K, gs, static_cast<uint8_t *>(Q),

@@ -117,7 +117,8 @@ def random_operands(fmt, M, N, K, seed):
 
 @pytest.mark.parametrize("fmt", [MX, NV])
 @pytest.mark.parametrize("M,N,K", [(1, 128, 128), (100, 256, 384), (128, 384, 256),
-                                   (300, 640, 1024), (513, 256, 2048), (256, 1280, 640)])
+                                   (300, 640, 1024), (513, 256, 2048), (256, 1280, 640),
+                                   (300, 512, 1024), (640, 1536, 768), (1100, 2048, 384)])
 def test_random_shapes(fmt, M, N, K):
     A, Asf, B, Bsf = random_operands(fmt, M, N, K, M * 7 + N + K + fmt)
     gs_a, gs_b = (None, None) if fmt == MX else (0.37, 2.5e-3)

@@ -125,7 +125,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     const int kc = (K / C::G) / 4;                     // 512-B SF tiles per 128 rows
     const int ntiles_n = args.N / BN;
 
-    // ---- tile count and group tables
+    // ---- tile count and group tables (the group offsets are the first
+    // global reads: wait for the previous kernel before them)
+    if (GROUPED) pdl_wait();
     int32_t total_tiles;
     if (GROUPED) {
         for (int i = threadIdx.x; i <= args.groups; i += blockDim.x) s_offs[i] = args.row_offsets[i];
@@ -167,6 +169,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (!GROUPED) pdl_wait();
+    pdl_launch_dependents();
 
     // Tile t -> coordinates.  Non-grouped: groups of 8 row-tiles sweep the
     // columns together so that a wave of CTAs shares A and B in L2.
@@ -432,8 +436,7 @@ int launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &a,
     const int sms = sm_count();
     if (sms <= 0) return QFP4_ERR_CUDA;
     const int grid = tiles < sms ? (tiles > 0 ? tiles : 1) : sms;
-    kern<<<grid, kThreads, C::SMEM, s>>>(ma, mb, a);
-    return launch_status(cudaGetLastError());
+    return launch_status(launch_pdl(kern, dim3(grid), dim3(kThreads), C::SMEM, s, ma, mb, a));
 }
 
 }  // namespace

@@ -149,6 +149,10 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // everything above overlaps the previous kernel's tail; global memory
+    // is touched only from here on
+    pdl_wait();
+    pdl_launch_dependents();
 
     if (warp == 0 || warp == 3) {
         // ------------------------------------------------ weight (warp 0) / token (warp 3) TMA producers
@@ -355,8 +359,7 @@ int launch_decode(const CUtensorMap &mw, const CUtensorMap &mt, const CUtensorMa
         configured_device = dev;
     }
     const int pairs = (g.N + 255) / 256;
-    kern<<<2 * pairs, kThreads, C::SMEM, s>>>(mw, mt, md, g);
-    return launch_status(cudaGetLastError());
+    return launch_status(launch_pdl(kern, dim3(2 * pairs), dim3(kThreads), C::SMEM, s, mw, mt, md, g));
 }
 
 }  // namespace

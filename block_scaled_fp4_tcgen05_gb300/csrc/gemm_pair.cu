@@ -143,6 +143,9 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const int32_t pair_id = blockIdx.x >> 1;
     const int32_t npairs = gridDim.x >> 1;
 
+    // the group offsets are the first global reads: wait for the previous
+    // kernel before them
+    if (GROUPED) pdl_wait();
     int32_t total_tiles;
     if (GROUPED) {
         for (int i = threadIdx.x; i <= p.groups; i += blockDim.x) s_offs[i] = p.row_offsets[i];
@@ -192,6 +195,8 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (!GROUPED) pdl_wait();
+    pdl_launch_dependents();
 
     auto tile_info = [&](int32_t t) {
         PairTile ti;
@@ -513,8 +518,8 @@ int launch(const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &prm, 
     if (sms < 2) return QFP4_ERR_CUDA;
     int64_t pairs = sms / 2;
     if (pair_tiles < pairs) pairs = pair_tiles > 0 ? pair_tiles : 1;
-    kern<<<static_cast<int>(2 * pairs), kThreads, C::SMEM, s>>>(ma, mb, prm);
-    return launch_status(cudaGetLastError());
+    return launch_status(launch_pdl(kern, dim3(static_cast<unsigned>(2 * pairs)), dim3(kThreads), C::SMEM, s,
+                                    ma, mb, prm));
 }
 
 }  // namespace

@@ -31,6 +31,42 @@ inline int sm_count()
     return n;
 }
 
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with programmatic stream serialisation: it may start (set up barriers,
+// tensor memory and descriptors) while the previous kernel on the stream is
+// still finishing, and it calls pdl_wait() before its first access to global
+// memory; that returns once the previous kernel has completed and its writes
+// are visible.  A preceding kernel that was launched without this attribute
+// (any other library's) is simply waited for in full.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allows the next kernel on the stream to begin launching now (it still
+// waits for this kernel to complete before it touches memory).
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Per-unit status readers (defined in each .cu that owns a status word).
 int read_clear_status_quant(cudaStream_t s, uint32_t *out);
 int read_clear_status_gemm(cudaStream_t s, uint32_t *out);

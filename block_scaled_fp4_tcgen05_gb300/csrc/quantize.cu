@@ -335,6 +335,8 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
     uint64_t *empty = full + kQStages;
     __shared__ int32_t s_offs[GROUPED ? kMaxGroups + 1 : 1];
     __shared__ int32_t s_tile0[GROUPED ? kMaxGroups : 1];
+    pdl_wait();                 // first global access below
+    pdl_launch_dependents();
     if (GROUPED) {
         for (int i = threadIdx.x; i <= groups; i += blockDim.x) s_offs[i] = row_offsets[i];
     }
@@ -475,6 +477,8 @@ amax_rows_kernel(const uint4 *__restrict__ X, int64_t rows, int64_t chunks_per_r
 {
     __shared__ int32_t s_offs[kMaxGroups + 1];
     __shared__ uint32_t s_max;
+    pdl_wait();
+    pdl_launch_dependents();
     if (row_offsets) {
         for (int i = threadIdx.x; i <= groups; i += blockDim.x) s_offs[i] = row_offsets[i];
     }
@@ -536,6 +540,8 @@ amax_rows_kernel(const uint4 *__restrict__ X, int64_t rows, int64_t chunks_per_r
 // gs = amax / (6 * 448), in place over the amax bit patterns.
 __global__ void gs_finalize_kernel(uint32_t *bits, int n)
 {
+    pdl_wait();
+    pdl_launch_dependents();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) {
         const float amax = __uint_as_float(bits[i]);
@@ -549,6 +555,8 @@ __global__ void __launch_bounds__(kThreads)
 sf_interleave_kernel(const uint8_t *__restrict__ in, uint8_t *__restrict__ out, int64_t rows,
                      int64_t cols, int64_t kc, int64_t words)
 {
+    pdl_wait();
+    pdl_launch_dependents();
     for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < words;
          w += (int64_t)gridDim.x * blockDim.x) {
         const int64_t tile = w >> 7, within = w & 127;
@@ -606,10 +614,9 @@ cudaError_t launch_quantize(const void *X, int64_t M, int64_t K, const float *gs
     // dependent chain, and more warps hide it
     int64_t grid = static_cast<int64_t>(sms > 0 ? sms : 148) * 4;
     if (chunks < grid) grid = chunks > 0 ? chunks : 1;
-    kern<<<static_cast<int>(grid), kThreads, smem, s>>>(
-        static_cast<const uint8_t *>(X), blocks, K, gs, static_cast<uint8_t *>(Q),
-        static_cast<uint8_t *>(SF), M, groups, offs, div_magic(static_cast<uint64_t>(K / G)));
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, s,
+                      static_cast<const uint8_t *>(X), blocks, K, gs, static_cast<uint8_t *>(Q),
+                      static_cast<uint8_t *>(SF), M, groups, offs, div_magic(static_cast<uint64_t>(K / G)));
 }
 
 }  // namespace
@@ -642,13 +649,12 @@ extern "C" int qfp4_global_scale(const void *X_bf16, int64_t rows, int64_t cols,
     if (cudaMemsetAsync(gs_out, 0, sizeof(float), s) != cudaSuccess) return QFP4_ERR_CUDA;
     if (rows > 0 && cols > 0) {
         const int grid = grid_for(rows, kThreads / 32);
-        amax_rows_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint4 *>(X_bf16), rows,
-                                                   cols / 8, 1, nullptr,
-                                                   reinterpret_cast<uint32_t *>(gs_out));
-        if (cudaGetLastError() != cudaSuccess) return QFP4_ERR_CUDA;
+        if (launch_pdl(amax_rows_kernel, dim3(grid), dim3(kThreads), 0, s, static_cast<const uint4 *>(X_bf16),
+                       rows, cols / 8, 1, nullptr, reinterpret_cast<uint32_t *>(gs_out)) != cudaSuccess)
+            return QFP4_ERR_CUDA;
     }
-    gs_finalize_kernel<<<1, 32, 0, s>>>(reinterpret_cast<uint32_t *>(gs_out), 1);
-    return launch_status(cudaGetLastError());
+    return launch_status(launch_pdl(gs_finalize_kernel, dim3(1), dim3(32), 0, s,
+                                    reinterpret_cast<uint32_t *>(gs_out), 1));
 }
 
 extern "C" int qfp4_global_scale_grouped(const void *X_bf16, int64_t total_rows, int64_t cols,
@@ -664,14 +670,13 @@ extern "C" int qfp4_global_scale_grouped(const void *X_bf16, int64_t total_rows,
     if (cudaMemsetAsync(gs_out, 0, sizeof(float) * groups, s) != cudaSuccess) return QFP4_ERR_CUDA;
     if (total_rows > 0 && cols > 0) {
         const int grid = grid_for(total_rows, kThreads / 32);
-        amax_rows_kernel<<<grid, kThreads, 0, s>>>(
-            static_cast<const uint4 *>(X_bf16), total_rows, cols / 8, static_cast<int>(groups),
-            row_offsets, reinterpret_cast<uint32_t *>(gs_out));
-        if (cudaGetLastError() != cudaSuccess) return QFP4_ERR_CUDA;
+        if (launch_pdl(amax_rows_kernel, dim3(grid), dim3(kThreads), 0, s, static_cast<const uint4 *>(X_bf16),
+                       total_rows, cols / 8, static_cast<int>(groups), row_offsets,
+                       reinterpret_cast<uint32_t *>(gs_out)) != cudaSuccess)
+            return QFP4_ERR_CUDA;
     }
-    gs_finalize_kernel<<<(static_cast<int>(groups) + 127) / 128, 128, 0, s>>>(
-        reinterpret_cast<uint32_t *>(gs_out), static_cast<int>(groups));
-    return launch_status(cudaGetLastError());
+    return launch_status(launch_pdl(gs_finalize_kernel, dim3((static_cast<unsigned>(groups) + 127) / 128), dim3(128),
+                                    0, s, reinterpret_cast<uint32_t *>(gs_out), static_cast<int>(groups)));
 }
 
 extern "C" int qfp4_quantize(int fmt, const void *X_bf16, int64_t M, int64_t K, const float *gs,
@@ -740,10 +745,10 @@ extern "C" int qfp4_sf_interleave(const void *SF_in, int64_t rows, int64_t cols,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int grid = grid_for(words, kThreads);
     if (layout == QFP4_SF_MMA)
-        sf_interleave_kernel<true><<<grid, kThreads, 0, s>>>(
-            static_cast<const uint8_t *>(SF_in), static_cast<uint8_t *>(SF_out), rows, cols, kc, words);
-    else
-        sf_interleave_kernel<false><<<grid, kThreads, 0, s>>>(
-            static_cast<const uint8_t *>(SF_in), static_cast<uint8_t *>(SF_out), rows, cols, kc, words);
-    return launch_status(cudaGetLastError());
+        return launch_status(launch_pdl(sf_interleave_kernel<true>, dim3(grid), dim3(kThreads), 0, s,
+                                        static_cast<const uint8_t *>(SF_in), static_cast<uint8_t *>(SF_out), rows,
+                                        cols, kc, words));
+    return launch_status(launch_pdl(sf_interleave_kernel<false>, dim3(grid), dim3(kThreads), 0, s,
+                                    static_cast<const uint8_t *>(SF_in), static_cast<uint8_t *>(SF_out), rows, cols,
+                                    kc, words));
 }

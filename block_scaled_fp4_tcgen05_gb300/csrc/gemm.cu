@@ -456,10 +456,20 @@ extern "C" int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K, const void
                             size_t ws_bytes, void *stream)
 {
     if (fmt != QFP4_MXFP4 && fmt != QFP4_NVFP4) return QFP4_ERR_INVALID_ARG;
-    if (M < 1 || N < 1 || K < 1) return QFP4_ERR_INVALID_ARG;
-    if (!A_packed || !A_sf || !B_packed || !B_sf || !D_bf16) return QFP4_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0) return QFP4_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return QFP4_OK;            // empty D: nothing to do, nothing launched
+    if (!D_bf16) return QFP4_ERR_INVALID_ARG;
     if (N % 128 != 0 || K % 128 != 0 || M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2)
         return QFP4_ERR_UNSUPPORTED;
+    if (K == 0) {
+        // an empty sum: D = 0 (BF16 +0 is all-zero bits)
+        if (!aligned16(D_bf16)) return QFP4_ERR_MISALIGNED;
+        return cudaMemsetAsync(D_bf16, 0, static_cast<size_t>(M) * static_cast<size_t>(N) * 2,
+                               static_cast<cudaStream_t>(stream)) == cudaSuccess
+                   ? QFP4_OK
+                   : QFP4_ERR_CUDA;
+    }
+    if (!A_packed || !A_sf || !B_packed || !B_sf) return QFP4_ERR_INVALID_ARG;
     if (!aligned16(A_packed) || !aligned16(A_sf) || !aligned16(B_packed) || !aligned16(B_sf) ||
         !aligned16(D_bf16) || (gs_a && !aligned4(gs_a)) || (gs_b && !aligned4(gs_b)))
         return QFP4_ERR_MISALIGNED;

@@ -82,7 +82,9 @@ def test_gemm_rejects_bad_arguments(lib):
         return L(*a)
 
     assert call(0, 3) == -1
-    assert call(1, 0) == -1
+    assert call(1, -1) == -1
+    assert call(1, 0) == 0                      # empty D: nothing to do, nothing launched
+    assert call(2, 0) == 0
     assert call(2, 100) == -2                   # N % 128
     assert call(3, 192) == -2                   # K % 128
     assert call(4, None) == -1

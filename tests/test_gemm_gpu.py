@@ -330,3 +330,19 @@ def test_grouped_equals_dense_per_group(N):
         torch.cuda.synchronize()
         same = torch.equal(De.view(torch.int16), outs[0][offs[e]:offs[e + 1]].view(torch.int16))
         assert same, f"group {e} ({m} rows) differs from the dense launch"
+
+
+# ----------------------------------------------------------------- degenerate shapes
+
+def test_degenerate_shapes():
+    """M == 0 or N == 0: nothing to compute; K == 0: an empty sum, D == 0."""
+    D = torch.full((4, 256), 7.0, dtype=torch.bfloat16, device="cuda")
+    z = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    qfp4.gemm_nt(NV, 0, 256, 256, z, z, z, z, None, None, D)
+    qfp4.gemm_nt(NV, 4, 0, 256, z, z, z, z, None, None, D)
+    torch.cuda.synchronize()
+    assert bool((D.float() == 7.0).all())
+    qfp4.gemm_nt(NV, 4, 256, 0, z, z, z, z, None, None, D)
+    torch.cuda.synchronize()
+    assert qfp4.poll_device_status() == 0
+    assert bool((D.float() == 0.0).all()) and not bool(torch.signbit(D.float()).any())

@@ -489,11 +489,13 @@ extern "C" int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K, const void
         return launch_gemm_decode(fmt, mb, ma, md, a, s);
     }
     if (N % 256 == 0 && M > 128) {
-        // CTA pairs on 256 x 256 tiles
+        // CTA pairs on 256 x 256 tiles; D leaves in 32-row x 16-column boxes
+        CUtensorMap md;
         int rc = make_map(&ma, A_packed, K / 2, M, kBKBytes, 128);
         if (rc == QFP4_OK) rc = make_map(&mb, B_packed, K / 2, N, kBKBytes, 128);
+        if (rc == QFP4_OK) rc = make_map_bf16(&md, D_bf16, N, M, 16, 32);
         if (rc != QFP4_OK) return rc;
-        return launch_gemm_pair(fmt, false, ma, mb, a, ((M + 255) / 256) * (N / 256), s);
+        return launch_gemm_pair(fmt, false, ma, mb, md, a, ((M + 255) / 256) * (N / 256), s);
     }
     const bool wide = N % 256 == 0;
     int rc = make_map(&ma, A_packed, K / 2, M, kBKBytes, kBM);
@@ -534,11 +536,13 @@ extern "C" int qfp4_gemm_nt_grouped(int fmt, int64_t groups, const int32_t *row_
     CUtensorMap ma, mb;
     (void)max_group_rows;
     if (N % 256 == 0) {
+        CUtensorMap md;
         int rc = make_map(&ma, A_packed, K / 2, total_rows, kBKBytes, 128);
         if (rc == QFP4_OK) rc = make_map(&mb, B_packed, K / 2, groups * N, kBKBytes, 128);
+        if (rc == QFP4_OK) rc = make_map_bf16(&md, D_bf16, N, total_rows, 16, 32);
         if (rc != QFP4_OK) return rc;
         // upper bound on pair tiles: every group may add one partial tile
-        return launch_gemm_pair(fmt, true, ma, mb, a, ((total_rows + 255) / 256 + groups) * (N / 256), s);
+        return launch_gemm_pair(fmt, true, ma, mb, md, a, ((total_rows + 255) / 256 + groups) * (N / 256), s);
     }
     int rc = make_map(&ma, A_packed, K / 2, total_rows, kBKBytes, kBM);
     if (rc == QFP4_OK) rc = make_map(&mb, B_packed, K / 2, groups * N, kBKBytes, 128);

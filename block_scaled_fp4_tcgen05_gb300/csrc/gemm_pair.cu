@@ -29,8 +29,9 @@
 //                 and only B's scales are replicated across the quarters.
 //   warps 12..19  epilogue: drain 128 rows x 256 columns of the accumulator in
 //                 two halves (scaled by gs_a * gs_b and rounded to BF16 on the
-//                 way), release it, and store while the next tile's main loop
-//                 runs.
+//                 way), release it once all eight have drained, and store it
+//                 through per-warp staging boxes with TMA stores while the
+//                 next tile's main loop runs.
 // Hand-offs between the CTAs use cluster-scope mbarrier arrivals; the ones
 // that only order tensor-memory writes (already complete after
 // tcgen05.wait::st and fenced) are relaxed, which keeps them off the
@@ -68,12 +69,14 @@ namespace {
 constexpr int kThreads = 640;          // 20 warps
 constexpr int kMaxGroups = 256;
 
-template <int FMT>
+template <int FMT, bool GROUPED>
 struct PairCfg {
     static constexpr int G = FMT == QFP4_MXFP4 ? 32 : 16;
     static constexpr int CPS = (256 / G) / 4;          // SF tiles per 128 rows per 256-K block
     static constexpr int AB_STAGES = FMT == QFP4_MXFP4 ? 6 : 5;
-    static constexpr int SF_STAGES = 8;                // scale-factor ring in shared memory
+    // scale-factor ring in shared memory (the grouped MXFP4 kernel gives up
+    // two stages to its per-group tables)
+    static constexpr int SF_STAGES = FMT == QFP4_MXFP4 && GROUPED ? 6 : 8;
     static constexpr int T_SLOTS = AB_STAGES;          // scale-factor slots in tensor memory (one per A/B stage)
     static constexpr int A_BYTES = 128 * 128;
     static constexpr int B_BYTES = 128 * 128;
@@ -86,12 +89,19 @@ struct PairCfg {
     static constexpr int SLOT_COLS = SFA_COLS + SFB_COLS;
     static constexpr int COL_SF = 256;
     static constexpr int OFF_SF = AB_STAGES * AB_BYTES;
-    static constexpr int OFF_BAR = OFF_SF + SF_STAGES * SF_BYTES;
+    // epilogue staging for TMA stores of D: per epilogue warp, D_BUFS boxes
+    // of 32 rows x 16 columns (BF16)
+    static constexpr int D_COLS = 16;
+    static constexpr int D_BOX_BYTES = 32 * D_COLS * 2;
+    static constexpr int D_BUFS = FMT == QFP4_NVFP4 && !GROUPED ? 2 : 1;
+    static constexpr int OFF_D = OFF_SF + SF_STAGES * SF_BYTES;
+    static constexpr int OFF_BAR = OFF_D + 8 * D_BUFS * D_BOX_BYTES;
     // full/empty[AB], sf_full/sf_empty[SF], acc_full, acc_empty
     static constexpr int NBAR = 2 * AB_STAGES + 2 * SF_STAGES + 2;
     static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
     static_assert(COL_SF + T_SLOTS * SLOT_COLS <= 512, "tensor memory overflow");
-    static_assert(SMEM <= 232448, "shared memory overflow");
+    // (the grouped kernel's per-group tables take 4 KB of static shared memory)
+    static_assert(SMEM + (GROUPED ? 4096 : 0) <= 232448, "shared memory overflow");
     static_assert(SF_STAGES % 2 == 0, "scale warps alternate K-blocks");
 };
 
@@ -111,9 +121,9 @@ struct PairTile {
 template <int FMT, bool GROUPED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const GemmParams p)
+                 const __grid_constant__ CUtensorMap tmD, const GemmParams p)
 {
-    using C = PairCfg<FMT>;
+    using C = PairCfg<FMT, GROUPED>;
     constexpr int SAB = C::AB_STAGES, SSF = C::SF_STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -178,13 +188,14 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             mbar_init(smem_u32(&sf_empty[s]), 4);
         }
         mbar_init(smem_u32(acc_full), 1);
-        mbar_init(smem_u32(acc_empty), 2 * 8);
+        mbar_init(smem_u32(acc_empty), 2);         // one release per CTA
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmD);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(tmem_slot), 512);
@@ -416,21 +427,26 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const int quad = warp & 3;
         const int half = (warp - 12) >> 2;
         const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
+        uint8_t *d_stage = smem + C::OFF_D + (warp - 12) * C::D_BUFS * C::D_BOX_BYTES;
         uint32_t acc_phase = 0;
         bool ok = true;
+        // the global scales are read before the accumulator is waited for,
+        // so that their latency stays off the drain
+        float gs_dense = 1.0f;
+        if (FMT == QFP4_NVFP4 && !GROUPED)
+            gs_dense = (p.gs_a ? p.gs_a[0] : 1.0f) * (p.gs_b ? p.gs_b[0] : 1.0f);
         for (int32_t t = pair_id; t < total_tiles; t += npairs) {
             const PairTile ti = tile_info(t);
+            float gs = gs_dense;
+            if (FMT == QFP4_NVFP4 && GROUPED)
+                gs = (p.gs_a ? p.gs_a[ti.group] : 1.0f) * (p.gs_b ? p.gs_b[ti.group] : 1.0f);
+            // A warp whose wait runs out still takes part in this tile's
+            // named barrier below (its drain reads are harmless); the barrier
+            // ANDs every thread's view of "all well", so the eight warps
+            // leave the loop together or not at all.
             const int got = __shfl_sync(0xffffffffu,
                                         lane == 0 ? (mbar_wait(smem_u32(acc_full), acc_phase) ? 1 : 0) : 0, 0);
-            if (!got) { ok = false; break; }
             tc_fence_after();
-            float gs = 1.0f;
-            if (FMT == QFP4_NVFP4) {
-                const int g = GROUPED ? ti.group : 0;
-                const float ga = p.gs_a ? p.gs_a[g] : 1.0f;
-                const float gb = p.gs_b ? p.gs_b[g] : 1.0f;
-                gs = ga * gb;
-            }
             const int32_t row = ti.row0 + 128 * static_cast<int32_t>(rank) + quad * 32 + lane;
             const bool row_ok = row < ti.row_end;
             __nv_bfloat16 *dst = p.D + static_cast<size_t>(row_ok ? row : 0) * p.N + ti.n0 + half * 128;
@@ -438,8 +454,10 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             // Drain this warp's 128 columns completely before releasing the
             // accumulator (the next tile's MMAs wait for that): the first
             // three 32-column chunks are scaled and rounded to BF16 pairs as
-            // they arrive, the fourth is held as loaded; the global stores
-            // only start after the release.
+            // they arrive, the fourth is held as loaded.  No global store
+            // starts before all eight warps have drained and the release is
+            // out: stores issued by early warps would otherwise queue ahead
+            // of the late warps' release and of the next tile's traffic.
             uint32_t packed[3][16];
 #pragma unroll
             for (int j = 0; j < 3; ++j) {
@@ -459,21 +477,48 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             tmem_ld_wait();
             tmem_regs_after_wait(last);
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
-            if (row_ok) {
+            if (!named_barrier_and(1, 256, got != 0 && *abort_flag == 0)) { ok = got != 0; break; }
+            if (warp == 12 && lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
+            uint32_t q3[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(last[2 * i]) * gs,
+                                                          __uint_as_float(last[2 * i + 1]) * gs);
+                q3[i] = *reinterpret_cast<uint32_t *>(&pr);
+            }
+            // Stores: the warp's 32 rows x 128 columns leave as eight TMA
+            // stores of 32 x 16 through its staging boxes, so that D is
+            // written in whole lines by the copy engine instead of one
+            // 32-byte piece of 32 different rows per store instruction.
+            // Rows past M are clipped by the tensor map; a grouped tile whose
+            // group ends inside this warp's rows stores row by row instead,
+            // as the rows beyond belong to the next group.
+            const int32_t wrow0 = ti.row0 + 128 * static_cast<int32_t>(rank) + quad * 32;
+            if (wrow0 < ti.row_end && (!GROUPED || wrow0 + 32 <= ti.row_end)) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t *src = c < 6 ? &packed[c >> 1][(c & 1) * 8] : &q3[(c & 1) * 8];
+                    uint8_t *box = d_stage + (c % C::D_BUFS) * C::D_BOX_BYTES;
+                    // the box is free again once the copy engine has read the
+                    // store issued from it D_BUFS stores ago
+                    if (lane == 0) bulk_wait_group_read<C::D_BUFS - 1>();
+                    __syncwarp();
+                    uint4 *row_dst = reinterpret_cast<uint4 *>(box + lane * (C::D_COLS * 2));
+                    row_dst[0] = make_uint4(src[0], src[1], src[2], src[3]);
+                    row_dst[1] = make_uint4(src[4], src[5], src[6], src[7]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmD, smem_u32(box), ti.n0 + half * 128 + c * C::D_COLS, wrow0);
+                        bulk_commit_group();
+                    }
+                }
+            } else if (row_ok) {
 #pragma unroll
                 for (int j = 0; j < 3; ++j) {
                     __nv_bfloat16 *d = dst + j * 32;
                     st_global_v8(d, *reinterpret_cast<const uint32_t(*)[8]>(&packed[j][0]));
                     st_global_v8(d + 16, *reinterpret_cast<const uint32_t(*)[8]>(&packed[j][8]));
-                }
-                uint32_t q3[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(last[2 * i]) * gs,
-                                                              __uint_as_float(last[2 * i + 1]) * gs);
-                    q3[i] = *reinterpret_cast<uint32_t *>(&pr);
                 }
                 st_global_v8(dst + 96, *reinterpret_cast<const uint32_t(*)[8]>(&q3[0]));
                 st_global_v8(dst + 112, *reinterpret_cast<const uint32_t(*)[8]>(&q3[8]));
@@ -481,6 +526,8 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             acc_phase ^= 1;
         }
         if (!ok && lane == 0) { record_timeout(); *abort_flag = 1; }
+        // the staging boxes must outlive the stores issued from them
+        if (lane == 0) bulk_wait_group<0>();
     }
 
     // ---- teardown.  Reconverge each warp first: lanes that skipped a
@@ -501,10 +548,10 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 }
 
 template <int FMT, bool GROUPED>
-int launch(const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &prm, int64_t pair_tiles,
-           cudaStream_t s)
+int launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &md, const GemmParams &prm,
+           int64_t pair_tiles, cudaStream_t s)
 {
-    using C = PairCfg<FMT>;
+    using C = PairCfg<FMT, GROUPED>;
     auto kern = gemm_pair_kernel<FMT, GROUPED>;
     static int configured_device = -1;
     int dev = 0;
@@ -519,19 +566,19 @@ int launch(const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &prm, 
     int64_t pairs = sms / 2;
     if (pair_tiles < pairs) pairs = pair_tiles > 0 ? pair_tiles : 1;
     return launch_status(launch_pdl(kern, dim3(static_cast<unsigned>(2 * pairs)), dim3(kThreads), C::SMEM, s,
-                                    ma, mb, prm));
+                                    ma, mb, md, prm));
 }
 
 }  // namespace
 
 int launch_gemm_pair(int fmt, bool grouped, const CUtensorMap &ma, const CUtensorMap &mb,
-                     const GemmParams &prm, int64_t pair_tiles, cudaStream_t s)
+                     const CUtensorMap &md, const GemmParams &prm, int64_t pair_tiles, cudaStream_t s)
 {
     if (fmt == QFP4_NVFP4)
-        return grouped ? launch<QFP4_NVFP4, true>(ma, mb, prm, pair_tiles, s)
-                       : launch<QFP4_NVFP4, false>(ma, mb, prm, pair_tiles, s);
-    return grouped ? launch<QFP4_MXFP4, true>(ma, mb, prm, pair_tiles, s)
-                   : launch<QFP4_MXFP4, false>(ma, mb, prm, pair_tiles, s);
+        return grouped ? launch<QFP4_NVFP4, true>(ma, mb, md, prm, pair_tiles, s)
+                       : launch<QFP4_NVFP4, false>(ma, mb, md, prm, pair_tiles, s);
+    return grouped ? launch<QFP4_MXFP4, true>(ma, mb, md, prm, pair_tiles, s)
+                   : launch<QFP4_MXFP4, false>(ma, mb, md, prm, pair_tiles, s);
 }
 
 }  // namespace qfp4

@@ -25,9 +25,10 @@ struct GemmParams {
 int make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, uint32_t box_inner,
              uint32_t box_rows);
 
-// CTA-pair (cta_group::2) GEMM over 256 x 256 tiles; N % 256 == 0.
+// CTA-pair (cta_group::2) GEMM over 256 x 256 tiles; N % 256 == 0.  ma and mb
+// have 128-row boxes; md is D (BF16) with 32-row x 16-column boxes.
 int launch_gemm_pair(int fmt, bool grouped, const CUtensorMap &ma, const CUtensorMap &mb,
-                     const GemmParams &prm, int64_t pair_tiles, cudaStream_t s);
+                     const CUtensorMap &md, const GemmParams &prm, int64_t pair_tiles, cudaStream_t s);
 
 int read_clear_status_gemm_pair(cudaStream_t s, uint32_t *out);
 

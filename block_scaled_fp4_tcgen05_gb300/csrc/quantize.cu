@@ -146,7 +146,9 @@ __device__ __forceinline__ BlockScale block_scale(float amax, float gs, float in
         b.mode = 1;
     } else {
         const float t = scale_target(amax, gs, inv_gs);
-        b.code = ue4m3_encode(t);
+        // t is NaN only for gs = 0 (an all-zero tensor: 0/0); like t = 0 it
+        // takes scale code 0, and the block then encodes as zeros
+        b.code = t > 0.0f ? ue4m3_encode(t) : 0u;
         b.s = __fmul_rn(ue4m3_decode(b.code), gs);
         if (b.s == 0.0f) {
             b.mode = 0;

@@ -131,7 +131,10 @@ int oracle_e2m1_round(float q)
 int oracle_ue4m3_round(float t)
 {
     double a = (double)t;
-    if (!(a > 0.0)) return 0;          /* zero (and, defensively, negatives) */
+    /* zero, and NaN: t = (0/6)/0 for the all-zero tensor, whose global
+     * scale is 0 (READING: the pages do not cover that tensor; code 0 makes
+     * s = 0 and the block encode as zeros, as for any zero block) */
+    if (!(a > 0.0)) return 0;
     return nearest_even_code(a, oracle_ue4m3_value, 0x7F);
 }
 

@@ -207,6 +207,16 @@ def test_quantize_zero_block_and_saturation():
     assert SF.tolist() == [[0, 0]] and Q.max() == 0
     Q, SF = oracle.quantize(MX, x, 1.0)
     assert SF.tolist() == [[0]] and Q.max() == 0
+    # an all-zero tensor has global scale 0; t = (0/6)/0 is NaN and takes
+    # scale code 0 like t = 0, and a non-zero block with gs = 0 has t = +inf,
+    # which saturates to 0x7E while s = 448 * 0 = 0 still zeroes its elements
+    assert oracle.global_scale(np.zeros((2, 16), np.uint16)) == 0.0
+    Q, SF = oracle.quantize(NV, x, 0.0)
+    assert SF.tolist() == [[0, 0]] and Q.max() == 0
+    y = np.zeros((1, 32), dtype=np.float32)
+    y[0, 20] = 1.0
+    Q, SF = oracle.quantize(NV, y, 0.0)
+    assert SF.tolist() == [[0, 0x7E]] and Q.max() == 0
     # NVFP4 scale saturation: t = amax/6/gs of 448, 464, 470, 1e6 -> 0x7E
     for t in (448.0, 464.0, 470.0, 1e6):
         x = np.zeros((1, 16), dtype=np.float32)

@@ -74,8 +74,10 @@ def test_quantize_special_values(fmt):
     rows.append(r)
     rows.append(np.geomspace(1e-30, 1e30, 256).astype(np.float32) * np.where(np.arange(256) % 2, -1, 1))
     x = synth.f32_to_bf16_bits(np.stack(rows))
+    # gs = 0 is what an all-zero tensor gets: (amax / 6) / gs is then NaN or
+    # +inf, and NaN must take scale code 0 like the oracle's rounding does
     for gs in ([None] if fmt == MX else [np.float32(1.0), np.float32(3.1e-3), np.float32(1e-30),
-                                          np.float32(7e25), oracle.global_scale(x)]):
+                                          np.float32(7e25), oracle.global_scale(x), np.float32(0.0)]):
         check_quantize(fmt, x, gs)
 
 
@@ -197,3 +199,15 @@ def test_sf_interleave_bitexact(rows, cols):
     torch.cuda.synchronize()
     assert np.array_equal(to_host(out), oracle.sf_to_mma(sf))
     assert np.array_equal(to_host(back), sf)
+
+
+def test_quantize_all_zero_tensor_nvfp4():
+    """An all-zero tensor: global scale 0, every block scale code 0 and every
+    element code 0, through the device global scale and the quantiser."""
+    x = np.zeros((130, 512), np.uint16)
+    X = to_dev_bf16(x)
+    gs = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+    qfp4.global_scale(X, gs)
+    torch.cuda.synchronize()
+    assert gs.item() == 0.0 == oracle.global_scale(x)
+    check_quantize(NV, x, np.float32(0.0))

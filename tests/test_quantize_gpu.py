@@ -211,3 +211,49 @@ def test_quantize_all_zero_tensor_nvfp4():
     torch.cuda.synchronize()
     assert gs.item() == 0.0 == oracle.global_scale(x)
     check_quantize(NV, x, np.float32(0.0))
+
+
+# ----------------------------------------------------------------- exhaustive element path
+
+def exhaustive_input(fmt, gs):
+    """Every (scale code, element) pair the quantiser can meet for this gs:
+    for each reachable scale code c, blocks whose first element is the largest
+    positive bf16 value that yields c, filled with every bf16 value (both
+    signs, and +-0) of magnitude at most that value."""
+    g = qfp4.block_size(fmt)
+    per_row = 128 // g if fmt == NV else 256 // g          # rows of 128 (NV) or 256 (MX) elements
+    pos = np.arange(1, 0x7F80, dtype=np.uint16)             # positive finite bf16
+    nb = len(pos)
+    probe = np.zeros(((nb + per_row - 1) // per_row * per_row, g), np.uint16)
+    probe[:nb, 0] = pos
+    _, sf = oracle.quantize(fmt, probe.reshape(-1, per_row * g), gs)
+    codes = sf.reshape(-1)[:nb]
+    blocks = []
+    for c in np.unique(codes):
+        amax = pos[codes == c].max()
+        mags = pos[pos <= amax]
+        vals = np.concatenate([mags, mags | 0x8000, np.array([0, 0x8000], np.uint16)])
+        fill = g - 1
+        nblk = (len(vals) + fill - 1) // fill
+        b = np.zeros((nblk, g), np.uint16)
+        b[:, 0] = amax
+        flat = np.zeros(nblk * fill, np.uint16)
+        flat[:len(vals)] = vals
+        b[:, 1:] = flat.reshape(nblk, fill)
+        blocks.append(b)
+    allb = np.concatenate(blocks)
+    pad = (-len(allb)) % per_row
+    allb = np.concatenate([allb, np.zeros((pad, g), np.uint16)])
+    return allb.reshape(-1, per_row * g), len(np.unique(codes))
+
+
+@pytest.mark.parametrize("fmt,gs", [(NV, np.float32(1.0)), (NV, np.float32(0.01371)),
+                                    (NV, np.float32(7.3e-6)), (MX, None)])
+def test_quantize_exhaustive_element_path(fmt, gs):
+    """Bit-exact against the oracle over every bf16 element value with every
+    reachable scale code (a few million elements per case): pins the scale
+    encoding, the quotient x / s and its E2M1 rounding at every input the
+    kernel can see for this global scale."""
+    x, ncodes = exhaustive_input(fmt, gs if gs is not None else np.float32(1.0))
+    assert ncodes >= (100 if fmt == NV else 200)
+    check_quantize(fmt, x, gs)

@@ -213,8 +213,8 @@ class Pipeline:
                   self.ws, self.ws_bytes)
 
     def kernels_per_step(self):
-        # amax + finalize (NVFP4), quantise, GEMM
-        return (2 if self.case.fmt == self.q.NVFP4 else 0) + 2
+        # init + amax + finalize (NVFP4 global scale), quantise, GEMM
+        return (3 if self.case.fmt == self.q.NVFP4 else 0) + 2
 
 
 def time_main(pipe, steps, warmup, flush, world, device, clocks_gpu):
@@ -623,7 +623,7 @@ def main():
 
 
 def pipe_kernels(case):
-    return (2 if case.fmt == 1 else 0) + 2
+    return (3 if case.fmt == 1 else 0) + 2
 
 
 if __name__ == "__main__":

@@ -469,8 +469,9 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
     }
 }
 
-// amax over rows of X, one warp per row; per group via atomicMax on the bit
-// pattern (non-negative floats order like unsigned integers).  Without
+// amax over rows of X, one warp per row (the per-expert global scales; one
+// group uses amax_flat_kernel); per group via atomicMax on the bit pattern
+// (non-negative floats order like unsigned integers).  Without
 // groups the warps of a CTA first fold their maxima in shared memory, so
 // that one atomic per CTA (not per row) reaches the single global word.
 __global__ void __launch_bounds__(kThreads)
@@ -537,6 +538,62 @@ amax_rows_kernel(const uint4 *__restrict__ X, int64_t rows, int64_t chunks_per_r
     if (cur >= 0 && lane == 0) atomicMax(&s_max, __float_as_uint(run));
     __syncthreads();
     if (threadIdx.x == 0 && s_max != 0u) atomicMax(amax_bits, s_max);
+}
+
+// amax over all of X (one group): the rows are contiguous, so X is walked as
+// one flat array of 16-byte vectors, eight loads in flight per thread per
+// round (one or two rounds of memory latency for a 32 MB tensor instead of
+// one per 2 KB of a row), then one atomic per CTA.
+constexpr int kAmaxUnroll = 8;
+__global__ void __launch_bounds__(kThreads)
+amax_flat_kernel(const uint4 *__restrict__ X, int64_t nvec, uint32_t *__restrict__ amax_bits)
+{
+    __shared__ float s_warp[kThreads / 32];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    float m = 0.0f;
+    for (int64_t base = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; base < nvec;
+         base += kAmaxUnroll * stride) {
+        uint4 v[kAmaxUnroll];
+#pragma unroll
+        for (int u = 0; u < kAmaxUnroll; ++u) {
+            const int64_t i = base + u * stride;
+            v[u] = i < nvec ? ld_stream_v4(X + i) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kAmaxUnroll; ++u) {
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float lo, hi;
+                bf16x2_to_f32(w[j], lo, hi);
+                m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float cm = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) cm = fmaxf(cm, s_warp[w]);
+        // non-negative floats order like their bit patterns
+        if (cm != 0.0f) atomicMax(amax_bits, __float_as_uint(cm));
+    }
+}
+
+// Zeroes the amax words before the atomics of the amax kernels.  A kernel
+// rather than a memset so that the next launch overlaps it; its wait also
+// keeps it behind the previous kernel, which may still read these words as
+// global scales.
+__global__ void gs_init_kernel(uint32_t *bits, int n)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) bits[i] = 0u;
 }
 
 // gs = amax / (6 * 448), in place over the amax bit patterns.
@@ -648,11 +705,16 @@ extern "C" int qfp4_global_scale(const void *X_bf16, int64_t rows, int64_t cols,
     if (cols % 8 != 0) return QFP4_ERR_UNSUPPORTED;
     if (!aligned16(X_bf16) || !aligned4(gs_out)) return QFP4_ERR_MISALIGNED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(gs_out, 0, sizeof(float), s) != cudaSuccess) return QFP4_ERR_CUDA;
+    if (launch_pdl(gs_init_kernel, dim3(1), dim3(32), 0, s, reinterpret_cast<uint32_t *>(gs_out), 1) != cudaSuccess)
+        return QFP4_ERR_CUDA;
     if (rows > 0 && cols > 0) {
-        const int grid = grid_for(rows, kThreads / 32);
-        if (launch_pdl(amax_rows_kernel, dim3(grid), dim3(kThreads), 0, s, static_cast<const uint4 *>(X_bf16),
-                       rows, cols / 8, 1, nullptr, reinterpret_cast<uint32_t *>(gs_out)) != cudaSuccess)
+        const int64_t nvec = rows * (cols / 8);
+        const int sms = sm_count();
+        int64_t grid = static_cast<int64_t>(sms > 0 ? sms : 148) * 6;
+        const int64_t want = (nvec + kThreads - 1) / kThreads;
+        if (want < grid) grid = want;
+        if (launch_pdl(amax_flat_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
+                       static_cast<const uint4 *>(X_bf16), nvec, reinterpret_cast<uint32_t *>(gs_out)) != cudaSuccess)
             return QFP4_ERR_CUDA;
     }
     return launch_status(launch_pdl(gs_finalize_kernel, dim3(1), dim3(32), 0, s,
@@ -669,7 +731,9 @@ extern "C" int qfp4_global_scale_grouped(const void *X_bf16, int64_t total_rows,
     if (!aligned16(X_bf16) || !aligned4(gs_out) || !aligned4(row_offsets))
         return QFP4_ERR_MISALIGNED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(gs_out, 0, sizeof(float) * groups, s) != cudaSuccess) return QFP4_ERR_CUDA;
+    if (launch_pdl(gs_init_kernel, dim3((static_cast<unsigned>(groups) + 127) / 128), dim3(128), 0, s,
+                   reinterpret_cast<uint32_t *>(gs_out), static_cast<int>(groups)) != cudaSuccess)
+        return QFP4_ERR_CUDA;
     if (total_rows > 0 && cols > 0) {
         const int grid = grid_for(total_rows, kThreads / 32);
         if (launch_pdl(amax_rows_kernel, dim3(grid), dim3(kThreads), 0, s, static_cast<const uint4 *>(X_bf16),

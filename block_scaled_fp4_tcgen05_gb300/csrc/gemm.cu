@@ -402,6 +402,20 @@ int make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, 
     return r == CUDA_SUCCESS ? QFP4_OK : QFP4_ERR_CUDA;
 }
 
+int make_map_kpairs(CUtensorMap *map, const void *base, uint64_t K, uint64_t rows)
+{
+    auto enc = get_encode_fn();
+    if (!enc) return QFP4_ERR_CUDA;
+    cuuint64_t dims[3] = {128, rows, K / 256};
+    cuuint64_t strides[2] = {K / 2, 128};
+    cuuint32_t box[3] = {128, 128, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? QFP4_OK : QFP4_ERR_CUDA;
+}
+
 int make_map_bf16(CUtensorMap *map, void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
                   uint32_t box_rows)
 {
@@ -491,8 +505,14 @@ extern "C" int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K, const void
     if (N % 256 == 0 && M > 128) {
         // CTA pairs on 256 x 256 tiles; D leaves in 32-row x 16-column boxes
         CUtensorMap md;
-        int rc = make_map(&ma, A_packed, K / 2, M, kBKBytes, 128);
-        if (rc == QFP4_OK) rc = make_map(&mb, B_packed, K / 2, N, kBKBytes, 128);
+        int rc;
+        if (gemm_pair_double_stages(fmt, false, K)) {
+            rc = make_map_kpairs(&ma, A_packed, K, M);
+            if (rc == QFP4_OK) rc = make_map_kpairs(&mb, B_packed, K, N);
+        } else {
+            rc = make_map(&ma, A_packed, K / 2, M, kBKBytes, 128);
+            if (rc == QFP4_OK) rc = make_map(&mb, B_packed, K / 2, N, kBKBytes, 128);
+        }
         if (rc == QFP4_OK) rc = make_map_bf16(&md, D_bf16, N, M, 16, 32);
         if (rc != QFP4_OK) return rc;
         return launch_gemm_pair(fmt, false, ma, mb, md, a, ((M + 255) / 256) * (N / 256), s);

@@ -69,18 +69,24 @@ namespace {
 constexpr int kThreads = 640;          // 20 warps
 constexpr int kMaxGroups = 256;
 
-template <int FMT, bool GROUPED>
+// DBL: operand stages of two 256-K blocks, each filled by one 3-D TMA box
+// per operand (32 KB per request instead of 16 KB); dense MXFP4 with
+// K % 512 == 0, whose shared memory holds three such stages.
+template <int FMT, bool GROUPED, bool DBL = false>
 struct PairCfg {
     static constexpr int G = FMT == QFP4_MXFP4 ? 32 : 16;
     static constexpr int CPS = (256 / G) / 4;          // SF tiles per 128 rows per 256-K block
-    static constexpr int AB_STAGES = FMT == QFP4_MXFP4 ? 6 : 5;
+    static constexpr int KBS = DBL ? 2 : 1;            // 256-K blocks per operand stage
+    static constexpr int AB_STAGES = DBL ? 3 : FMT == QFP4_MXFP4 ? 6 : 5;
     // scale-factor ring in shared memory (the grouped MXFP4 kernel gives up
     // two stages to its per-group tables)
     static constexpr int SF_STAGES = FMT == QFP4_MXFP4 && GROUPED ? 6 : 8;
-    static constexpr int T_SLOTS = AB_STAGES;          // scale-factor slots in tensor memory (one per A/B stage)
-    static constexpr int A_BYTES = 128 * 128;
+    // scale-factor slots in tensor memory, one per K-block of the ring
+    static constexpr int T_SLOTS = AB_STAGES * KBS;
+    static constexpr int A_BYTES = 128 * 128;          // one 256-K block of A (this CTA's 128 rows)
     static constexpr int B_BYTES = 128 * 128;
-    static constexpr int AB_BYTES = A_BYTES + B_BYTES;
+    static constexpr int A_STAGE = KBS * A_BYTES;      // A part of a stage; B follows it
+    static constexpr int AB_BYTES = KBS * (A_BYTES + B_BYTES);
     static constexpr int SFA_BYTES = CPS * 512;        // this CTA's 128 rows
     static constexpr int SFB_BYTES = 2 * CPS * 512;    // all 256 columns of the pair tile
     static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
@@ -103,6 +109,7 @@ struct PairCfg {
     // (the grouped kernel's per-group tables take 4 KB of static shared memory)
     static_assert(SMEM + (GROUPED ? 4096 : 0) <= 232448, "shared memory overflow");
     static_assert(SF_STAGES % 2 == 0, "scale warps alternate K-blocks");
+    static_assert(!DBL || (FMT == QFP4_MXFP4 && !GROUPED), "double stages: dense MXFP4 only");
 };
 
 __device__ __forceinline__ void record_timeout()
@@ -118,13 +125,13 @@ struct PairTile {
     int32_t group;
 };
 
-template <int FMT, bool GROUPED>
+template <int FMT, bool GROUPED, bool DBL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmD, const GemmParams p)
 {
-    using C = PairCfg<FMT, GROUPED>;
-    constexpr int SAB = C::AB_STAGES, SSF = C::SF_STAGES;
+    using C = PairCfg<FMT, GROUPED, DBL>;
+    constexpr int SAB = C::AB_STAGES, SSF = C::SF_STAGES, TSL = C::T_SLOTS, KBS = C::KBS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -180,7 +187,8 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SAB; ++s) {
-            mbar_init(smem_u32(&full[s]), 1 + 8);   // producer (with the bytes) + 4 scale warps x 2 CTAs
+            // producer (with the bytes) + 4 scale warps x 2 CTAs per K-block of the stage
+            mbar_init(smem_u32(&full[s]), 1 + 8 * KBS);
             mbar_init(smem_u32(&empty[s]), 1);
         }
         for (int s = 0; s < SSF; ++s) {
@@ -243,8 +251,9 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         return ti;
     };
 
-    // j counts K-blocks over all tiles this pair processes; every ring slot
-    // and phase parity is derived from it.
+    // j counts K-blocks (operand stages, for the producers and the MMA) over
+    // all tiles this pair processes; every ring slot and phase parity is
+    // derived from it.
     if (warp == 0 || warp == 3) {
         // ------------------------------------------------ A (warp 0) and B (warp 3) TMA producers
         // Two issuing warps: the copy engine works through the requests of
@@ -259,7 +268,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const PairTile ti = tile_info(t);
                 const int32_t arow = ti.row0 + 128 * static_cast<int32_t>(rank);
                 const int32_t brow = (GROUPED ? ti.group * p.N : 0) + ti.n0 + 128 * static_cast<int32_t>(rank);
-                for (int kb = 0; kb < kblocks; ++kb, ++j) {
+                for (int kb = 0; kb < kblocks; kb += KBS, ++j) {
                     const uint32_t s = j % SAB;
                     if (!mbar_wait(smem_u32(&empty[s]), ((j / SAB) & 1) ^ 1)) { ok = false; break; }
                     const uint32_t dst = smem_u32(smem + s * C::AB_BYTES);
@@ -267,9 +276,11 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     if (is_a) {
                         // the leader's A thread posts the byte count of both CTAs' A and B
                         if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * C::AB_BYTES);
-                        tma_load_2d_pair(dst, &tmA, fb, kb * 128, arow);
+                        if (DBL) tma_load_3d_pair(dst, &tmA, fb, 0, arow, kb);
+                        else tma_load_2d_pair(dst, &tmA, fb, kb * 128, arow);
                     } else {
-                        tma_load_2d_pair(dst + C::A_BYTES, &tmB, fb, kb * 128, brow);
+                        if (DBL) tma_load_3d_pair(dst + C::A_STAGE, &tmB, fb, 0, brow, kb);
+                        else tma_load_2d_pair(dst + C::A_STAGE, &tmB, fb, kb * 128, brow);
                     }
                 }
             }
@@ -310,50 +321,57 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         // position is stepped instead of divided out.
         if (rank == 0 && lane == 0) {
             const uint64_t a_desc0 = smem_desc(smem_u32(smem), 16, 1024, kSwizzle128B);
-            const uint64_t b_desc0 = smem_desc(smem_u32(smem) + C::A_BYTES, 16, 1024, kSwizzle128B);
+            const uint64_t b_desc0 = smem_desc(smem_u32(smem) + C::A_STAGE, 16, 1024, kSwizzle128B);
             constexpr uint64_t kStageDesc = static_cast<uint64_t>(C::AB_BYTES >> 4);
+            constexpr uint64_t kBlockDesc = static_cast<uint64_t>(C::A_BYTES >> 4);   // next K-block of a stage
             const uint32_t sf0 = tmem_base + C::COL_SF;
-            uint32_t s = 0, phase = 0, acc_phase = 0;
+            uint32_t s = 0, phase = 0, acc_phase = 0, ts = 0;
             bool ok = true;
             const int full_kblocks = K / 256;                  // K-blocks with all four K=64 steps
             for (int32_t t = pair_id; t < total_tiles && ok; t += npairs) {
                 if (!mbar_wait(smem_u32(acc_empty), acc_phase ^ 1)) { ok = false; break; }
                 tc_fence_after();
-                for (int kb = 0; kb < kblocks; ++kb) {
+                for (int kb0 = 0; kb0 < kblocks; kb0 += KBS) {
                     if (!mbar_wait(smem_u32(&full[s]), phase)) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t ad = a_desc0 + s * kStageDesc;
-                    const uint64_t bd = b_desc0 + s * kStageDesc;
-                    const uint32_t sfa_t = sf0 + s * C::SLOT_COLS;
-                    const uint32_t sfb_t = sfa_t + C::SFA_COLS;
-                    const uint32_t acc0 = kb > 0 ? 1u : 0u;
-                    if (kb < full_kblocks) {
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            if (FMT == QFP4_NVFP4) {
-                                constexpr uint32_t id = idesc_block_scaled(256, 256, false, 0, 0);
-                                tc_mma_nvf4_pair(tmem_base, ad + 2 * kk, bd + 2 * kk, id, sfa_t + kk * 4,
-                                                 sfb_t + kk * 8, kk > 0 ? 1u : acc0);
-                            } else {
-                                constexpr uint32_t id0 = idesc_block_scaled(256, 256, true, 0, 0);
-                                constexpr uint32_t id1 = idesc_block_scaled(256, 256, true, 2, 2);
-                                tc_mma_mxf4_pair(tmem_base, ad + 2 * kk, bd + 2 * kk, (kk & 1) ? id1 : id0,
-                                                 sfa_t + (kk >> 1) * 4, sfb_t + (kk >> 1) * 8, kk > 0 ? 1u : acc0);
+                    for (int kbi = 0; kbi < KBS; ++kbi) {
+                        const int kb = kb0 + kbi;
+                        const uint64_t ad = a_desc0 + s * kStageDesc + kbi * kBlockDesc;
+                        const uint64_t bd = b_desc0 + s * kStageDesc + kbi * kBlockDesc;
+                        const uint32_t sfa_t = sf0 + ts * C::SLOT_COLS;
+                        const uint32_t sfb_t = sfa_t + C::SFA_COLS;
+                        if (++ts == TSL) ts = 0;
+                        const uint32_t acc0 = kb > 0 ? 1u : 0u;
+                        if (kb < full_kblocks) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                if (FMT == QFP4_NVFP4) {
+                                    constexpr uint32_t id = idesc_block_scaled(256, 256, false, 0, 0);
+                                    tc_mma_nvf4_pair(tmem_base, ad + 2 * kk, bd + 2 * kk, id, sfa_t + kk * 4,
+                                                     sfb_t + kk * 8, kk > 0 ? 1u : acc0);
+                                } else {
+                                    constexpr uint32_t id0 = idesc_block_scaled(256, 256, true, 0, 0);
+                                    constexpr uint32_t id1 = idesc_block_scaled(256, 256, true, 2, 2);
+                                    tc_mma_mxf4_pair(tmem_base, ad + 2 * kk, bd + 2 * kk, (kk & 1) ? id1 : id0,
+                                                     sfa_t + (kk >> 1) * 4, sfb_t + (kk >> 1) * 8,
+                                                     kk > 0 ? 1u : acc0);
+                                }
                             }
-                        }
-                    } else {
-                        // trailing half K-block (K % 256 == 128): two K=64 steps
+                        } else {
+                            // trailing half K-block (K % 256 == 128): two K=64 steps
 #pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {
-                            if (FMT == QFP4_NVFP4) {
-                                constexpr uint32_t id = idesc_block_scaled(256, 256, false, 0, 0);
-                                tc_mma_nvf4_pair(tmem_base, ad + 2 * kk, bd + 2 * kk, id, sfa_t + kk * 4,
-                                                 sfb_t + kk * 8, kk > 0 ? 1u : acc0);
-                            } else {
-                                constexpr uint32_t id0 = idesc_block_scaled(256, 256, true, 0, 0);
-                                constexpr uint32_t id1 = idesc_block_scaled(256, 256, true, 2, 2);
-                                tc_mma_mxf4_pair(tmem_base, ad + 2 * kk, bd + 2 * kk, (kk & 1) ? id1 : id0,
-                                                 sfa_t, sfb_t, kk > 0 ? 1u : acc0);
+                            for (int kk = 0; kk < 2; ++kk) {
+                                if (FMT == QFP4_NVFP4) {
+                                    constexpr uint32_t id = idesc_block_scaled(256, 256, false, 0, 0);
+                                    tc_mma_nvf4_pair(tmem_base, ad + 2 * kk, bd + 2 * kk, id, sfa_t + kk * 4,
+                                                     sfb_t + kk * 8, kk > 0 ? 1u : acc0);
+                                } else {
+                                    constexpr uint32_t id0 = idesc_block_scaled(256, 256, true, 0, 0);
+                                    constexpr uint32_t id1 = idesc_block_scaled(256, 256, true, 2, 2);
+                                    tc_mma_mxf4_pair(tmem_base, ad + 2 * kk, bd + 2 * kk, (kk & 1) ? id1 : id0,
+                                                     sfa_t, sfb_t, kk > 0 ? 1u : acc0);
+                                }
                             }
                         }
                     }
@@ -383,7 +401,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         for (int32_t t = pair_id; t < total_tiles && ok; t += npairs) {
             for (int kb = 0; kb < kblocks; ++kb, ++j) {
                 if ((j & 1) != set) continue;
-                const uint32_t s = j % SSF, slot = j % SAB;
+                const uint32_t s = j % SSF, slot = j % TSL, stage = (j / KBS) % SAB;
                 int got = __shfl_sync(0xffffffffu,
                                       lane == 0 ? (mbar_wait(smem_u32(&sf_full[s]), (j / SSF) & 1) ? 1 : 0) : 0, 0);
                 if (!got) { ok = false; break; }
@@ -400,9 +418,16 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     vb[8 * c + 0] = b0.x; vb[8 * c + 1] = b0.y; vb[8 * c + 2] = b0.z; vb[8 * c + 3] = b0.w;
                     vb[8 * c + 4] = b1.x; vb[8 * c + 5] = b1.y; vb[8 * c + 6] = b1.z; vb[8 * c + 7] = b1.w;
                 }
-                got = __shfl_sync(0xffffffffu,
-                                  lane == 0 ? (mbar_wait(smem_u32(&empty[slot]), ((j / SAB) & 1) ^ 1) ? 1 : 0) : 0, 0);
-                if (!got) { ok = false; break; }
+                // tensor-memory slot j % TSL is free once the MMAs of K-block
+                // j - TSL have completed: the commit on that K-block's
+                // operand stage (global stage index jf / KBS) says so
+                if (j >= static_cast<uint32_t>(TSL)) {
+                    const uint32_t js = (j - TSL) / KBS;
+                    got = __shfl_sync(0xffffffffu,
+                                      lane == 0 ? (mbar_wait(smem_u32(&empty[js % SAB]), (js / SAB) & 1) ? 1 : 0) : 0,
+                                      0);
+                    if (!got) { ok = false; break; }
+                }
                 tc_fence_after();
                 const uint32_t col = tmem_base + C::COL_SF + slot * C::SLOT_COLS;
                 tmem_st_32x32b<C::SFA_COLS>(lane_base + col, va);
@@ -417,7 +442,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 // and a refill of the slot would then be read instead).
                 if (lane == 0) {
                     mbar_arrive(smem_u32(&sf_empty[s]));
-                    mbar_arrive_cluster_relaxed(ready0_leader + slot * 8);
+                    mbar_arrive_cluster_relaxed(ready0_leader + stage * 8);
                 }
             }
         }
@@ -547,12 +572,12 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     }
 }
 
-template <int FMT, bool GROUPED>
+template <int FMT, bool GROUPED, bool DBL = false>
 int launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &md, const GemmParams &prm,
            int64_t pair_tiles, cudaStream_t s)
 {
-    using C = PairCfg<FMT, GROUPED>;
-    auto kern = gemm_pair_kernel<FMT, GROUPED>;
+    using C = PairCfg<FMT, GROUPED, DBL>;
+    auto kern = gemm_pair_kernel<FMT, GROUPED, DBL>;
     static int configured_device = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return QFP4_ERR_CUDA;
@@ -571,9 +596,16 @@ int launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &md, 
 
 }  // namespace
 
+bool gemm_pair_double_stages(int fmt, bool grouped, int64_t K)
+{
+    return fmt == QFP4_MXFP4 && !grouped && K % 512 == 0;
+}
+
 int launch_gemm_pair(int fmt, bool grouped, const CUtensorMap &ma, const CUtensorMap &mb,
                      const CUtensorMap &md, const GemmParams &prm, int64_t pair_tiles, cudaStream_t s)
 {
+    if (gemm_pair_double_stages(fmt, grouped, prm.K))
+        return launch<QFP4_MXFP4, false, true>(ma, mb, md, prm, pair_tiles, s);
     if (fmt == QFP4_NVFP4)
         return grouped ? launch<QFP4_NVFP4, true>(ma, mb, md, prm, pair_tiles, s)
                        : launch<QFP4_NVFP4, false>(ma, mb, md, prm, pair_tiles, s);

@@ -25,8 +25,17 @@ struct GemmParams {
 int make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, uint32_t box_inner,
              uint32_t box_rows);
 
+// Packed FP4 matrix [rows, K/2 bytes] viewed as {128 bytes, rows, K/256 blocks}
+// (strides K/2 and 128 bytes), 128-byte swizzle, box {128, 128, 2}: one
+// request brings two consecutive 256-K blocks of 128 rows, laid out as two
+// 16 KB swizzled tiles one after the other.  K % 512 == 0.
+int make_map_kpairs(CUtensorMap *map, const void *base, uint64_t K, uint64_t rows);
+
 // CTA-pair (cta_group::2) GEMM over 256 x 256 tiles; N % 256 == 0.  ma and mb
-// have 128-row boxes; md is D (BF16) with 32-row x 16-column boxes.
+// have 128-row boxes (2-D, 128 bytes of K; or, when gemm_pair_double_stages
+// says so, 3-D {128 bytes, rows, 256-K blocks} boxes of two K-blocks, see
+// make_map_kpairs); md is D (BF16) with 32-row x 16-column boxes.
+bool gemm_pair_double_stages(int fmt, bool grouped, int64_t K);
 int launch_gemm_pair(int fmt, bool grouped, const CUtensorMap &ma, const CUtensorMap &mb,
                      const CUtensorMap &md, const GemmParams &prm, int64_t pair_tiles, cudaStream_t s);
 

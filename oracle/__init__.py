@@ -71,6 +71,12 @@ def _load():
                                        c_f, c_f, c_p, c_p]),
             "oracle_gemm_nt_entries": (c_int, [c_int, c_i64, c_p, c_p, c_p, c_p, c_f, c_f,
                                                c_i64, c_p, c_p, c_p, c_p]),
+            "oracle_global_scale_rows_bf16": (c_int, [c_p, c_i64, c_i64, c_p]),
+            "oracle_quantize_bf16_rows": (c_int, [c_int, c_p, c_i64, c_i64, c_p, c_p, c_p]),
+            "oracle_gemm_nt_scaled": (c_int, [c_int, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_p,
+                                              c_f, c_f, c_p, c_p, c_p, c_p]),
+            "oracle_gemm_nt_scaled_entries": (c_int, [c_int, c_i64, c_p, c_p, c_p, c_p, c_f, c_f, c_p, c_p,
+                                                      c_i64, c_p, c_p, c_p, c_p]),
             "oracle_num_threads": (c_int, []),
         }
         for name, (res, args) in sigs.items():
@@ -139,14 +145,34 @@ def global_scale(x: np.ndarray) -> np.float32:
     return np.float32(lib.oracle_global_scale(_ptr(x), x.size))
 
 
-def quantize(fmt: int, x: np.ndarray, gs: float = 1.0):
-    """x [M, K] fp32, or bf16 bits as uint16 -> (Q uint8 [M, K/2], SF uint8 [M, K/g])."""
+def global_scale_rows(x: np.ndarray) -> np.ndarray:
+    """Per-row gs[m] = amax of row m / (6*448) (fp32 [M]); ``x`` is bf16 bits as uint16."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    M, K = x.shape
+    gs = np.zeros(M, dtype=np.float32)
+    if lib.oracle_global_scale_rows_bf16(_ptr(x), M, K, _ptr(gs)) != 0:
+        raise ValueError("bad shape")
+    return gs
+
+
+def quantize(fmt: int, x: np.ndarray, gs=1.0):
+    """x [M, K] fp32, or bf16 bits as uint16 -> (Q uint8 [M, K/2], SF uint8 [M, K/g]).
+    ``gs`` is one global scale, or (bf16 input) an array of one per row."""
     lib = _load()
     x = np.ascontiguousarray(x)
     M, K = x.shape
     g = block_size(fmt)
     Q = np.zeros((M, K // 2), dtype=np.uint8)
     SF = np.zeros((M, K // g), dtype=np.uint8)
+    if np.ndim(gs) == 1:
+        if x.dtype != np.uint16:
+            raise ValueError("per-row global scales take bf16 input")
+        gsr = np.ascontiguousarray(gs, dtype=np.float32)
+        assert gsr.size == M
+        if lib.oracle_quantize_bf16_rows(fmt, _ptr(x), M, K, _ptr(gsr), _ptr(Q), _ptr(SF)) != 0:
+            raise ValueError("oracle quantize rejected its input (shape or non-finite value)")
+        return Q, SF
     if x.dtype == np.uint16:
         rc = lib.oracle_quantize_bf16(fmt, _ptr(x), M, K, float(np.float32(gs)), _ptr(Q), _ptr(SF))
     else:
@@ -191,14 +217,33 @@ def sf_from_mma(buf: np.ndarray, rows: int, cols: int) -> np.ndarray:
     return out
 
 
+def _opt_f32(v, n):
+    if v is None:
+        return None, None
+    a = np.ascontiguousarray(v, dtype=np.float32)
+    assert a.size == n
+    return a, _ptr(a)
+
+
 def gemm_nt(fmt: int, A: np.ndarray, A_sf: np.ndarray, B: np.ndarray, B_sf: np.ndarray,
-            gs_a: float = 1.0, gs_b: float = 1.0):
-    """Full reference GEMM. Returns (D fp64 [M,N], T fp64 [M,N]); SF row-major."""
+            gs_a: float = 1.0, gs_b: float = 1.0, row_scale=None, col_scale=None):
+    """Full reference GEMM. Returns (D fp64 [M,N], T fp64 [M,N]); SF row-major.
+    ``row_scale`` [M] and ``col_scale`` [N] (fp32, optional) rescale row m and
+    column n of D (the two-level epilogue)."""
     lib = _load()
     A, A_sf, B, B_sf = (np.ascontiguousarray(v, dtype=np.uint8) for v in (A, A_sf, B, B_sf))
     M, N, K = A.shape[0], B.shape[0], A.shape[1] * 2
     D = np.zeros((M, N), dtype=np.float64)
     T = np.zeros((M, N), dtype=np.float64)
+    if row_scale is not None or col_scale is not None:
+        rs, rsp = _opt_f32(row_scale, M)
+        cs, csp = _opt_f32(col_scale, N)
+        rc = lib.oracle_gemm_nt_scaled(fmt, M, N, K, _ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf),
+                                       float(np.float32(gs_a)), float(np.float32(gs_b)), rsp, csp,
+                                       _ptr(D), _ptr(T))
+        if rc != 0:
+            raise ValueError("bad shape")
+        return D, T
     rc = lib.oracle_gemm_nt(fmt, M, N, K, _ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf),
                             float(np.float32(gs_a)), float(np.float32(gs_b)), _ptr(D), _ptr(T))
     if rc != 0:
@@ -206,7 +251,7 @@ def gemm_nt(fmt: int, A: np.ndarray, A_sf: np.ndarray, B: np.ndarray, B_sf: np.n
     return D, T
 
 
-def gemm_nt_entries(fmt: int, A, A_sf, B, B_sf, gs_a, gs_b, mi, ni):
+def gemm_nt_entries(fmt: int, A, A_sf, B, B_sf, gs_a, gs_b, mi, ni, row_scale=None, col_scale=None):
     """Reference values at sampled (m, n) positions. Returns (D, T) fp64 [count]."""
     lib = _load()
     A, A_sf, B, B_sf = (np.ascontiguousarray(v, dtype=np.uint8) for v in (A, A_sf, B, B_sf))
@@ -215,6 +260,15 @@ def gemm_nt_entries(fmt: int, A, A_sf, B, B_sf, gs_a, gs_b, mi, ni):
     ni = np.ascontiguousarray(ni, dtype=np.int64)
     D = np.zeros(mi.size, dtype=np.float64)
     T = np.zeros(mi.size, dtype=np.float64)
+    if row_scale is not None or col_scale is not None:
+        rs, rsp = _opt_f32(row_scale, A.shape[0])
+        cs, csp = _opt_f32(col_scale, B.shape[0])
+        rc = lib.oracle_gemm_nt_scaled_entries(fmt, K, _ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf),
+                                               float(np.float32(gs_a)), float(np.float32(gs_b)), rsp, csp,
+                                               mi.size, _ptr(mi), _ptr(ni), _ptr(D), _ptr(T))
+        if rc != 0:
+            raise ValueError("bad shape")
+        return D, T
     rc = lib.oracle_gemm_nt_entries(fmt, K, _ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf),
                                     float(np.float32(gs_a)), float(np.float32(gs_b)),
                                     mi.size, _ptr(mi), _ptr(ni), _ptr(D), _ptr(T))

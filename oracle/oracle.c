@@ -19,7 +19,9 @@
  *         (quantize_dynamic_scaled_fp4fp8) and the re-interleave of rank-2
  *         scale factors into the 5D TCGEN layout (block_scales_interleave).
  *   [QB]  "quadbit" README, section "Accuracy (real models)": per-16 ue4m3
- *         local scale with an fp32 global scale (NVFP4), ue8m0 (MXFP4).
+ *         local scale with an fp32 global scale (NVFP4), ue8m0 (MXFP4); the
+ *         two-level recipe with a per-row fp32 global scale, and a per-row
+ *         and per-column fp32 global rescale in the MMA epilogue.
  *   [QG]  "qgemm-mx" project page, section "The gap": MXFP4 moves ~1.88x fewer
  *         bytes per weight than FP8.
  * The pages do not print the bit layouts.  Those are taken from the public
@@ -282,6 +284,30 @@ int oracle_quantize_bf16(int fmt, const uint16_t *X, int64_t M, int64_t K, float
     return bad ? -1 : 0;
 }
 
+/* Two-level NVFP4 ([QB] "Accuracy (real models)"): every row m has its own
+ * fp32 global scale gs_rows[m] = amax over row m / (6 * 448), and row m is
+ * quantised exactly as oracle_quantize_bf16 quantises it alone with that
+ * scale.  READING: "per-row fp32 global" is taken as the same amax / (6*448)
+ * rule applied to each row instead of the whole tensor. */
+int oracle_global_scale_rows_bf16(const uint16_t *X, int64_t M, int64_t K, float *gs_out)
+{
+    if (M < 0 || K < 0) return -1;
+    for (int64_t m = 0; m < M; ++m) gs_out[m] = oracle_global_scale_bf16(X + m * K, K);
+    return 0;
+}
+
+int oracle_quantize_bf16_rows(int fmt, const uint16_t *X, int64_t M, int64_t K, const float *gs_rows,
+                              uint8_t *Q, uint8_t *SF)
+{
+    int g = oracle_block_size(fmt);
+    if (M < 0 || K < 0 || K % g != 0) return -1;
+    int bad = 0;
+    for (int64_t m = 0; m < M; ++m)
+        if (oracle_quantize_bf16(fmt, X + m * K, 1, K, gs_rows[m], Q + m * (K / 2), SF + m * (K / g)) != 0)
+            bad = 1;
+    return bad ? -1 : 0;
+}
+
 /* Dequantise packed codes back to fp64: x[m,k] = E2M1(Q[m,k]) * SF[m,k/g] * gs. */
 int oracle_dequantize(int fmt, const uint8_t *Q, const uint8_t *SF, int64_t M, int64_t K,
                       float gs, double *X)
@@ -401,6 +427,47 @@ int oracle_gemm_nt_entries(int fmt, int64_t K,
 #pragma omp parallel for schedule(dynamic, 64)
     for (int64_t i = 0; i < count; ++i)
         gemm_entry(fmt, K, A, Asf, B, Bsf, gsab, mi[i], ni[i], &D[i], &T[i]);
+    return 0;
+}
+
+/* Two-level GEMM ([QB] "Accuracy (real models)": a per-row and per-column
+ * fp32 global rescale in the MMA epilogue):
+ *   D[m,n] = gs_a gs_b row_scale[m] col_scale[n] sum_k a[m,k] b[n,k]
+ * with T scaled alike.  A NULL row_scale or col_scale stands for all ones.
+ * MXFP4 ignores gs_a, gs_b (1.0) but not the row and column scales. */
+static double rc_scale(const float *rs, const float *cs, int64_t m, int64_t n)
+{
+    return (rs ? (double)rs[m] : 1.0) * (cs ? (double)cs[n] : 1.0);
+}
+
+int oracle_gemm_nt_scaled(int fmt, int64_t M, int64_t N, int64_t K,
+                          const uint8_t *A, const uint8_t *Asf, const uint8_t *B, const uint8_t *Bsf,
+                          float gs_a, float gs_b, const float *row_scale, const float *col_scale,
+                          double *D, double *T)
+{
+    int g = oracle_block_size(fmt);
+    if (K % g != 0 || K % 2 != 0) return -1;
+    double gsab = fmt == ORACLE_MXFP4 ? 1.0 : (double)gs_a * (double)gs_b;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            gemm_entry(fmt, K, A, Asf, B, Bsf, gsab * rc_scale(row_scale, col_scale, m, n), m, n,
+                       &D[m * N + n], &T[m * N + n]);
+    return 0;
+}
+
+int oracle_gemm_nt_scaled_entries(int fmt, int64_t K,
+                                  const uint8_t *A, const uint8_t *Asf, const uint8_t *B, const uint8_t *Bsf,
+                                  float gs_a, float gs_b, const float *row_scale, const float *col_scale,
+                                  int64_t count, const int64_t *mi, const int64_t *ni, double *D, double *T)
+{
+    int g = oracle_block_size(fmt);
+    if (K % g != 0 || K % 2 != 0) return -1;
+    double gsab = fmt == ORACLE_MXFP4 ? 1.0 : (double)gs_a * (double)gs_b;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t i = 0; i < count; ++i)
+        gemm_entry(fmt, K, A, Asf, B, Bsf, gsab * rc_scale(row_scale, col_scale, mi[i], ni[i]), mi[i], ni[i],
+                   &D[i], &T[i]);
     return 0;
 }
 

@@ -399,6 +399,43 @@ def test_gemm_global_scale_identity():
     assert np.array_equal(D2, 2.0 * D1) and np.array_equal(T2, 2.0 * T1)
 
 
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_gemm_row_col_rescale_identity(fmt):
+    """Two-level epilogue: D(rs, cs)[m,n] = rs[m] cs[n] D(1,1)[m,n], exact in
+    fp64 for power-of-two scales (and T alike); NULL scales are ones; sampled
+    entries agree with the full product."""
+    A, Asf, B, Bsf = _random_operands(fmt, 12, 20, 256, 53 + fmt)
+    gen = np.random.default_rng(9)
+    rs = (2.0 ** gen.integers(-6, 7, 12)).astype(np.float32)
+    cs = (2.0 ** gen.integers(-6, 7, 20)).astype(np.float32)
+    D1, T1 = oracle.gemm_nt(fmt, A, Asf, B, Bsf, 0.5, 0.25)
+    D2, T2 = oracle.gemm_nt(fmt, A, Asf, B, Bsf, 0.5, 0.25, rs, cs)
+    outer = rs.astype(np.float64)[:, None] * cs.astype(np.float64)[None, :]
+    assert np.array_equal(D2, outer * D1) and np.array_equal(T2, outer * T1)
+    Dr, _ = oracle.gemm_nt(fmt, A, Asf, B, Bsf, 0.5, 0.25, rs, None)
+    Dc, _ = oracle.gemm_nt(fmt, A, Asf, B, Bsf, 0.5, 0.25, None, cs)
+    assert np.array_equal(Dr, rs.astype(np.float64)[:, None] * D1)
+    assert np.array_equal(Dc, cs.astype(np.float64)[None, :] * D1)
+    mi, ni = gen.integers(0, 12, 50), gen.integers(0, 20, 50)
+    De, Te = oracle.gemm_nt_entries(fmt, A, Asf, B, Bsf, 0.5, 0.25, mi, ni, rs, cs)
+    assert np.array_equal(De, D2[mi, ni]) and np.array_equal(Te, T2[mi, ni])
+
+
+def test_per_row_global_scale_and_quantise_reduce_to_per_tensor():
+    """Per-row global scales are the per-tensor rule on each row alone, and
+    quantising with them equals quantising each row alone with its scale."""
+    x = synth.activations_bf16(81, 7, 256)
+    x[3] = 0                                     # an all-zero row: gs 0
+    gs = oracle.global_scale_rows(x)
+    for m in range(7):
+        assert gs[m] == oracle.global_scale(x[m:m + 1])
+    assert gs[3] == 0.0
+    Q, SF = oracle.quantize(NV, x, gs)
+    for m in range(7):
+        q1, s1 = oracle.quantize(NV, x[m:m + 1], gs[m])
+        assert np.array_equal(Q[m:m + 1], q1) and np.array_equal(SF[m:m + 1], s1)
+
+
 def test_gemm_ue8m0_increment_doubles_one_block():
     """Scale byte + 1 on one block of one A row adds exactly that block's
     contribution once more (it doubles)."""

@@ -301,6 +301,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         bool ok = true;
         for (int32_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
             const TileInfo ti = tile_info(t);
+            const int32_t row = ti.row0 + quad * 32 + lane;
+            // two-level epilogue: this lane's row scale, and lane i holding
+            // the scale of column 32 j + i of each 32-column chunk j (shared
+            // out by shuffles); read before the accumulator wait
+            const float rsv = (args.row_scale && row < ti.row_end) ? args.row_scale[row] : 1.0f;
+            float csv[NCH];
+#pragma unroll
+            for (int j = 0; j < NCH; ++j)
+                csv[j] = args.col_scale ? args.col_scale[ti.n0 + half * COLS + j * 32 + lane] : 1.0f;
             // lane 0 waits; the result is broadcast so the warp stays converged
             // for the warp-wide tensor-memory loads below
             const int got = __shfl_sync(0xffffffffu,
@@ -326,23 +335,32 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 const float gb = args.gs_b ? args.gs_b[g] : 1.0f;
                 gs = ga * gb;
             }
-            const int32_t row = ti.row0 + quad * 32 + lane;
-            if (row < ti.row_end) {
+            if (args.row_scale) gs = gs * rsv;
+            const bool cscale = args.col_scale != nullptr;
+            if (row < ti.row_end || cscale) {
                 __nv_bfloat16 *dst = args.D + static_cast<size_t>(row) * args.N + ti.n0 + half * COLS;
 #pragma unroll
                 for (int j = 0; j < NCH; ++j) {
                     uint32_t packed[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float lo = __uint_as_float(v[j][2 * i]) * gs;
-                        const float hi = __uint_as_float(v[j][2 * i + 1]) * gs;
+                        float lo = __uint_as_float(v[j][2 * i]) * gs;
+                        float hi = __uint_as_float(v[j][2 * i + 1]) * gs;
+                        if (cscale) {
+                            // every lane of the warp takes part in the shuffles
+                            lo = lo * __shfl_sync(0xffffffffu, csv[j], 2 * i);
+                            hi = hi * __shfl_sync(0xffffffffu, csv[j], 2 * i + 1);
+                        }
                         __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
                         packed[i] = *reinterpret_cast<uint32_t *>(&p);
                     }
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + j * 32);
+                    if (row < ti.row_end) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + j * 32);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                        for (int i = 0; i < 4; ++i)
+                            d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                               packed[4 * i + 3]);
+                    }
                 }
             }
         }
@@ -464,10 +482,9 @@ extern "C" size_t qfp4_gemm_workspace_bytes(int fmt, int64_t M, int64_t N, int64
     return 0;   // every kernel keeps its partial sums on chip
 }
 
-extern "C" int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K, const void *A_packed,
-                            const void *A_sf, const void *B_packed, const void *B_sf,
-                            const float *gs_a, const float *gs_b, void *D_bf16, void *workspace,
-                            size_t ws_bytes, void *stream)
+static int gemm_nt_impl(int fmt, int64_t M, int64_t N, int64_t K, const void *A_packed, const void *A_sf,
+                        const void *B_packed, const void *B_sf, const float *gs_a, const float *gs_b,
+                        const float *row_scale, const float *col_scale, void *D_bf16, void *stream)
 {
     if (fmt != QFP4_MXFP4 && fmt != QFP4_NVFP4) return QFP4_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0) return QFP4_ERR_INVALID_ARG;
@@ -485,14 +502,14 @@ extern "C" int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K, const void
     }
     if (!A_packed || !A_sf || !B_packed || !B_sf) return QFP4_ERR_INVALID_ARG;
     if (!aligned16(A_packed) || !aligned16(A_sf) || !aligned16(B_packed) || !aligned16(B_sf) ||
-        !aligned16(D_bf16) || (gs_a && !aligned4(gs_a)) || (gs_b && !aligned4(gs_b)))
+        !aligned16(D_bf16) || (gs_a && !aligned4(gs_a)) || (gs_b && !aligned4(gs_b)) ||
+        (row_scale && !aligned4(row_scale)) || (col_scale && !aligned4(col_scale)))
         return QFP4_ERR_MISALIGNED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     GemmParams a{static_cast<const uint8_t *>(A_sf), static_cast<const uint8_t *>(B_sf), gs_a, gs_b,
                  static_cast<__nv_bfloat16 *>(D_bf16), static_cast<int32_t>(M), static_cast<int32_t>(N),
-                 static_cast<int32_t>(K), 0, nullptr};
+                 static_cast<int32_t>(K), 0, nullptr, row_scale, col_scale};
     CUtensorMap ma, mb;
-    (void)workspace; (void)ws_bytes;
     if (M <= 128) {
         // decode shapes: swap AB on CTA pairs, weights in the MMA's M slot
         CUtensorMap md;
@@ -528,6 +545,27 @@ extern "C" int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K, const void
     }
     if (wide) return launch_gemm<QFP4_MXFP4, 256, 4, false>(ma, mb, a, mtiles * (N / 256), s);
     return launch_gemm<QFP4_MXFP4, 128, 6, false>(ma, mb, a, mtiles * (N / 128), s);
+}
+
+extern "C" int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K, const void *A_packed,
+                            const void *A_sf, const void *B_packed, const void *B_sf,
+                            const float *gs_a, const float *gs_b, void *D_bf16, void *workspace,
+                            size_t ws_bytes, void *stream)
+{
+    (void)workspace; (void)ws_bytes;
+    return gemm_nt_impl(fmt, M, N, K, A_packed, A_sf, B_packed, B_sf, gs_a, gs_b, nullptr, nullptr, D_bf16,
+                        stream);
+}
+
+extern "C" int qfp4_gemm_nt_scaled(int fmt, int64_t M, int64_t N, int64_t K, const void *A_packed,
+                                   const void *A_sf, const void *B_packed, const void *B_sf,
+                                   const float *gs_a, const float *gs_b, const float *row_scale,
+                                   const float *col_scale, void *D_bf16, void *workspace, size_t ws_bytes,
+                                   void *stream)
+{
+    (void)workspace; (void)ws_bytes;
+    return gemm_nt_impl(fmt, M, N, K, A_packed, A_sf, B_packed, B_sf, gs_a, gs_b, row_scale, col_scale,
+                        D_bf16, stream);
 }
 
 extern "C" int qfp4_gemm_nt_grouped(int fmt, int64_t groups, const int32_t *row_offsets,

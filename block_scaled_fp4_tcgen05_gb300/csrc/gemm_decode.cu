@@ -282,6 +282,18 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         // memory (a warp writes 64 consecutive bytes per token), and one
         // TMA store moves the tile to D; rows m >= M are clipped by it.
         if (set == 0) {
+        // two-level epilogue: D[m][n] = bf16((acc * (gs * row_scale[m])) *
+        // col_scale[n]); here n is this lane's weight row and the tokens m
+        // are the columns, so the column scale is per lane and lane i holds
+        // the row scale of token 32 j + i, shared out by shuffles.  Read
+        // before the accumulator wait.
+        const int n_lane = quad * 32 + lane;
+        const float cs_lane = (p.col_scale && w_valid) ? p.col_scale[wtile * 128 + n_lane] : 1.0f;
+        float rsv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            rsv[j] = (p.row_scale && j * 32 + lane < p.M) ? p.row_scale[j * 32 + lane] : 1.0f;
+        const bool rscale = p.row_scale != nullptr, cscale = p.col_scale != nullptr;
         const int got = ok ? __shfl_sync(0xffffffffu,
                                          lane == 0 ? (mbar_wait(smem_u32(acc_full), 0) ? 1 : 0) : 0, 0)
                            : 0;
@@ -303,9 +315,19 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 tmem_ld_32x32b_x32(taddr + j * 32, v);
                 tmem_ld_wait();
                 tmem_regs_after_wait(v);
+                const float rs_j = j == 0 ? rsv[0] : j == 1 ? rsv[1] : j == 2 ? rsv[2] : rsv[3];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    const float a = __uint_as_float(v[i]) * gs, b = __uint_as_float(v[i + 1]) * gs;
+                    float ga = gs, gb = gs;
+                    if (rscale) {
+                        ga = gs * __shfl_sync(0xffffffffu, rs_j, i);
+                        gb = gs * __shfl_sync(0xffffffffu, rs_j, i + 1);
+                    }
+                    float a = __uint_as_float(v[i]) * ga, b = __uint_as_float(v[i + 1]) * gb;
+                    if (cscale) {
+                        a = a * cs_lane;
+                        b = b * cs_lane;
+                    }
                     const float other = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
                     const int m = j * 32 + i + (odd ? 1 : 0);
                     // columns n0 (low half) and n0 + 1 (high half) of token row m

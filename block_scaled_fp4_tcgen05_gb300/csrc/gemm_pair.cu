@@ -125,7 +125,10 @@ struct PairTile {
     int32_t group;
 };
 
-template <int FMT, bool GROUPED, bool DBL>
+// SCALED: the two-level epilogue (per-row and per-column rescale), dense only;
+// a separate instantiation so that the plain kernels carry none of its
+// registers.
+template <int FMT, bool GROUPED, bool DBL, bool SCALED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmD, const GemmParams p)
@@ -465,6 +468,18 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             float gs = gs_dense;
             if (FMT == QFP4_NVFP4 && GROUPED)
                 gs = (p.gs_a ? p.gs_a[ti.group] : 1.0f) * (p.gs_b ? p.gs_b[ti.group] : 1.0f);
+            // two-level epilogue (dense only): the row's scale folds into gs;
+            // lane i holds the scale of column 32 j + i of chunk j, shared
+            // out by shuffles during the conversion
+            float csv[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+            if (SCALED) {
+                const int32_t r = ti.row0 + 128 * static_cast<int32_t>(rank) + quad * 32 + lane;
+                if (p.row_scale) gs = gs * (r < ti.row_end ? p.row_scale[r] : 1.0f);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    csv[j] = p.col_scale ? p.col_scale[ti.n0 + half * 128 + j * 32 + lane] : 1.0f;
+            }
+            const bool cscale = SCALED && p.col_scale != nullptr;
             // A warp whose wait runs out still takes part in this tile's
             // named barrier below (its drain reads are harmless); the barrier
             // ANDs every thread's view of "all well", so the eight warps
@@ -492,8 +507,12 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 tmem_regs_after_wait(v);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * gs,
-                                                              __uint_as_float(v[2 * i + 1]) * gs);
+                    float lo = __uint_as_float(v[2 * i]) * gs, hi = __uint_as_float(v[2 * i + 1]) * gs;
+                    if (cscale) {
+                        lo = lo * __shfl_sync(0xffffffffu, csv[j], 2 * i);
+                        hi = hi * __shfl_sync(0xffffffffu, csv[j], 2 * i + 1);
+                    }
+                    __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
                     packed[j][i] = *reinterpret_cast<uint32_t *>(&pr);
                 }
             }
@@ -507,8 +526,12 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             uint32_t q3[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(last[2 * i]) * gs,
-                                                          __uint_as_float(last[2 * i + 1]) * gs);
+                float lo = __uint_as_float(last[2 * i]) * gs, hi = __uint_as_float(last[2 * i + 1]) * gs;
+                if (cscale) {
+                    lo = lo * __shfl_sync(0xffffffffu, csv[3], 2 * i);
+                    hi = hi * __shfl_sync(0xffffffffu, csv[3], 2 * i + 1);
+                }
+                __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
                 q3[i] = *reinterpret_cast<uint32_t *>(&pr);
             }
             // Stores: the warp's 32 rows x 128 columns leave as eight TMA
@@ -572,12 +595,12 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     }
 }
 
-template <int FMT, bool GROUPED, bool DBL = false>
+template <int FMT, bool GROUPED, bool DBL = false, bool SCALED = false>
 int launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &md, const GemmParams &prm,
            int64_t pair_tiles, cudaStream_t s)
 {
     using C = PairCfg<FMT, GROUPED, DBL>;
-    auto kern = gemm_pair_kernel<FMT, GROUPED, DBL>;
+    auto kern = gemm_pair_kernel<FMT, GROUPED, DBL, SCALED>;
     static int configured_device = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return QFP4_ERR_CUDA;
@@ -604,8 +627,13 @@ bool gemm_pair_double_stages(int fmt, bool grouped, int64_t K)
 int launch_gemm_pair(int fmt, bool grouped, const CUtensorMap &ma, const CUtensorMap &mb,
                      const CUtensorMap &md, const GemmParams &prm, int64_t pair_tiles, cudaStream_t s)
 {
+    const bool scaled = !grouped && (prm.row_scale || prm.col_scale);
     if (gemm_pair_double_stages(fmt, grouped, prm.K))
-        return launch<QFP4_MXFP4, false, true>(ma, mb, md, prm, pair_tiles, s);
+        return scaled ? launch<QFP4_MXFP4, false, true, true>(ma, mb, md, prm, pair_tiles, s)
+                      : launch<QFP4_MXFP4, false, true>(ma, mb, md, prm, pair_tiles, s);
+    if (scaled)
+        return fmt == QFP4_NVFP4 ? launch<QFP4_NVFP4, false, false, true>(ma, mb, md, prm, pair_tiles, s)
+                                 : launch<QFP4_MXFP4, false, false, true>(ma, mb, md, prm, pair_tiles, s);
     if (fmt == QFP4_NVFP4)
         return grouped ? launch<QFP4_NVFP4, true>(ma, mb, md, prm, pair_tiles, s)
                        : launch<QFP4_NVFP4, false>(ma, mb, md, prm, pair_tiles, s);

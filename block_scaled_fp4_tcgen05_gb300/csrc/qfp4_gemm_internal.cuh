@@ -18,6 +18,10 @@ struct GemmParams {
     int32_t M, N, K;
     int32_t groups;             // grouped launches only
     const int32_t *row_offsets; // grouped launches only (device, groups + 1)
+    // two-level epilogue (dense launches only): D[m,n] =
+    // bf16((acc * (gs_a*gs_b * row_scale[m])) * col_scale[n]); NULL = ones
+    const float *row_scale;     // [M] or NULL
+    const float *col_scale;     // [N] or NULL
 };
 
 // 2D byte matrix [rows, inner] tensor map with 128-byte swizzle and a box of

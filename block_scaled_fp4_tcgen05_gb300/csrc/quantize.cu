@@ -318,7 +318,8 @@ __host__ __device__ constexpr uint64_t div_magic(uint64_t d) { return ~0ull / d 
 // threads take consecutive blocks, so the four scale bytes of one 32-bit word
 // of the scale layout come from four neighbouring lanes.  GROUPED: per-row
 // global scale gs[group] and the per-group MMA scale layout.
-template <int FMT, int SF_LAYOUT, bool GROUPED>
+// ROWGS (NVFP4): row m has its own global scale gs_ptr[m] (two-level NVFP4).
+template <int FMT, int SF_LAYOUT, bool GROUPED, bool ROWGS = false>
 __global__ void __launch_bounds__(kThreads, 4)
 quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
                 const float *__restrict__ gs_ptr, uint8_t *__restrict__ Q,
@@ -358,7 +359,7 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
         }
     }
     __syncthreads();
-    const float gs_one = (FMT == QFP4_MXFP4 || GROUPED) ? 1.0f : *gs_ptr;
+    const float gs_one = (FMT == QFP4_MXFP4 || GROUPED || ROWGS) ? 1.0f : *gs_ptr;
     const float inv_gs_one = __frcp_rn(gs_one);
 
     // MMA layout without groups: zero the padding rows [M, ceil128(M)).
@@ -422,6 +423,10 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
                     gs = gs_ptr[grp];
                     inv_gs = __frcp_rn(gs);
                 }
+            }
+            if (ROWGS && FMT == QFP4_NVFP4 && valid) {
+                gs = gs_ptr[row];
+                inv_gs = __frcp_rn(gs);
             }
             const BlockScale bs = block_scale<FMT>(amax, gs, inv_gs);
             uint32_t packed[W / 4];
@@ -585,6 +590,51 @@ amax_flat_kernel(const uint4 *__restrict__ X, int64_t nvec, uint32_t *__restrict
     }
 }
 
+// Per-row global scales (two-level NVFP4): one warp per row, gs[r] =
+// amax(row r) / (6 * 448), written directly (no atomics, no zeroing).
+__global__ void __launch_bounds__(kThreads)
+gs_rows_kernel(const uint4 *__restrict__ X, int64_t rows, int64_t chunks_per_row, float *__restrict__ gs_out)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t r = warp; r < rows; r += nwarps) {
+        const uint4 *p = X + r * chunks_per_row;
+        float m = 0.0f;
+        int64_t i = lane;
+        for (; i + 96 < chunks_per_row; i += 128) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = ld_stream_v4(p + i + 32 * u);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float lo, hi;
+                    bf16x2_to_f32(w[j], lo, hi);
+                    m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
+                }
+            }
+        }
+        for (; i < chunks_per_row; i += 32) {
+            const uint4 v = ld_stream_v4(p + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float lo, hi;
+                bf16x2_to_f32(w[j], lo, hi);
+                m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) gs_out[r] = __fdiv_rn(m, 2688.0f);
+    }
+}
+
 // Zeroes the amax words before the atomics of the amax kernels.  A kernel
 // rather than a memset so that the next launch overlaps it; its wait also
 // keeps it behind the previous kernel, which may still read these words as
@@ -650,7 +700,7 @@ int grid_for(int64_t work_items, int per_block)
     return static_cast<int>(g < 1 ? 1 : g);
 }
 
-template <int FMT, int LAYOUT, bool GROUPED>
+template <int FMT, int LAYOUT, bool GROUPED, bool ROWGS = false>
 cudaError_t launch_quantize(const void *X, int64_t M, int64_t K, const float *gs, void *Q,
                             void *SF, int groups, const int32_t *offs, cudaStream_t s)
 {
@@ -659,7 +709,7 @@ cudaError_t launch_quantize(const void *X, int64_t M, int64_t K, const float *gs
     constexpr int kChunkBytes = chunk_bytes<FMT>();
     const int64_t chunks = (blocks * 2 * G + kChunkBytes - 1) / kChunkBytes;
     constexpr int smem = kQStages * kChunkBytes + 2 * kQStages * 8;
-    auto kern = quantize_kernel<FMT, LAYOUT, GROUPED>;
+    auto kern = quantize_kernel<FMT, LAYOUT, GROUPED, ROWGS>;
     static int configured_device = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorUnknown;
@@ -743,6 +793,53 @@ extern "C" int qfp4_global_scale_grouped(const void *X_bf16, int64_t total_rows,
     }
     return launch_status(launch_pdl(gs_finalize_kernel, dim3((static_cast<unsigned>(groups) + 127) / 128), dim3(128),
                                     0, s, reinterpret_cast<uint32_t *>(gs_out), static_cast<int>(groups)));
+}
+
+extern "C" int qfp4_global_scale_rows(const void *X_bf16, int64_t rows, int64_t cols, float *gs_out,
+                                      void *stream)
+{
+    if (rows < 0 || cols < 0) return QFP4_ERR_INVALID_ARG;
+    if (cols % 8 != 0) return QFP4_ERR_UNSUPPORTED;
+    if (rows == 0) return QFP4_OK;
+    if (!gs_out) return QFP4_ERR_INVALID_ARG;
+    if (!aligned4(gs_out)) return QFP4_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cols == 0)      // empty rows: amax 0, gs 0
+        return cudaMemsetAsync(gs_out, 0, sizeof(float) * rows, s) == cudaSuccess ? QFP4_OK : QFP4_ERR_CUDA;
+    if (!X_bf16) return QFP4_ERR_INVALID_ARG;
+    if (!aligned16(X_bf16)) return QFP4_ERR_MISALIGNED;
+    const int grid = grid_for(rows, kThreads / 32);
+    return launch_status(launch_pdl(gs_rows_kernel, dim3(grid), dim3(kThreads), 0, s,
+                                    static_cast<const uint4 *>(X_bf16), rows, cols / 8, gs_out));
+}
+
+extern "C" int qfp4_quantize_rows(int fmt, const void *X_bf16, int64_t M, int64_t K, const float *gs_rows,
+                                  void *Q_packed, void *SF, int sf_layout, void *stream)
+{
+    if (fmt != QFP4_MXFP4 && fmt != QFP4_NVFP4) return QFP4_ERR_INVALID_ARG;
+    if (sf_layout != QFP4_SF_ROWMAJOR && sf_layout != QFP4_SF_MMA) return QFP4_ERR_INVALID_ARG;
+    if (M < 0 || K < 0) return QFP4_ERR_INVALID_ARG;
+    if (K % 128 != 0) return QFP4_ERR_UNSUPPORTED;
+    if (M == 0 || K == 0) return QFP4_OK;
+    if ((M + 128) * (K / 16) >= (int64_t{1} << 32) - 4096) return QFP4_ERR_UNSUPPORTED;
+    if (!X_bf16 || !Q_packed || !SF) return QFP4_ERR_INVALID_ARG;
+    if (fmt == QFP4_NVFP4 && !gs_rows) return QFP4_ERR_INVALID_ARG;
+    if (!aligned16(X_bf16) || !aligned16(Q_packed) || !aligned4(SF) || (gs_rows && !aligned4(gs_rows)))
+        return QFP4_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (fmt == QFP4_MXFP4)        // MXFP4 has no global scale: the plain quantiser
+        e = sf_layout == QFP4_SF_MMA
+                ? launch_quantize<QFP4_MXFP4, QFP4_SF_MMA, false>(X_bf16, M, K, nullptr, Q_packed, SF, 1, nullptr, s)
+                : launch_quantize<QFP4_MXFP4, QFP4_SF_ROWMAJOR, false>(X_bf16, M, K, nullptr, Q_packed, SF, 1,
+                                                                       nullptr, s);
+    else
+        e = sf_layout == QFP4_SF_MMA
+                ? launch_quantize<QFP4_NVFP4, QFP4_SF_MMA, false, true>(X_bf16, M, K, gs_rows, Q_packed, SF, 1,
+                                                                        nullptr, s)
+                : launch_quantize<QFP4_NVFP4, QFP4_SF_ROWMAJOR, false, true>(X_bf16, M, K, gs_rows, Q_packed, SF,
+                                                                             1, nullptr, s);
+    return launch_status(e);
 }
 
 extern "C" int qfp4_quantize(int fmt, const void *X_bf16, int64_t M, int64_t K, const float *gs,

@@ -37,6 +37,10 @@ SIGNATURES = {
     "qfp4_global_scale": (_i32, [_vp, _i64, _i64, _vp, _vp]),
     "qfp4_global_scale_grouped": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
     "qfp4_quantize": (_i32, [_i32, _vp, _i64, _i64, _vp, _vp, _vp, _i32, _vp]),
+    "qfp4_global_scale_rows": (_i32, [_vp, _i64, _i64, _vp, _vp]),
+    "qfp4_quantize_rows": (_i32, [_i32, _vp, _i64, _i64, _vp, _vp, _vp, _i32, _vp]),
+    "qfp4_gemm_nt_scaled": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                   _sz, _vp]),
     "qfp4_quantize_grouped": (_i32, [_i32, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "qfp4_sf_interleave": (_i32, [_vp, _i64, _i64, _vp, _i32, _vp]),
     "qfp4_gemm_workspace_bytes": (_sz, [_i32, _i64, _i64, _i64]),
@@ -141,6 +145,20 @@ def quantize(fmt, X, gs, Q, SF, sf_layout=SF_ROWMAJOR, stream=None) -> None:
            load().qfp4_quantize(fmt, _p(X), M, K, _p(gs), _p(Q), _p(SF), sf_layout, _stream(stream)))
 
 
+def global_scale_rows(X, gs_out, stream=None) -> None:
+    """Per-row NVFP4 global scales: gs_out[r] = amax(row r) / (6*448)."""
+    rows, cols = X.shape
+    _check("qfp4_global_scale_rows",
+           load().qfp4_global_scale_rows(_p(X), rows, cols, _p(gs_out), _stream(stream)))
+
+
+def quantize_rows(fmt, X, gs_rows, Q, SF, sf_layout=SF_ROWMAJOR, stream=None) -> None:
+    """Quantise with one global scale per row (two-level NVFP4)."""
+    M, K = X.shape
+    _check("qfp4_quantize_rows",
+           load().qfp4_quantize_rows(fmt, _p(X), M, K, _p(gs_rows), _p(Q), _p(SF), sf_layout, _stream(stream)))
+
+
 def quantize_grouped(fmt, X, row_offsets, gs, Q, SF_mma, stream=None) -> None:
     rows, K = X.shape
     groups = row_offsets.numel() - 1
@@ -152,6 +170,16 @@ def quantize_grouped(fmt, X, row_offsets, gs, Q, SF_mma, stream=None) -> None:
 def sf_interleave(SF_in, rows, cols, SF_out, layout=SF_MMA, stream=None) -> None:
     _check("qfp4_sf_interleave",
            load().qfp4_sf_interleave(_p(SF_in), rows, cols, _p(SF_out), layout, _stream(stream)))
+
+
+def gemm_nt_scaled(fmt, M, N, K, A, A_sf, B, B_sf, gs_a, gs_b, row_scale, col_scale, D, workspace=None,
+                   ws_bytes=0, stream=None) -> None:
+    """The GEMM with the two-level epilogue: row m of D times row_scale[m],
+    column n times col_scale[n] (either may be None)."""
+    _check("qfp4_gemm_nt_scaled",
+           load().qfp4_gemm_nt_scaled(fmt, M, N, K, _p(A), _p(A_sf), _p(B), _p(B_sf), _p(gs_a), _p(gs_b),
+                                      _p(row_scale), _p(col_scale), _p(D), _p(workspace), ws_bytes,
+                                      _stream(stream)))
 
 
 def gemm_nt(fmt, M, N, K, A, A_sf, B, B_sf, gs_a, gs_b, D, workspace=None, ws_bytes=0,

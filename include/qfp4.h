@@ -115,6 +115,14 @@ int qfp4_global_scale_grouped(const void *X_bf16, int64_t total_rows, int64_t co
                               int64_t groups, const int32_t *row_offsets, float *gs_out,
                               void *stream);
 
+/* Per-row global scales (two-level NVFP4; quadbit README, "Accuracy (real
+ * models)": per-16 UE4M3 local scales under a per-row fp32 global scale):
+ * gs_out[r] = amax(|X[r, :]|) / (6 * 448), the rule of qfp4_global_scale on
+ * each row alone.  gs_out is a DEVICE fp32 [rows].  Requirements as
+ * qfp4_global_scale; rows == 0 launches nothing, cols == 0 writes zeros. */
+int qfp4_global_scale_rows(const void *X_bf16, int64_t rows, int64_t cols, float *gs_out,
+                           void *stream);
+
 /* ---------------------------------------------------------------------- */
 /* Quantiser                                                                */
 /* ---------------------------------------------------------------------- */
@@ -136,6 +144,14 @@ int qfp4_global_scale_grouped(const void *X_bf16, int64_t total_rows, int64_t co
  * Requirements: M >= 0, K % 128 == 0, X/Q 16-byte aligned, SF 4-byte aligned. */
 int qfp4_quantize(int fmt, const void *X_bf16, int64_t M, int64_t K, const float *gs,
                   void *Q_packed, void *SF, int sf_layout, void *stream);
+
+/* Quantiser with a per-row global scale (two-level NVFP4): row m is
+ * quantised exactly as qfp4_quantize quantises it alone with
+ * gs = gs_rows[m] (bit-exact to that rule).  gs_rows is a DEVICE fp32 [M]
+ * (required for NVFP4; MXFP4 ignores it and runs qfp4_quantize).  Other
+ * arguments and requirements as qfp4_quantize. */
+int qfp4_quantize_rows(int fmt, const void *X_bf16, int64_t M, int64_t K, const float *gs_rows,
+                       void *Q_packed, void *SF, int sf_layout, void *stream);
 
 /* Per-group quantiser for MoE-shaped batches (Mojo page "fp4_quantization",
  * grouped_quantize_dynamic_scaled_fp4_async): rows of group e use gs[e]; the
@@ -167,9 +183,9 @@ int qfp4_sf_interleave(const void *SF_in, int64_t rows, int64_t cols, void *SF_o
 /* ---------------------------------------------------------------------- */
 
 /* Workspace bytes qfp4_gemm_nt uses for this shape.  Every kernel keeps its
- * partial sums on chip (tensor memory, and distributed shared memory for
- * split-K), so this is 0; the argument is kept so that a caller written
- * against it needs no change if a future kernel uses scratch. */
+ * partial sums on chip (tensor memory), so this is 0; the argument is kept
+ * so that a caller written against it needs no change if a future kernel
+ * uses scratch. */
 size_t qfp4_gemm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K);
 
 /* D[M,N] (BF16, row-major) = bf16_rne(gs_a * gs_b * sum_k a[m,k] * b[n,k]),
@@ -195,6 +211,26 @@ int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K,
                  const void *B_packed, const void *B_sf,
                  const float *gs_a, const float *gs_b,
                  void *D_bf16, void *workspace, size_t ws_bytes, void *stream);
+
+/* Two-level epilogue (quadbit README, "Accuracy (real models)": a per-row and
+ * per-column fp32 global rescale in the MMA epilogue, the deploy path of
+ * NVFP4 with per-row global scales):
+ *   D[m,n] = bf16_rne( (acc[m,n] * (gs_a*gs_b * row_scale[m])) * col_scale[n] )
+ * in fp32, with acc the same sum as in qfp4_gemm_nt (MXFP4 ignores gs_a and
+ * gs_b, not the row and column scales).
+ *   row_scale  DEVICE fp32 [M] or NULL (ones), e.g. the activations' per-row
+ *              global scales from qfp4_global_scale_rows
+ *   col_scale  DEVICE fp32 [N] or NULL (ones), e.g. the weights' per-row
+ *              (output-channel) global scales
+ * With both NULL the result is bit-identical to qfp4_gemm_nt.  Same kernels,
+ * requirements and accuracy bound (with the scales in the exact product);
+ * the scale pointers must be 4-byte aligned. */
+int qfp4_gemm_nt_scaled(int fmt, int64_t M, int64_t N, int64_t K,
+                        const void *A_packed, const void *A_sf,
+                        const void *B_packed, const void *B_sf,
+                        const float *gs_a, const float *gs_b,
+                        const float *row_scale, const float *col_scale,
+                        void *D_bf16, void *workspace, size_t ws_bytes, void *stream);
 
 /* Grouped per-expert GEMM in one launch (quadbit README "End-to-end
  * serving": one-launch segmented MoE kernel; Mojo page: grouped per-expert

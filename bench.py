@@ -364,8 +364,55 @@ def sweep(device, l2_bytes, peaks):
                     "frac_fp4_peak": round(tf / fp4_peak, 3)})
     # grouped MoE up-projection
     out.append(grouped_time(device, fp4_peak))
+    # two-level NVFP4 (per-row global scales, row/column rescale in the epilogue)
+    out.append(two_level_time(device, l2_bytes, fp4_peak))
     torch.cuda.empty_cache()
     return out
+
+
+def two_level_time(device, l2_bytes, fp4_peak):
+    """NVFP4 4096^3 with per-row global scales: the step (per-row scales and
+    quantisation of the activations, GEMM with the row/column rescale) and the
+    rescaled GEMM against the plain one, weights rotated past the L2."""
+    import torch
+    from block_scaled_fp4_tcgen05_gb300 import qfp4
+    case = synth.PREFILL_NV
+    M, N, K = case.M, case.N, case.K
+    X = torch.from_numpy(synth.activations_bf16(case.seed, M, K).view(np.int16).copy()).view(
+        torch.bfloat16).to(device)
+    W = torch.from_numpy(synth.weights_bf16(case.seed + 1000, N, K).view(np.int16).copy()).view(
+        torch.bfloat16).to(device)
+    gs_x = torch.empty(M, dtype=torch.float32, device=device)
+    gs_w = torch.empty(N, dtype=torch.float32, device=device)
+    Qa = torch.empty((M, K // 2), dtype=torch.uint8, device=device)
+    SFa = torch.empty(qfp4.sf_mma_bytes(M, K // 16), dtype=torch.uint8, device=device)
+    Qb = torch.empty((N, K // 2), dtype=torch.uint8, device=device)
+    SFb = torch.empty(qfp4.sf_mma_bytes(N, K // 16), dtype=torch.uint8, device=device)
+    qfp4.global_scale_rows(W, gs_w)
+    qfp4.quantize_rows(qfp4.NVFP4, W, gs_w, Qb, SFb, qfp4.SF_MMA)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    copies = max(1, min(16, int(np.ceil(2 * l2_bytes / (Qb.numel() + SFb.numel()))) + 1))
+    Qs = [Qb] + [Qb.clone() for _ in range(copies - 1)]
+    SFs = [SFb] + [SFb.clone() for _ in range(copies - 1)]
+
+    def step(i):
+        qfp4.global_scale_rows(X, gs_x)
+        qfp4.quantize_rows(qfp4.NVFP4, X, gs_x, Qa, SFa, qfp4.SF_MMA)
+        qfp4.gemm_nt_scaled(qfp4.NVFP4, M, N, K, Qa, SFa, Qs[i], SFs[i], None, None, gs_x, gs_w, D)
+
+    step_ms = graph_time([(lambda i=i: step(i)) for i in range(copies)], 5)
+    scaled_ms = graph_time([(lambda i=i: qfp4.gemm_nt_scaled(qfp4.NVFP4, M, N, K, Qa, SFa, Qs[i], SFs[i], None,
+                                                              None, gs_x, gs_w, D)) for i in range(copies)], 5)
+    plain_ms = graph_time([(lambda i=i: qfp4.gemm_nt(qfp4.NVFP4, M, N, K, Qa, SFa, Qs[i], SFs[i], None, None, D))
+                           for i in range(copies)], 5)
+    flop = 2 * M * N * K
+    res = {"workload": f"nvfp4_two_level_{M}x{N}x{K}", "us_step": round(step_ms * 1e3, 2),
+           "TFLOP/s_step": round(flop / (step_ms * 1e-3) / 1e12, 1),
+           "us_gemm_rescaled": round(scaled_ms * 1e3, 2), "us_gemm_plain": round(plain_ms * 1e3, 2),
+           "rescale_cost": round(scaled_ms / plain_ms - 1.0, 3),
+           "frac_fp4_peak_gemm": round(flop / (scaled_ms * 1e-3) / 1e12 / fp4_peak, 3)}
+    del Qs, SFs, X, W
+    return res
 
 
 def grouped_time(device, fp4_peak):

@@ -252,7 +252,9 @@ def time_main(pipe, steps, warmup, flush, world, device, clocks_gpu):
 
 
 def time_e2e(pipe, steps, warmup):
-    """Same step through host buffers: pinned H2D of X, the path, D2H of D."""
+    """Same step through host buffers: pinned H2D of X, the path, D2H of D,
+    one step after the other on one stream.  Returns (ms per step, H2D
+    bytes, D2H bytes)."""
     torch = pipe.torch
     stream = torch.cuda.current_stream()
 
@@ -273,6 +275,72 @@ def time_e2e(pipe, steps, warmup):
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / steps
     return ms, pipe.X_pinned.numel() * 2, pipe.D_pinned.numel() * 2
+
+
+def time_e2e_pipelined(pipe, steps, warmup, slices=1):
+    """The same steps as a serving loop runs them: two steps in flight, the
+    H2D of X for step i+1 and the D2H of D from step i-1 overlapping the
+    kernels of step i, with two device copies of X and D (and two pinned D
+    buffers).  A copy may be split into `slices` row ranges on streams of
+    their own; measured on GB300, four slices were slower than one (more
+    host work per step, no more copy bandwidth), so one is the default.
+    Every step still moves all of its X in and all of its D out inside the
+    timed region.  Returns ms per step."""
+    torch = pipe.torch
+    dev = pipe.X.device
+    Xs = [pipe.X, torch.empty_like(pipe.X)]
+    Ds = [pipe.D, torch.empty_like(pipe.D)]
+    Dh = [pipe.D_pinned, torch.empty_like(pipe.D_pinned).pin_memory()]
+    s_in = [torch.cuda.Stream(device=dev) for _ in range(slices)]
+    s_out = [torch.cuda.Stream(device=dev) for _ in range(slices)]
+    s_run = torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()
+    h2d_done = [[ev() for _ in range(slices)] for _ in range(2)]
+    d2h_done = [[ev() for _ in range(slices)] for _ in range(2)]
+    run_done = [ev(), ev()]
+    cur = torch.cuda.current_stream()
+    for b in range(2):
+        run_done[b].record(cur)
+        for e_ in d2h_done[b]:
+            e_.record(cur)
+    xr = (pipe.X.shape[0] + slices - 1) // slices
+    dr = (pipe.D.shape[0] + slices - 1) // slices
+
+    def step(i):
+        b = i % 2
+        for k in range(slices):
+            with torch.cuda.stream(s_in[k]):
+                s_in[k].wait_event(run_done[b])          # step i-2 is done reading X[b]
+                Xs[b][k * xr:(k + 1) * xr].copy_(pipe.X_pinned[k * xr:(k + 1) * xr], non_blocking=True)
+                h2d_done[b][k].record(s_in[k])
+        with torch.cuda.stream(s_run):
+            for k in range(slices):
+                s_run.wait_event(h2d_done[b][k])
+                s_run.wait_event(d2h_done[b][k])         # step i-2's D[b] has left
+            pipe.prologue(Xs[b])
+            pipe.gemm(D=Ds[b])
+            run_done[b].record(s_run)
+        for k in range(slices):
+            with torch.cuda.stream(s_out[k]):
+                s_out[k].wait_event(run_done[b])
+                Dh[b][k * dr:(k + 1) * dr].copy_(Ds[b][k * dr:(k + 1) * dr], non_blocking=True)
+                d2h_done[b][k].record(s_out[k])
+
+    for i in range(max(warmup, 2)):
+        step(i)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(s_run)
+    for k in range(slices):
+        s_in[k].wait_stream(s_run)                       # nothing of the loop starts before `start`
+    for i in range(steps):
+        step(i)
+    for k in range(slices):
+        cur.wait_stream(s_out[k])
+    cur.wait_stream(s_run)
+    end.record(cur)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
 
 
 def graph_time(calls, reps=10):
@@ -635,7 +703,8 @@ def main():
             torch.distributed.destroy_process_group()
         return
 
-    e2e_ms, h2d, d2h = time_e2e(pipe, max(10, args.steps // 2), args.warmup)
+    e2e_serial_ms, h2d, d2h = time_e2e(pipe, max(10, args.steps // 2), args.warmup)
+    e2e_ms = time_e2e_pipelined(pipe, max(20, args.steps), args.warmup)
     gemm_tf = flops / (gemm_ms * 1e-3) / 1e12
     traffic = ncu_traffic("gemm_pair_kernel nvfp4 4096x4096x4096")
     roof = {"bound": "tensor", "achieved": round(gemm_tf, 1), "peak": round(fp4_peak, 1),
@@ -661,7 +730,11 @@ def main():
             "gpu_launches": pipe_kernels(case) * args.steps,
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "mode": "pipelined: H2D of step i+1 and D2H of step i-1 overlap step i (copy-in, "
+                            "kernel and copy-out streams, two device copies of X and D)",
+                    "ms_per_step": round(e2e_ms, 4),
+                    "serial_value": round(world * flops / (e2e_serial_ms * 1e-3) / 1e12, 2)},
             "clocks": clocks, "sweep": extra}
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -46,6 +46,7 @@ int read_clear_status_quant(cudaStream_t s, uint32_t *out)
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kQThreads = kThreads + 32;   // quantiser CTA: 8 consumer warps + 1 producer warp
 constexpr int kMaxGroups = 256;
 
 __device__ __forceinline__ uint4 ld_stream_v4(const uint4 *p)
@@ -320,7 +321,7 @@ __host__ __device__ constexpr uint64_t div_magic(uint64_t d) { return ~0ull / d 
 // global scale gs[group] and the per-group MMA scale layout.
 // ROWGS (NVFP4): row m has its own global scale gs_ptr[m] (two-level NVFP4).
 template <int FMT, int SF_LAYOUT, bool GROUPED, bool ROWGS = false>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kQThreads, 4)
 quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
                 const float *__restrict__ gs_ptr, uint8_t *__restrict__ Q,
                 uint8_t *__restrict__ SF, int64_t M, int groups,
@@ -380,8 +381,9 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
     const int lane = threadIdx.x & 31;
     bool ok = true;
 
-    // producer: thread 0 issues the first kQStages chunks, then one chunk
-    // per consumed chunk (after the stage's empty barrier completes)
+    // producer: the ninth warp's lane 0 keeps kQStages chunks in flight,
+    // refilling a stage as soon as the eight consumer warps have released it
+    // (a consumer thread doing this would hold up its own warp every chunk)
     auto issue = [&](int64_t c, uint32_t it) {
         const uint32_t st = it % kQStages;
         const int64_t off = c * kChunkBytes;
@@ -390,9 +392,25 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
         mbar_arrive_expect_tx(smem_u32(&full[st]), bytes);
         bulk_load(smem_u32(qsmem + st * kChunkBytes), X + off, bytes, smem_u32(&full[st]));
     };
-    if (threadIdx.x == 0) {
-        uint32_t it = 0;
-        for (int64_t c = blockIdx.x; c < nchunks && it < kQStages; c += gridDim.x, ++it) issue(c, it);
+    if (threadIdx.x >= kThreads) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++it) {
+                const uint32_t st = it % kQStages;
+                // stage st was last filled for iteration it - kQStages
+                if (it >= kQStages && !mbar_wait(smem_u32(&empty[st]), ((it / kQStages) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                issue(c, it);
+            }
+        }
+        if (!ok) {
+            atomicOr(&g_status_quant, static_cast<uint32_t>(kStatusTimeout));
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 1000000ull) { }
+        }
+        return;
     }
     uint32_t it = 0;
     for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++it) {
@@ -457,13 +475,6 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
-        if (threadIdx.x == 0) {
-            const int64_t cn = c + static_cast<int64_t>(kQStages) * gridDim.x;
-            if (cn < nchunks) {
-                if (!mbar_wait(smem_u32(&empty[st]), ph)) { ok = false; break; }
-                issue(cn, it + kQStages);
-            }
-        }
     }
     if (!ok) atomicOr(&g_status_quant, static_cast<uint32_t>(kStatusTimeout));
     // no bulk copy may be left in flight: every issued chunk was consumed,
@@ -723,7 +734,7 @@ cudaError_t launch_quantize(const void *X, int64_t M, int64_t K, const float *gs
     // dependent chain, and more warps hide it
     int64_t grid = static_cast<int64_t>(sms > 0 ? sms : 148) * 4;
     if (chunks < grid) grid = chunks > 0 ? chunks : 1;
-    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, s,
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kQThreads), smem, s,
                       static_cast<const uint8_t *>(X), blocks, K, gs, static_cast<uint8_t *>(Q),
                       static_cast<uint8_t *>(SF), M, groups, offs, div_magic(static_cast<uint64_t>(K / G)));
 }

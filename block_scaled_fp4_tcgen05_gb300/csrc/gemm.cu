@@ -534,16 +534,12 @@ static int gemm_nt_impl(int fmt, int64_t M, int64_t N, int64_t K, const void *A_
         if (rc != QFP4_OK) return rc;
         return launch_gemm_pair(fmt, false, ma, mb, md, a, ((M + 255) / 256) * (N / 256), s);
     }
-    const bool wide = N % 256 == 0;
+    // single CTAs on 128 x 128 tiles (M > 128, N % 256 == 128)
     int rc = make_map(&ma, A_packed, K / 2, M, kBKBytes, kBM);
-    if (rc == QFP4_OK) rc = make_map(&mb, B_packed, K / 2, N, kBKBytes, wide ? 256 : 128);
+    if (rc == QFP4_OK) rc = make_map(&mb, B_packed, K / 2, N, kBKBytes, 128);
     if (rc != QFP4_OK) return rc;
     const int32_t mtiles = static_cast<int32_t>((M + kBM - 1) / kBM);
-    if (fmt == QFP4_NVFP4) {
-        if (wide) return launch_gemm<QFP4_NVFP4, 256, 4, false>(ma, mb, a, mtiles * (N / 256), s);
-        return launch_gemm<QFP4_NVFP4, 128, 6, false>(ma, mb, a, mtiles * (N / 128), s);
-    }
-    if (wide) return launch_gemm<QFP4_MXFP4, 256, 4, false>(ma, mb, a, mtiles * (N / 256), s);
+    if (fmt == QFP4_NVFP4) return launch_gemm<QFP4_NVFP4, 128, 6, false>(ma, mb, a, mtiles * (N / 128), s);
     return launch_gemm<QFP4_MXFP4, 128, 6, false>(ma, mb, a, mtiles * (N / 128), s);
 }
 

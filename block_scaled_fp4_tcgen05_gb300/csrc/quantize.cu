@@ -485,23 +485,18 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
     }
 }
 
-// amax over rows of X, one warp per row (the per-expert global scales; one
-// group uses amax_flat_kernel); per group via atomicMax on the bit pattern
-// (non-negative floats order like unsigned integers).  Without
-// groups the warps of a CTA first fold their maxima in shared memory, so
-// that one atomic per CTA (not per row) reaches the single global word.
+// Per-expert amax (the grouped global scales): one warp per row, each row's
+// maximum folded into its group's word with atomicMax on the bit pattern
+// (non-negative floats order like unsigned integers); a warp keeps a running
+// maximum while its rows stay in one group.  One tensor uses amax_flat_kernel.
 __global__ void __launch_bounds__(kThreads)
 amax_rows_kernel(const uint4 *__restrict__ X, int64_t rows, int64_t chunks_per_row, int groups,
                  const int32_t *__restrict__ row_offsets, uint32_t *__restrict__ amax_bits)
 {
     __shared__ int32_t s_offs[kMaxGroups + 1];
-    __shared__ uint32_t s_max;
     pdl_wait();
     pdl_launch_dependents();
-    if (row_offsets) {
-        for (int i = threadIdx.x; i <= groups; i += blockDim.x) s_offs[i] = row_offsets[i];
-    }
-    if (threadIdx.x == 0) s_max = 0u;
+    for (int i = threadIdx.x; i <= groups; i += blockDim.x) s_offs[i] = row_offsets[i];
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
@@ -539,7 +534,7 @@ amax_rows_kernel(const uint4 *__restrict__ X, int64_t rows, int64_t chunks_per_r
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const int g = row_offsets ? find_group(s_offs, groups, r) : 0;
+        const int g = find_group(s_offs, groups, r);
         if (g != cur) {
             if (cur >= 0 && lane == 0) atomicMax(amax_bits + cur, __float_as_uint(run));
             cur = g;
@@ -547,13 +542,7 @@ amax_rows_kernel(const uint4 *__restrict__ X, int64_t rows, int64_t chunks_per_r
         }
         run = fmaxf(run, m);
     }
-    if (row_offsets) {
-        if (cur >= 0 && lane == 0) atomicMax(amax_bits + cur, __float_as_uint(run));
-        return;
-    }
-    if (cur >= 0 && lane == 0) atomicMax(&s_max, __float_as_uint(run));
-    __syncthreads();
-    if (threadIdx.x == 0 && s_max != 0u) atomicMax(amax_bits, s_max);
+    if (cur >= 0 && lane == 0) atomicMax(amax_bits + cur, __float_as_uint(run));
 }
 
 // amax over all of X (one group): the rows are contiguous, so X is walked as

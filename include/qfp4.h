@@ -201,7 +201,7 @@ size_t qfp4_gemm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K);
  * pairs with A and B swapped (256 weight rows per pair in the MMA's M slot,
  * the tokens in its N slot, all of K per pair, no split-K); M > 128 and
  * N % 256 == 0: CTA pairs (cta_group::2) on 256 x 256 tiles; otherwise
- * single-CTA 128 x 128 / 128 x 256 tiles.
+ * single-CTA 128 x 128 tiles.
  * Requirements: N % 128 == 0, K % 128 == 0, all pointers 16-byte aligned.
  * Degenerate shapes: M == 0 or N == 0 returns QFP4_OK with nothing launched
  * (no pointer is read); K == 0 is an empty sum and writes D = 0.

@@ -103,3 +103,38 @@ def test_grouped_and_interleave_reject_bad_arguments(lib):
     assert lib.qfp4_sf_interleave(FAKE, 0, 10, FAKE, 1, None) == 0
     assert lib.qfp4_global_scale(FAKE, 10, 12, FAKE, None) == -2
     assert lib.qfp4_global_scale(FAKE + 2, 10, 16, FAKE, None) == -3
+
+
+def test_two_level_entry_points_reject_bad_arguments(lib):
+    # per-row global scales
+    assert lib.qfp4_global_scale_rows(FAKE, -1, 16, FAKE, None) == -1
+    assert lib.qfp4_global_scale_rows(FAKE, 10, 12, FAKE, None) == -2          # cols % 8
+    assert lib.qfp4_global_scale_rows(FAKE, 10, 16, None, None) == -1
+    assert lib.qfp4_global_scale_rows(FAKE + 2, 10, 16, FAKE, None) == -3
+    assert lib.qfp4_global_scale_rows(FAKE, 10, 16, FAKE + 2, None) == -3
+    assert lib.qfp4_global_scale_rows(None, 0, 16, None, None) == 0            # no rows: nothing launched
+    # quantisation with per-row global scales
+    q = lib.qfp4_quantize_rows
+    assert q(2, FAKE, 16, 256, FAKE, FAKE, FAKE, 0, None) == -1               # format
+    assert q(1, FAKE, 16, 256, FAKE, FAKE, FAKE, 5, None) == -1               # layout
+    assert q(1, FAKE, 16, 200, FAKE, FAKE, FAKE, 0, None) == -2               # K % 128
+    assert q(1, FAKE, 16, 256, None, FAKE, FAKE, 0, None) == -1               # NVFP4 needs gs_rows
+    assert q(1, FAKE, 16, 256, FAKE + 2, FAKE, FAKE, 0, None) == -3
+    assert q(1, FAKE + 8, 16, 256, FAKE, FAKE, FAKE, 0, None) == -3
+    assert q(1, FAKE, 0, 256, FAKE, FAKE, FAKE, 0, None) == 0                 # empty
+    # GEMM with the row/column rescale
+    g = lib.qfp4_gemm_nt_scaled
+    base = [1, 256, 256, 256, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, None]
+
+    def call(i=None, v=None):
+        a = list(base)
+        if i is not None:
+            a[i] = v
+        return g(*a)
+
+    assert call(0, 3) == -1
+    assert call(1, -1) == -1
+    assert call(1, 0) == 0                                                       # empty D
+    assert call(2, 100) == -2                                                    # N % 128
+    assert call(10, FAKE + 2) == -3                                              # row_scale alignment
+    assert call(11, FAKE + 2) == -3                                              # col_scale alignment

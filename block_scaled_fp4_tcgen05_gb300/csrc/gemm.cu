@@ -309,7 +309,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             float csv[NCH];
 #pragma unroll
             for (int j = 0; j < NCH; ++j)
-                csv[j] = args.col_scale ? args.col_scale[ti.n0 + half * COLS + j * 32 + lane] : 1.0f;
+                csv[j] = args.col_scale
+                             ? args.col_scale[(GROUPED ? ti.group * args.N : 0) + ti.n0 + half * COLS + j * 32 + lane]
+                             : 1.0f;
             // lane 0 waits; the result is broadcast so the warp stays converged
             // for the warp-wide tensor-memory loads below
             const int got = __shfl_sync(0xffffffffu,
@@ -564,11 +566,11 @@ extern "C" int qfp4_gemm_nt_scaled(int fmt, int64_t M, int64_t N, int64_t K, con
                         D_bf16, stream);
 }
 
-extern "C" int qfp4_gemm_nt_grouped(int fmt, int64_t groups, const int32_t *row_offsets,
-                                    int64_t total_rows, int64_t max_group_rows, int64_t N, int64_t K,
-                                    const void *A_packed, const void *A_sf, const void *B_packed,
-                                    const void *B_sf, const float *gs_a, const float *gs_b,
-                                    void *D_bf16, void *stream)
+static int gemm_nt_grouped_impl(int fmt, int64_t groups, const int32_t *row_offsets, int64_t total_rows,
+                                int64_t max_group_rows, int64_t N, int64_t K, const void *A_packed,
+                                const void *A_sf, const void *B_packed, const void *B_sf, const float *gs_a,
+                                const float *gs_b, const float *row_scale, const float *col_scale, void *D_bf16,
+                                void *stream)
 {
     if (fmt != QFP4_MXFP4 && fmt != QFP4_NVFP4) return QFP4_ERR_INVALID_ARG;
     if (groups < 1 || !row_offsets || total_rows < 0 || max_group_rows < 0 || N < 1 || K < 1)
@@ -579,14 +581,14 @@ extern "C" int qfp4_gemm_nt_grouped(int fmt, int64_t groups, const int32_t *row_
         return QFP4_ERR_UNSUPPORTED;
     if (!aligned16(A_packed) || !aligned16(A_sf) || !aligned16(B_packed) || !aligned16(B_sf) ||
         !aligned16(D_bf16) || !aligned4(row_offsets) || (gs_a && !aligned4(gs_a)) ||
-        (gs_b && !aligned4(gs_b)))
+        (gs_b && !aligned4(gs_b)) || (row_scale && !aligned4(row_scale)) || (col_scale && !aligned4(col_scale)))
         return QFP4_ERR_MISALIGNED;
     if (total_rows == 0) return QFP4_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     GemmParams a{static_cast<const uint8_t *>(A_sf), static_cast<const uint8_t *>(B_sf), gs_a, gs_b,
                  static_cast<__nv_bfloat16 *>(D_bf16), static_cast<int32_t>(total_rows),
                  static_cast<int32_t>(N), static_cast<int32_t>(K), static_cast<int32_t>(groups),
-                 row_offsets};
+                 row_offsets, row_scale, col_scale};
     CUtensorMap ma, mb;
     (void)max_group_rows;
     if (N % 256 == 0) {
@@ -605,4 +607,25 @@ extern "C" int qfp4_gemm_nt_grouped(int fmt, int64_t groups, const int32_t *row_
     const int32_t tiles = static_cast<int32_t>(mt_bound * (N / 128));
     if (fmt == QFP4_NVFP4) return launch_gemm<QFP4_NVFP4, 128, 6, true>(ma, mb, a, tiles, s);
     return launch_gemm<QFP4_MXFP4, 128, 6, true>(ma, mb, a, tiles, s);
+}
+
+extern "C" int qfp4_gemm_nt_grouped(int fmt, int64_t groups, const int32_t *row_offsets,
+                                    int64_t total_rows, int64_t max_group_rows, int64_t N, int64_t K,
+                                    const void *A_packed, const void *A_sf, const void *B_packed,
+                                    const void *B_sf, const float *gs_a, const float *gs_b,
+                                    void *D_bf16, void *stream)
+{
+    return gemm_nt_grouped_impl(fmt, groups, row_offsets, total_rows, max_group_rows, N, K, A_packed, A_sf,
+                                B_packed, B_sf, gs_a, gs_b, nullptr, nullptr, D_bf16, stream);
+}
+
+extern "C" int qfp4_gemm_nt_grouped_scaled(int fmt, int64_t groups, const int32_t *row_offsets,
+                                           int64_t total_rows, int64_t max_group_rows, int64_t N, int64_t K,
+                                           const void *A_packed, const void *A_sf, const void *B_packed,
+                                           const void *B_sf, const float *gs_a, const float *gs_b,
+                                           const float *row_scale, const float *col_scale, void *D_bf16,
+                                           void *stream)
+{
+    return gemm_nt_grouped_impl(fmt, groups, row_offsets, total_rows, max_group_rows, N, K, A_packed, A_sf,
+                                B_packed, B_sf, gs_a, gs_b, row_scale, col_scale, D_bf16, stream);
 }

@@ -125,9 +125,9 @@ struct PairTile {
     int32_t group;
 };
 
-// SCALED: the two-level epilogue (per-row and per-column rescale), dense only;
-// a separate instantiation so that the plain kernels carry none of its
-// registers.
+// SCALED: the two-level epilogue (per-row and per-column rescale; grouped:
+// column scales [groups][N]); a separate instantiation so that the plain
+// kernels carry none of its registers.
 template <int FMT, bool GROUPED, bool DBL, bool SCALED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -468,18 +468,18 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             float gs = gs_dense;
             if (FMT == QFP4_NVFP4 && GROUPED)
                 gs = (p.gs_a ? p.gs_a[ti.group] : 1.0f) * (p.gs_b ? p.gs_b[ti.group] : 1.0f);
-            // two-level epilogue (dense only): the row's scale folds into gs;
-            // lane i holds the scale of column 32 j + i of chunk j, shared
-            // out by shuffles during the conversion
+            // two-level epilogue: the row's scale folds into gs; lane i holds
+            // the scale of column 32 j + i of chunk j, shared out by shuffles
+            // during the conversion
             float csv[4] = {1.0f, 1.0f, 1.0f, 1.0f};
             if (SCALED) {
                 const int32_t r = ti.row0 + 128 * static_cast<int32_t>(rank) + quad * 32 + lane;
                 if (p.row_scale) gs = gs * (r < ti.row_end ? p.row_scale[r] : 1.0f);
+                const int32_t c0 = (GROUPED ? ti.group * p.N : 0) + ti.n0 + half * 128;
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    csv[j] = p.col_scale ? p.col_scale[ti.n0 + half * 128 + j * 32 + lane] : 1.0f;
+                for (int j = 0; j < 4; ++j) csv[j] = p.col_scale ? p.col_scale[c0 + j * 32 + lane] : 1.0f;
             }
-            const bool cscale = SCALED && p.col_scale != nullptr;
+            const bool cscale = SCALED && p.col_scale != nullptr;   // uniform over the kernel
             // A warp whose wait runs out still takes part in this tile's
             // named barrier below (its drain reads are harmless); the barrier
             // ANDs every thread's view of "all well", so the eight warps
@@ -627,13 +627,17 @@ bool gemm_pair_double_stages(int fmt, bool grouped, int64_t K)
 int launch_gemm_pair(int fmt, bool grouped, const CUtensorMap &ma, const CUtensorMap &mb,
                      const CUtensorMap &md, const GemmParams &prm, int64_t pair_tiles, cudaStream_t s)
 {
-    const bool scaled = !grouped && (prm.row_scale || prm.col_scale);
+    const bool scaled = prm.row_scale || prm.col_scale;
     if (gemm_pair_double_stages(fmt, grouped, prm.K))
         return scaled ? launch<QFP4_MXFP4, false, true, true>(ma, mb, md, prm, pair_tiles, s)
                       : launch<QFP4_MXFP4, false, true>(ma, mb, md, prm, pair_tiles, s);
-    if (scaled)
-        return fmt == QFP4_NVFP4 ? launch<QFP4_NVFP4, false, false, true>(ma, mb, md, prm, pair_tiles, s)
-                                 : launch<QFP4_MXFP4, false, false, true>(ma, mb, md, prm, pair_tiles, s);
+    if (scaled) {
+        if (fmt == QFP4_NVFP4)
+            return grouped ? launch<QFP4_NVFP4, true, false, true>(ma, mb, md, prm, pair_tiles, s)
+                           : launch<QFP4_NVFP4, false, false, true>(ma, mb, md, prm, pair_tiles, s);
+        return grouped ? launch<QFP4_MXFP4, true, false, true>(ma, mb, md, prm, pair_tiles, s)
+                       : launch<QFP4_MXFP4, false, false, true>(ma, mb, md, prm, pair_tiles, s);
+    }
     if (fmt == QFP4_NVFP4)
         return grouped ? launch<QFP4_NVFP4, true>(ma, mb, md, prm, pair_tiles, s)
                        : launch<QFP4_NVFP4, false>(ma, mb, md, prm, pair_tiles, s);

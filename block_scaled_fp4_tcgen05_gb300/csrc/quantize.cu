@@ -437,7 +437,7 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
             float gs = gs_one, inv_gs = inv_gs_one;
             if (GROUPED && valid) {
                 grp = find_group(s_offs, groups, row);
-                if (FMT == QFP4_NVFP4 && gs_ptr) {
+                if (FMT == QFP4_NVFP4 && gs_ptr && !ROWGS) {
                     gs = gs_ptr[grp];
                     inv_gs = __frcp_rn(gs);
                 }
@@ -893,6 +893,29 @@ extern "C" int qfp4_quantize_grouped(int fmt, const void *X_bf16, int64_t total_
         ? launch_quantize<QFP4_MXFP4, QFP4_SF_MMA, true>(X_bf16, total_rows, K, gs, Q_packed, SF_mma, g, row_offsets, s)
         : launch_quantize<QFP4_NVFP4, QFP4_SF_MMA, true>(X_bf16, total_rows, K, gs, Q_packed, SF_mma, g, row_offsets, s);
     return launch_status(e);
+}
+
+extern "C" int qfp4_quantize_grouped_rows(int fmt, const void *X_bf16, int64_t total_rows, int64_t K,
+                                          int64_t groups, const int32_t *row_offsets, const float *gs_rows,
+                                          void *Q_packed, void *SF_mma, void *stream)
+{
+    if (fmt == QFP4_MXFP4)        // MXFP4 has no global scale: the plain grouped quantiser
+        return qfp4_quantize_grouped(fmt, X_bf16, total_rows, K, groups, row_offsets, nullptr, Q_packed, SF_mma,
+                                     stream);
+    if (fmt != QFP4_NVFP4) return QFP4_ERR_INVALID_ARG;
+    if (total_rows < 0 || K < 0 || groups < 1 || !row_offsets) return QFP4_ERR_INVALID_ARG;
+    if (groups > kMaxGroups || K % 128 != 0) return QFP4_ERR_UNSUPPORTED;
+    if ((total_rows + 128 * (groups + 1)) * (K / 16) >= (int64_t{1} << 32) - 4096) return QFP4_ERR_UNSUPPORTED;
+    if (!gs_rows || !X_bf16 || !Q_packed || !SF_mma) return QFP4_ERR_INVALID_ARG;
+    if (!aligned16(X_bf16) || !aligned16(Q_packed) || !aligned4(SF_mma) || !aligned4(row_offsets) ||
+        !aligned4(gs_rows))
+        return QFP4_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t sf_bytes = qfp4_sf_mma_grouped_bytes(total_rows, groups, K / 16);
+    if (cudaMemsetAsync(SF_mma, 0, sf_bytes, s) != cudaSuccess) return QFP4_ERR_CUDA;
+    if (total_rows == 0 || K == 0) return QFP4_OK;
+    return launch_status(launch_quantize<QFP4_NVFP4, QFP4_SF_MMA, true, true>(
+        X_bf16, total_rows, K, gs_rows, Q_packed, SF_mma, static_cast<int>(groups), row_offsets, s));
 }
 
 extern "C" int qfp4_sf_interleave(const void *SF_in, int64_t rows, int64_t cols, void *SF_out,

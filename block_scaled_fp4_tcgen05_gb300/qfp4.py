@@ -41,6 +41,9 @@ SIGNATURES = {
     "qfp4_quantize_rows": (_i32, [_i32, _vp, _i64, _i64, _vp, _vp, _vp, _i32, _vp]),
     "qfp4_gemm_nt_scaled": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                    _sz, _vp]),
+    "qfp4_quantize_grouped_rows": (_i32, [_i32, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+    "qfp4_gemm_nt_grouped_scaled": (_i32, [_i32, _i64, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
+                                           _vp, _vp, _vp, _vp, _vp, _vp]),
     "qfp4_quantize_grouped": (_i32, [_i32, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "qfp4_sf_interleave": (_i32, [_vp, _i64, _i64, _vp, _i32, _vp]),
     "qfp4_gemm_workspace_bytes": (_sz, [_i32, _i64, _i64, _i64]),
@@ -167,6 +170,15 @@ def quantize_grouped(fmt, X, row_offsets, gs, Q, SF_mma, stream=None) -> None:
                                         _p(SF_mma), _stream(stream)))
 
 
+def quantize_grouped_rows(fmt, X, row_offsets, gs_rows, Q, SF_mma, stream=None) -> None:
+    """Grouped quantiser with one global scale per row (per-group MMA scale layout)."""
+    rows, K = X.shape
+    groups = row_offsets.numel() - 1
+    _check("qfp4_quantize_grouped_rows",
+           load().qfp4_quantize_grouped_rows(fmt, _p(X), rows, K, groups, _p(row_offsets), _p(gs_rows), _p(Q),
+                                             _p(SF_mma), _stream(stream)))
+
+
 def sf_interleave(SF_in, rows, cols, SF_out, layout=SF_MMA, stream=None) -> None:
     _check("qfp4_sf_interleave",
            load().qfp4_sf_interleave(_p(SF_in), rows, cols, _p(SF_out), layout, _stream(stream)))
@@ -196,3 +208,14 @@ def gemm_nt_grouped(fmt, row_offsets, total_rows, max_group_rows, N, K, A, A_sf,
            load().qfp4_gemm_nt_grouped(fmt, groups, _p(row_offsets), total_rows, max_group_rows, N, K,
                                        _p(A), _p(A_sf), _p(B), _p(B_sf), _p(gs_a), _p(gs_b), _p(D),
                                        _stream(stream)))
+
+
+def gemm_nt_grouped_scaled(fmt, row_offsets, total_rows, max_group_rows, N, K, A, A_sf, B, B_sf,
+                           gs_a, gs_b, row_scale, col_scale, D, stream=None) -> None:
+    """Grouped GEMM with the two-level epilogue: row m times row_scale[m],
+    column n of group e times col_scale[e*N + n] (either may be None)."""
+    groups = row_offsets.numel() - 1
+    _check("qfp4_gemm_nt_grouped_scaled",
+           load().qfp4_gemm_nt_grouped_scaled(fmt, groups, _p(row_offsets), total_rows, max_group_rows, N, K,
+                                              _p(A), _p(A_sf), _p(B), _p(B_sf), _p(gs_a), _p(gs_b),
+                                              _p(row_scale), _p(col_scale), _p(D), _stream(stream)))

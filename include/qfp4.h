@@ -164,6 +164,16 @@ int qfp4_quantize_grouped(int fmt, const void *X_bf16, int64_t total_rows, int64
                           int64_t groups, const int32_t *row_offsets, const float *gs,
                           void *Q_packed, void *SF_mma, void *stream);
 
+/* Grouped quantiser with one global scale per row (two-level NVFP4 for MoE
+ * batches): row m is quantised exactly as qfp4_quantize quantises it alone
+ * with gs_rows[m], and the scales go to the per-group MMA layout of
+ * qfp4_quantize_grouped.  gs_rows is a DEVICE fp32 [total_rows] (NVFP4;
+ * MXFP4 ignores it and runs qfp4_quantize_grouped).  Other arguments and
+ * requirements as qfp4_quantize_grouped. */
+int qfp4_quantize_grouped_rows(int fmt, const void *X_bf16, int64_t total_rows, int64_t K,
+                               int64_t groups, const int32_t *row_offsets, const float *gs_rows,
+                               void *Q_packed, void *SF_mma, void *stream);
+
 /* ---------------------------------------------------------------------- */
 /* Scale-factor interleave                                                  */
 /* ---------------------------------------------------------------------- */
@@ -251,6 +261,21 @@ int qfp4_gemm_nt_grouped(int fmt, int64_t groups, const int32_t *row_offsets,
                          const void *B_packed, const void *B_sf,
                          const float *gs_a, const float *gs_b,
                          void *D_bf16, void *stream);
+
+/* Grouped GEMM with the two-level epilogue of qfp4_gemm_nt_scaled:
+ *   D[m,n] = bf16_rne( (acc[m,n] * (gs_a[e]*gs_b[e] * row_scale[m])) * col_scale[e*N + n] )
+ * for row m of group e.  row_scale is a DEVICE fp32 [total_rows] (e.g. per-row
+ * global scales of the concatenated activations) or NULL; col_scale is a
+ * DEVICE fp32 [groups * N] (each expert's per-row weight scales) or NULL.
+ * With both NULL the result is bit-identical to qfp4_gemm_nt_grouped.  Other
+ * arguments and requirements as qfp4_gemm_nt_grouped. */
+int qfp4_gemm_nt_grouped_scaled(int fmt, int64_t groups, const int32_t *row_offsets,
+                                int64_t total_rows, int64_t max_group_rows, int64_t N, int64_t K,
+                                const void *A_packed, const void *A_sf,
+                                const void *B_packed, const void *B_sf,
+                                const float *gs_a, const float *gs_b,
+                                const float *row_scale, const float *col_scale,
+                                void *D_bf16, void *stream);
 
 #ifdef __cplusplus
 }

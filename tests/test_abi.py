@@ -138,3 +138,16 @@ def test_two_level_entry_points_reject_bad_arguments(lib):
     assert call(2, 100) == -2                                                    # N % 128
     assert call(10, FAKE + 2) == -3                                              # row_scale alignment
     assert call(11, FAKE + 2) == -3                                              # col_scale alignment
+
+
+def test_grouped_two_level_entry_points_reject_bad_arguments(lib):
+    q = lib.qfp4_quantize_grouped_rows
+    assert q(2, FAKE, 10, 256, 2, FAKE, FAKE, FAKE, FAKE, None) == -1          # format
+    assert q(1, FAKE, 10, 256, 0, FAKE, FAKE, FAKE, FAKE, None) == -1          # groups
+    assert q(1, FAKE, 10, 200, 2, FAKE, FAKE, FAKE, FAKE, None) == -2          # K % 128
+    assert q(1, FAKE, 10, 256, 2, FAKE, None, FAKE, FAKE, None) == -1          # NVFP4 needs gs_rows
+    assert q(1, FAKE, 10, 256, 2, FAKE, FAKE + 2, FAKE, FAKE, None) == -3
+    g = lib.qfp4_gemm_nt_grouped_scaled
+    assert g(1, 0, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE, None, None, None, None, FAKE, None) == -1
+    assert g(1, 2, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE, None, None, FAKE + 2, None, FAKE, None) == -3
+    assert g(1, 2, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE + 2, FAKE, None) == -3

@@ -169,3 +169,68 @@ def test_two_level_nvfp4_pipeline_4096():
     ni = np.concatenate([gen.integers(0, N, 20000), np.tile(np.arange(N), len(rows))])
     d_ref, t_ref = oracle.gemm_nt_entries(NV, qa, sfa, qb, sfb, 1.0, 1.0, mi, ni, gsa_ref, gsb_ref)
     assert_gemm_close(bf16_to_f64(D)[mi, ni], d_ref, t_ref, "two-level 4096^3 sampled")
+
+
+# ----------------------------------------------------------------- grouped (MoE) two-level
+
+@pytest.mark.parametrize("N", [256, 384])
+def test_grouped_two_level_nvfp4(N):
+    """Per-row global scales of the concatenated activations and of each
+    expert's weight rows, grouped per-row quantisation (bit-exact, per-group
+    scale layout), then the grouped GEMM with row and column rescales against
+    the oracle per expert.  N = 256 runs CTA pairs, N = 384 single CTAs."""
+    counts = np.array([300, 17, 0, 140, 256])
+    E, K, g = len(counts), 512, 16
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows = int(offs[-1])
+    xa = synth.activations_bf16(8000 + N, rows, K)
+    xw = synth.weights_bf16(8001 + N, E * N, K)
+    d_offs = torch.from_numpy(offs).cuda()
+    w_offs = torch.arange(0, (E + 1) * N, N, dtype=torch.int32, device="cuda")
+    out = []
+    for x, o, nrow in ((xa, d_offs, rows), (xw, w_offs, E * N)):
+        X = to_dev_bf16(x)
+        gs = torch.empty(nrow, dtype=torch.float32, device="cuda")
+        qfp4.global_scale_rows(X, gs)
+        Q = torch.empty((nrow, K // 2), dtype=torch.uint8, device="cuda")
+        SF = torch.full((qfp4.sf_mma_grouped_bytes(nrow, E, K // g),), 0xEE, dtype=torch.uint8, device="cuda")
+        qfp4.quantize_grouped_rows(NV, X, o, gs, Q, SF)
+        torch.cuda.synchronize()
+        out.append((Q, SF, gs, to_host(Q), to_host(SF), to_host(gs)))
+    (Qa, SFa, gsa, qa_h, sfa_h, gsa_h), (Qb, SFb, gsb, qb_h, sfb_h, gsb_h) = out
+    assert np.array_equal(gsa_h, oracle.global_scale_rows(xa))
+    assert np.array_equal(gsb_h, oracle.global_scale_rows(xw))
+    # quantised bytes and the per-group scale layout
+    kc = K // g // 4
+    for x, q_h, sf_h, gs_h, seg in ((xa, qa_h, sfa_h, gsa_h, offs), (xw, qb_h, sfb_h, gsb_h, np.arange(0, (E + 1) * N, N))):
+        tile = 0
+        for e in range(E):
+            lo, hi = int(seg[e]), int(seg[e + 1])
+            if hi == lo:
+                continue
+            q_ref, sf_ref = oracle.quantize(NV, x[lo:hi], gs_h[lo:hi])
+            assert np.array_equal(q_h[lo:hi], q_ref), e
+            ref_mma = oracle.sf_to_mma(sf_ref)
+            assert np.array_equal(sf_h[tile * kc * 512:tile * kc * 512 + ref_mma.size], ref_mma), e
+            tile += -(-(hi - lo) // 128)
+    D = torch.empty((rows, N), dtype=torch.bfloat16, device="cuda")
+    qfp4.gemm_nt_grouped_scaled(NV, d_offs, rows, int(counts.max()), N, K, Qa, SFa, Qb, SFb, None, None, gsa, gsb, D)
+    D0 = torch.empty((rows, N), dtype=torch.bfloat16, device="cuda")
+    D1 = torch.empty((rows, N), dtype=torch.bfloat16, device="cuda")
+    qfp4.gemm_nt_grouped_scaled(NV, d_offs, rows, int(counts.max()), N, K, Qa, SFa, Qb, SFb, None, None,
+                                None, None, D0)
+    qfp4.gemm_nt_grouped(NV, d_offs, rows, int(counts.max()), N, K, Qa, SFa, Qb, SFb, None, None, D1)
+    torch.cuda.synchronize()
+    assert qfp4.poll_device_status() == 0
+    assert torch.equal(D0.view(torch.int16), D1.view(torch.int16))      # no scales: the plain grouped GEMM
+    Dh = bf16_to_f64(D)
+    for e in range(E):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        if hi == lo:
+            continue
+        sfa_e = oracle.sf_from_mma(np.ascontiguousarray(sfa_h[sum(-(-int(c) // 128) for c in counts[:e]) * kc * 512:]),
+                                   hi - lo, K // g)
+        sfb_e = oracle.sf_from_mma(np.ascontiguousarray(sfb_h[e * (N // 128) * kc * 512:]), N, K // g)
+        d_ref, t_ref = oracle.gemm_nt(NV, qa_h[lo:hi], sfa_e, qb_h[e * N:(e + 1) * N], sfb_e, 1.0, 1.0,
+                                      gsa_h[lo:hi], gsb_h[e * N:(e + 1) * N])
+        assert_gemm_close(Dh[lo:hi], d_ref, t_ref, f"expert {e}")

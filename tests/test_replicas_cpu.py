@@ -3,9 +3,14 @@ so N ranks run independent replicas and only the timing is reduced (max over
 ranks).  Two gloo ranks on 127.0.0.1 stand in for the GPUs."""
 import os
 import socket
+import subprocess
+import sys
 
 import pytest
 import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+BENCH = os.path.join(ROOT, "bench.py")
 
 
 def _free_port():
@@ -47,3 +52,24 @@ def test_two_rank_max_reduction():
 def test_single_process_reduce_is_identity():
     import bench
     assert bench.reduce_max(3.25, 1, None) == 3.25
+
+
+def test_reference_arm_json_line():
+    """bench.py --impl reference runs the oracle on the host and prints one
+    JSON line with the contract's keys (no GPU needed)."""
+    import json
+    r = subprocess.run([sys.executable, BENCH, "--impl", "reference", "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["value"] > 0 and d["warmup"] >= 3
+    assert d["config"]["workload"] == "nvfp4_gemm_nt_4096x4096x4096"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    assert d["e2e"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0

@@ -27,18 +27,30 @@ _lock = threading.Lock()
 _lib = None
 
 
+def _paths():
+    """Source and library to use.  QFP4_ORACLE_SOURCE names a modified copy
+    of oracle.c (the pin suite's planted-mistake check builds one per
+    mistake); its library is built beside it, never over the real one."""
+    src = os.environ.get("QFP4_ORACLE_SOURCE")
+    if src:
+        src = os.path.abspath(src)
+        return src, os.path.join(os.path.dirname(src), "liboracle.so")
+    return _SRC, _LIB_PATH
+
+
 def build(force: bool = False) -> str:
     """Compile oracle.c into a shared library (gcc, OpenMP, strict IEEE fp32)."""
-    os.makedirs(_BUILD, exist_ok=True)
-    stale = (not os.path.exists(_LIB_PATH)
-             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    src, lib_path = _paths()
+    os.makedirs(os.path.dirname(lib_path), exist_ok=True)
+    stale = (not os.path.exists(lib_path)
+             or os.path.getmtime(lib_path) < os.path.getmtime(src))
     if force or stale:
-        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        tmp = lib_path + f".{os.getpid()}.tmp"
         cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
-               "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+               "-shared", "-fPIC", "-o", tmp, src, "-lm"]
         subprocess.run(cmd, check=True)
-        os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 def _load():
@@ -189,6 +201,7 @@ def dequantize(fmt: int, Q: np.ndarray, SF: np.ndarray, gs: float = 1.0) -> np.n
     SF = np.ascontiguousarray(SF, dtype=np.uint8)
     M = Q.shape[0]
     K = Q.shape[1] * 2
+    _check_sf(fmt, SF, M, K)
     X = np.zeros((M, K), dtype=np.float64)
     if lib.oracle_dequantize(fmt, _ptr(Q), _ptr(SF), M, K, float(np.float32(gs)), _ptr(X)) != 0:
         raise ValueError("bad shape")
@@ -225,6 +238,13 @@ def _opt_f32(v, n):
     return a, _ptr(a)
 
 
+def _check_sf(fmt: int, sf: np.ndarray, rows: int, K: int):
+    """Scale factors must be row-major [rows, K/g] for the format's block g."""
+    g = block_size(fmt)
+    if K % g != 0 or sf.size != rows * (K // g):
+        raise ValueError(f"scale factors: {sf.size} bytes for [{rows}, {K}/{g}]")
+
+
 def gemm_nt(fmt: int, A: np.ndarray, A_sf: np.ndarray, B: np.ndarray, B_sf: np.ndarray,
             gs_a: float = 1.0, gs_b: float = 1.0, row_scale=None, col_scale=None):
     """Full reference GEMM. Returns (D fp64 [M,N], T fp64 [M,N]); SF row-major.
@@ -233,6 +253,8 @@ def gemm_nt(fmt: int, A: np.ndarray, A_sf: np.ndarray, B: np.ndarray, B_sf: np.n
     lib = _load()
     A, A_sf, B, B_sf = (np.ascontiguousarray(v, dtype=np.uint8) for v in (A, A_sf, B, B_sf))
     M, N, K = A.shape[0], B.shape[0], A.shape[1] * 2
+    _check_sf(fmt, A_sf, M, K)
+    _check_sf(fmt, B_sf, N, K)
     D = np.zeros((M, N), dtype=np.float64)
     T = np.zeros((M, N), dtype=np.float64)
     if row_scale is not None or col_scale is not None:
@@ -256,8 +278,13 @@ def gemm_nt_entries(fmt: int, A, A_sf, B, B_sf, gs_a, gs_b, mi, ni, row_scale=No
     lib = _load()
     A, A_sf, B, B_sf = (np.ascontiguousarray(v, dtype=np.uint8) for v in (A, A_sf, B, B_sf))
     K = A.shape[1] * 2
+    _check_sf(fmt, A_sf, A.shape[0], K)
+    _check_sf(fmt, B_sf, B.shape[0], K)
     mi = np.ascontiguousarray(mi, dtype=np.int64)
     ni = np.ascontiguousarray(ni, dtype=np.int64)
+    if mi.size != ni.size or (mi.size and (mi.min() < 0 or mi.max() >= A.shape[0]
+                                           or ni.min() < 0 or ni.max() >= B.shape[0])):
+        raise ValueError("sampled positions out of range")
     D = np.zeros(mi.size, dtype=np.float64)
     T = np.zeros(mi.size, dtype=np.float64)
     if row_scale is not None or col_scale is not None:

@@ -1,0 +1,112 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case below plants one mistake in a copy of oracle.c, the kind that a
+careful reading could still let through: a dropped term, a wrong sign, bias or
+index, a transposed operand, a swapped nibble or layout order, a different tie
+rule.  The copy is built on its own (QFP4_ORACLE_SOURCE names it), and the
+CPU pin suite run against it must fail.  A control case builds the unmodified
+source the same way and must pass, so a failure is due to the planted mistake
+and not to the harness.  Only the CPU is used; the real oracle library is not
+touched.
+"""
+import os
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+PINS = os.path.join(ROOT, "tests", "test_oracle_pins.py")
+
+# (name, text in oracle.c, replacement): every occurrence is replaced.
+# Left out as equivalent (the result does not change): swapping the nibble
+# order of A and B together in the GEMM, since elements k and k^1 always share
+# a scale block and the sum pairs them the same way.
+MUTANTS = [
+    # rounding to the formats
+    ("tie_to_odd_code", "return (lo & 1) ? hi : lo;", "return (lo & 1) ? lo : hi;"),
+    ("tie_always_up", "return (lo & 1) ? hi : lo;", "return hi;"),
+    ("round_toward_zero", "if (dlo < dhi) return lo;", "return lo;"),
+    ("e2m1_sign_dropped", "return signbit(q) ? (mag | 8) : mag;", "return mag;"),
+    # decoding
+    ("e2m1_subnormal_step", "(e == 0) ? 0.5 * m :", "(e == 0) ? 1.0 * m :"),
+    ("e2m1_exponent_bias", "ldexp(1.0, e - 1)", "ldexp(1.0, e - 2)"),
+    ("ue8m0_exponent_bias", "ldexp(1.0, byte - 127)", "ldexp(1.0, byte - 128)"),
+    ("ue4m3_exponent_bias", "(1.0 + m / 8.0) * ldexp(1.0, e - 7)", "(1.0 + m / 8.0) * ldexp(1.0, e - 8)"),
+    ("ue4m3_subnormal_step", "ldexp((double)m, -9)", "ldexp((double)m, -10)"),
+    ("block_sizes_swapped", "return fmt == ORACLE_MXFP4 ? 32 : 16;", "return fmt == ORACLE_MXFP4 ? 16 : 32;"),
+    ("scale_types_swapped",
+     "fmt == ORACLE_MXFP4 ? oracle_ue8m0_value(byte) : oracle_ue4m3_value(byte)",
+     "fmt == ORACLE_MXFP4 ? oracle_ue4m3_value(byte) : oracle_ue8m0_value(byte)"),
+    # quantiser
+    ("global_scale_without_448", "return amax / 2688.0f;", "return amax / 6.0f;"),
+    ("block_amax_signed",
+     "if (isnan(x[i]) || isinf(x[i])) return -1;\n        float a = fabsf(x[i]);",
+     "if (isnan(x[i]) || isinf(x[i])) return -1;\n        float a = x[i];"),
+    ("scale_target_times_gs", "float t = (amax / 6.0f) / gs;", "float t = (amax / 6.0f) * gs;"),
+    ("scale_target_without_6", "float t = (amax / 6.0f) / gs;", "float t = amax / gs;"),
+    ("element_scale_without_gs", "float s = (float)oracle_scale_value(fmt, code) * gs;",
+     "float s = (float)oracle_scale_value(fmt, code);"),
+    ("quantise_packs_high_nibble_first", "(uint8_t)(nib[i] | (nib[i + 1] << 4))",
+     "(uint8_t)((nib[i] << 4) | nib[i + 1])"),
+    ("per_row_scale_from_first_row", "oracle_global_scale_bf16(X + m * K, K)", "oracle_global_scale_bf16(X, K)"),
+    ("dequantise_high_nibble_first", "int code = (k & 1) ? (byte >> 4) : (byte & 15);",
+     "int code = (k & 1) ? (byte & 15) : (byte >> 4);"),
+    # scale-factor layout
+    ("sf_row_split_swapped", "(rr % 32) * 16 + (rr / 32) * 4", "(rr / 32) * 16 + (rr % 32) * 4"),
+    ("sf_tiles_column_major", "int64_t tile = (r / 128) * ctiles + c / 4;",
+     "int64_t tile = (c / 4) * ((rows + 127) / 128) + r / 128;"),
+    # GEMM
+    ("gemm_b_nibble_order_only", "int cb = (k & 1) ? (bb >> 4) : (bb & 15);",
+     "int cb = (k & 1) ? (bb & 15) : (bb >> 4);"),
+    ("gemm_b_scale_blocks_reversed", "Bsf[n * kg + k / g]", "Bsf[n * kg + (K - 1 - k) / g]"),
+    ("gemm_b_elements_reversed", "int bb = B[n * (K / 2) + k / 2];", "int bb = B[n * (K / 2) + (K - 1 - k) / 2];"),
+    ("gemm_a_scale_block_of_16", "Asf[m * kg + k / g]", "Asf[m * kg + k / 16]"),
+    ("gemm_drops_global_scale", "*d_out = gsab * acc;", "*d_out = acc;"),
+    ("gemm_global_scale_of_a_twice", "(double)gs_a * (double)gs_b", "(double)gs_a * (double)gs_a"),
+    ("gemm_accumulates_in_fp32", "double acc = 0.0, tacc = 0.0;", "float acc = 0.0f; double tacc = 0.0;"),
+    ("rescale_row_twice", "(cs ? (double)cs[n] : 1.0)", "(rs ? (double)rs[m] : 1.0)"),
+    ("rescale_drops_column", "(cs ? (double)cs[n] : 1.0)", "1.0"),
+]
+
+
+def _run(workdir, text):
+    """Build the given oracle source in workdir and run the pin suite on it.
+    Returns (build returncode, pin-suite returncode, pin-suite output)."""
+    os.makedirs(workdir, exist_ok=True)
+    src = os.path.join(workdir, "oracle.c")
+    with open(src, "w") as f:
+        f.write(text)
+    env = dict(os.environ, QFP4_ORACLE_SOURCE=src, OMP_NUM_THREADS="2")
+    b = subprocess.run([sys.executable, "-c", "import oracle; print(oracle.build(force=True))"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    if b.returncode != 0 or os.path.dirname(b.stdout.strip()) != workdir:
+        return b.returncode or -1, None, b.stderr[-2000:]
+    r = subprocess.run([sys.executable, "-m", "pytest", PINS, "-x", "-q", "-p", "no:cacheprovider"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    return 0, r.returncode, r.stdout[-2000:]
+
+
+def test_unmodified_copy_passes(tmp_path):
+    with open(SRC) as f:
+        brc, rc, out = _run(str(tmp_path), f.read())
+    assert brc == 0, out
+    assert rc == 0, out
+
+
+def test_planted_mistakes_are_caught(tmp_path):
+    with open(SRC) as f:
+        text = f.read()
+    for name, old, new in MUTANTS:
+        assert old in text, f"{name}: text to mutate not found in oracle.c"
+    jobs = {name: (str(tmp_path / name), text.replace(old, new)) for name, old, new in MUTANTS}
+    workers = max(1, min(8, (os.cpu_count() or 2) // 2))
+    with ThreadPoolExecutor(workers) as pool:
+        results = dict(zip(jobs, pool.map(lambda j: _run(*j), jobs.values())))
+    not_built = {n: r[2] for n, r in results.items() if r[0] != 0}
+    assert not not_built, f"mutants that did not build: {not_built}"
+    # pytest exit code 1 = some pin failed; 0 = survived; anything else (a
+    # usage error or a crash) does not count as caught
+    survived = {n: r[2] for n, r in results.items() if r[1] != 1}
+    assert not survived, "mistakes the pins let through:\n" + "\n".join(
+        f"{n}:\n{out}" for n, out in survived.items())

@@ -49,6 +49,9 @@ MUTANTS = [
      "float s = (float)oracle_scale_value(fmt, code);"),
     ("quantise_packs_high_nibble_first", "(uint8_t)(nib[i] | (nib[i + 1] << 4))",
      "(uint8_t)((nib[i] << 4) | nib[i + 1])"),
+    ("mxfp4_quantise_takes_gs", "if (fmt == ORACLE_MXFP4) gs = 1.0f;", ""),
+    ("mxfp4_dequantise_takes_gs", "double gsd = fmt == ORACLE_MXFP4 ? 1.0 : (double)gs;", "double gsd = (double)gs;"),
+    ("dequantise_without_gs", "double gsd = fmt == ORACLE_MXFP4 ? 1.0 : (double)gs;", "double gsd = 1.0;"),
     ("per_row_scale_from_first_row", "oracle_global_scale_bf16(X + m * K, K)", "oracle_global_scale_bf16(X, K)"),
     ("dequantise_high_nibble_first", "int code = (k & 1) ? (byte >> 4) : (byte & 15);",
      "int code = (k & 1) ? (byte & 15) : (byte >> 4);"),
@@ -63,6 +66,8 @@ MUTANTS = [
     ("gemm_b_elements_reversed", "int bb = B[n * (K / 2) + k / 2];", "int bb = B[n * (K / 2) + (K - 1 - k) / 2];"),
     ("gemm_a_scale_block_of_16", "Asf[m * kg + k / g]", "Asf[m * kg + k / 16]"),
     ("gemm_drops_global_scale", "*d_out = gsab * acc;", "*d_out = acc;"),
+    ("mxfp4_gemm_takes_gs", "double gsab = fmt == ORACLE_MXFP4 ? 1.0 : (double)gs_a * (double)gs_b;",
+     "double gsab = (double)gs_a * (double)gs_b;"),
     ("gemm_global_scale_of_a_twice", "(double)gs_a * (double)gs_b", "(double)gs_a * (double)gs_a"),
     ("gemm_accumulates_in_fp32", "double acc = 0.0, tacc = 0.0;", "float acc = 0.0f; double tacc = 0.0;"),
     ("rescale_row_twice", "(cs ? (double)cs[n] : 1.0)", "(rs ? (double)rs[m] : 1.0)"),

@@ -261,6 +261,25 @@ def test_quantize_element_error_property():
                     assert abs(abs(q) - v) <= np.min(np.abs(abs(q) - GRID)) + 0.0
 
 
+def test_mxfp4_has_no_global_scale():
+    """MXFP4 carries only its UE8M0 block scales (DeepGEMM PR, "Summary");
+    a global scale handed to it is ignored by the quantiser, the dequantiser
+    and the GEMM alike."""
+    xb = synth.activations_bf16(17, 8, 256)
+    Q1, SF1 = oracle.quantize(MX, xb, 1.0)
+    Q2, SF2 = oracle.quantize(MX, xb, 0.37)
+    assert np.array_equal(Q1, Q2) and np.array_equal(SF1, SF2)
+    assert np.array_equal(oracle.dequantize(MX, Q1, SF1, 0.37), oracle.dequantize(MX, Q1, SF1, 1.0))
+    Qw, SFw = oracle.quantize(MX, synth.weights_bf16(18, 4, 256))
+    d1, t1 = oracle.gemm_nt(MX, Q1, SF1, Qw, SFw, 1.0, 1.0)
+    d2, t2 = oracle.gemm_nt(MX, Q1, SF1, Qw, SFw, 0.37, 3.0)
+    assert np.array_equal(d1, d2) and np.array_equal(t1, t2)
+    mi, ni = np.array([0, 7, 3]), np.array([1, 0, 3])
+    e1, _ = oracle.gemm_nt_entries(MX, Q1, SF1, Qw, SFw, 1.0, 1.0, mi, ni)
+    e2, _ = oracle.gemm_nt_entries(MX, Q1, SF1, Qw, SFw, 0.37, 3.0, mi, ni)
+    assert np.array_equal(e1, e2) and np.array_equal(e1, d1[mi, ni])
+
+
 def test_global_scale_puts_largest_block_at_448():
     xb = synth.activations_bf16(5, 64, 512)
     gs = oracle.global_scale(xb)

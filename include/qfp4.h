@@ -14,8 +14,9 @@
  *     BF16 -> NVFP4/MXFP4 quantisation with per-block scale factors, the
  *     re-interleave of rank-2 scale factors into the 5D TCGEN layout, and the
  *     grouped per-expert quantiser and matmul.
- *   "quadbit" README, "End-to-end serving": the split-K decode kernel that
- *     fills the GPU at small M, and the one-launch segmented MoE kernel.
+ *   "quadbit" README, "End-to-end serving": the decode GEMM at small M (the
+ *     page fills the GPU with split-K; this library needs none, see
+ *     qfp4_gemm_nt) and the one-launch segmented MoE kernel.
  *
  * Conventions for every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller; the library
@@ -110,7 +111,8 @@ int qfp4_global_scale(const void *X_bf16, int64_t rows, int64_t cols, float *gs_
 /* Per-group version: group e covers rows [row_offsets[e], row_offsets[e+1])
  * of X (row_offsets is a DEVICE int32 array of groups+1 non-decreasing
  * entries, row_offsets[0] = 0, row_offsets[groups] = total_rows).
- * gs_out[e] = amax over group e / (6 * 448).  Same requirements. */
+ * gs_out[e] = amax over group e / (6 * 448).  Same requirements, and
+ * 1 <= groups <= 256. */
 int qfp4_global_scale_grouped(const void *X_bf16, int64_t total_rows, int64_t cols,
                               int64_t groups, const int32_t *row_offsets, float *gs_out,
                               void *stream);
@@ -141,7 +143,9 @@ int qfp4_global_scale_rows(const void *X_bf16, int64_t rows, int64_t cols, float
  *   sf_layout  QFP4_SF_ROWMAJOR: SF is [M, K/g] row-major;
  *              QFP4_SF_MMA: SF is written directly in the MMA layout
  *              (buffer of qfp4_sf_mma_bytes(M, K/g) bytes, padding zeroed).
- * Requirements: M >= 0, K % 128 == 0, X/Q 16-byte aligned, SF 4-byte aligned. */
+ * Requirements: M >= 0, K % 128 == 0, X/Q 16-byte aligned, SF 4-byte aligned,
+ * and (M + 128) * (K / 16) < 2^32 - 4096 (block indices and scale-byte offsets
+ * are 32-bit: up to about 2^36 elements); QFP4_ERR_UNSUPPORTED otherwise. */
 int qfp4_quantize(int fmt, const void *X_bf16, int64_t M, int64_t K, const float *gs,
                   void *Q_packed, void *SF, int sf_layout, void *stream);
 
@@ -159,7 +163,9 @@ int qfp4_quantize_rows(int fmt, const void *X_bf16, int64_t M, int64_t K, const 
  * 128-row tile sum_{e' < e} ceil(rows_e' / 128).  Q is [total_rows, K/2].
  * row_offsets as in qfp4_global_scale_grouped.  SF_mma must hold
  * qfp4_sf_mma_grouped_bytes(total_rows, groups, K/g) bytes; it is zeroed
- * by this call before the scale bytes are written. */
+ * by this call before the scale bytes are written.  Requirements as
+ * qfp4_quantize, with 1 <= groups <= 256 and
+ * (total_rows + 128 * (groups + 1)) * (K / 16) < 2^32 - 4096. */
 int qfp4_quantize_grouped(int fmt, const void *X_bf16, int64_t total_rows, int64_t K,
                           int64_t groups, const int32_t *row_offsets, const float *gs,
                           void *Q_packed, void *SF_mma, void *stream);
@@ -254,7 +260,8 @@ int qfp4_gemm_nt_scaled(int fmt, int64_t M, int64_t N, int64_t K,
  *   row_offsets DEVICE int32 [groups + 1]; max_group_rows is an upper bound
  *              on any group's rows (sizes the launch; rows beyond it are an
  *              error recorded in the device status word).
- * Requirements as qfp4_gemm_nt; no workspace is needed. */
+ * Requirements as qfp4_gemm_nt, with 1 <= groups <= 256; no workspace is
+ * needed. */
 int qfp4_gemm_nt_grouped(int fmt, int64_t groups, const int32_t *row_offsets,
                          int64_t total_rows, int64_t max_group_rows, int64_t N, int64_t K,
                          const void *A_packed, const void *A_sf,

@@ -69,6 +69,9 @@ def test_quantize_rejects_bad_arguments(lib):
     assert call(Q=FAKE + 4) == -3
     assert call(SF=FAKE + 2) == -3
     assert call(M=0) == 0                       # empty: nothing to do, nothing launched
+    # (M + 128) * (K / 16) must stay below 2^32 - 4096 (32-bit block indices)
+    assert call(M=(1 << 32) // 16 - 128 - 256, K=256) == -2
+    assert call(M=(1 << 32) // 16 - 128 - 257, K=256, X=None) == -1   # just inside: reaches the pointer checks
 
 
 def test_gemm_rejects_bad_arguments(lib):
@@ -98,6 +101,10 @@ def test_grouped_and_interleave_reject_bad_arguments(lib):
     assert lib.qfp4_gemm_nt_grouped(1, 300, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE,
                                     None, None, FAKE, None) == -2
     assert lib.qfp4_quantize_grouped(1, FAKE, 10, 256, 2, FAKE, None, FAKE, FAKE, None) == -1
+    assert lib.qfp4_quantize_grouped(1, FAKE, 10, 256, 257, FAKE, FAKE, FAKE, FAKE, None) == -2
+    assert lib.qfp4_gemm_nt_grouped(1, 257, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE,
+                                    None, None, FAKE, None) == -2
+    assert lib.qfp4_global_scale_grouped(FAKE, 10, 16, 257, FAKE, FAKE, None) == -2
     assert lib.qfp4_sf_interleave(FAKE, 10, 10, FAKE, 7, None) == -1
     assert lib.qfp4_sf_interleave(FAKE, 10, 10, FAKE + 1, 1, None) == -3
     assert lib.qfp4_sf_interleave(FAKE, 0, 10, FAKE, 1, None) == 0

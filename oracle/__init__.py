@@ -89,6 +89,9 @@ def _load():
                                               c_f, c_f, c_p, c_p, c_p, c_p]),
             "oracle_gemm_nt_scaled_entries": (c_int, [c_int, c_i64, c_p, c_p, c_p, c_p, c_f, c_f, c_p, c_p,
                                                       c_i64, c_p, c_p, c_p, c_p]),
+            "oracle_swiglu_f64": (c_int, [c_p, c_p, c_i64, c_p]),
+            "oracle_e2m1_round_n": (c_int, [c_p, c_i64, c_p]),
+            "oracle_scale_round_n": (c_int, [c_int, c_p, c_i64, c_p]),
             "oracle_num_threads": (c_int, []),
         }
         for name, (res, args) in sigs.items():
@@ -302,6 +305,119 @@ def gemm_nt_entries(fmt: int, A, A_sf, B, B_sf, gs_a, gs_b, mi, ni, row_scale=No
     if rc != 0:
         raise ValueError("bad shape")
     return D, T
+
+
+# ---- SwiGLU of the MoE up-projection, and its requantisation ------------------
+
+def swiglu(G: np.ndarray, U: np.ndarray) -> np.ndarray:
+    """H = silu(G) * U = G * U / (1 + exp(-G)), elementwise in fp64."""
+    lib = _load()
+    G = np.ascontiguousarray(G, dtype=np.float64)
+    U = np.ascontiguousarray(U, dtype=np.float64)
+    if G.shape != U.shape:
+        raise ValueError("gate and up outputs differ in shape")
+    H = np.zeros(G.shape, dtype=np.float64)
+    if lib.oracle_swiglu_f64(_ptr(G), _ptr(U), G.size, _ptr(H)) != 0:
+        raise ValueError("bad size")
+    return H
+
+
+def swiglu_up(fmt: int, A, A_sf, Wg, Wg_sf, Wu, Wu_sf, gs_a: float = 1.0, gs_w: float = 1.0):
+    """Exact output of an up-projection with SwiGLU: tokens A [M, K/2], gate
+    and up weight rows Wg, Wu [I, K/2], all with row-major scale factors.
+        G = gemm_nt(A, Wg),  U = gemm_nt(A, Wu)   (exact sums, times gs_a gs_w)
+        H = silu(G) * U
+    Returns (H, G, U, TG, TU), fp64 [M, I]; TG and TU are the scaled sums of
+    |a_k w_k| in which the GEMM's accumulation error is bounded."""
+    G, TG = gemm_nt(fmt, A, A_sf, Wg, Wg_sf, gs_a, gs_w)
+    U, TU = gemm_nt(fmt, A, A_sf, Wu, Wu_sf, gs_a, gs_w)
+    return swiglu(G, U), G, U, TG, TU
+
+
+def swiglu_requantize(fmt: int, H: np.ndarray, gs2: float = 1.0):
+    """The requantised SwiGLU output: H rounded to fp32, then the quantiser's
+    rule with the next layer's activation global scale gs2 (NVFP4; MXFP4 has
+    none).  Returns (Q [M, I/2], SF row-major [M, I/g])."""
+    return quantize(fmt, np.asarray(H, dtype=np.float64).astype(np.float32), gs2)
+
+
+def _e2m1_round_n(q: np.ndarray) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    out = np.zeros(q.shape, dtype=np.uint8)
+    _load().oracle_e2m1_round_n(_ptr(q), q.size, _ptr(out))
+    return out
+
+
+def _scale_round_n(fmt: int, t: np.ndarray) -> np.ndarray:
+    t = np.ascontiguousarray(t, dtype=np.float32)
+    out = np.zeros(t.shape, dtype=np.uint8)
+    _load().oracle_scale_round_n(fmt, _ptr(t), t.size, _ptr(out))
+    return out
+
+
+def _f32_down(x: np.ndarray) -> np.ndarray:
+    """Largest fp32 value <= x (elementwise, x fp64)."""
+    y = x.astype(np.float32)
+    return np.where(y.astype(np.float64) > x, np.nextafter(y, np.float32(-np.inf)), y)
+
+
+def _f32_up(x: np.ndarray) -> np.ndarray:
+    """Smallest fp32 value >= x."""
+    y = x.astype(np.float32)
+    return np.where(y.astype(np.float64) < x, np.nextafter(y, np.float32(np.inf)), y)
+
+
+def requant_valid(fmt: int, Q: np.ndarray, SF: np.ndarray, H: np.ndarray, delta: np.ndarray,
+                  gs2: float = 1.0) -> np.ndarray:
+    """Which blocks of a quantised matrix are what the quantiser's rule gives
+    for SOME fp32 matrix within delta of H (elementwise)?
+
+    Where the value being quantised comes out of an fp32 accumulation, only H
+    (exact) and a bound delta on the distance are known; any fp32 value in
+    [H - delta, H + delta] is then a correct input.  The rule is monotone in
+    every step, so a block passes when
+      - its scale byte lies between the codes the rule gives for the smallest
+        and the largest block amax that the box allows, and
+      - with the scale s that byte decodes to, each element's code lies
+        between the codes of the smallest and the largest value of its own
+        range divided by s (codes ordered along the real line, -0 just
+        below +0); if s is 0 every code must be 0.
+    Q [M, I/2] packed, SF row-major [M, I/g], H and delta fp64 [M, I],
+    gs2 > 0 (NVFP4; ignored for MXFP4).  Returns a bool mask [M, I/g]."""
+    g = block_size(fmt)
+    H = np.asarray(H, dtype=np.float64)
+    delta = np.asarray(delta, dtype=np.float64)
+    M, I = H.shape
+    if I % g or Q.shape != (M, I // 2) or SF.shape != (M, I // g) or delta.shape != H.shape:
+        raise ValueError("shapes")
+    if np.any(delta < 0) or not np.all(np.isfinite(H)):
+        raise ValueError("delta must be >= 0 and H finite")
+    gs = np.float32(1.0) if fmt == MXFP4 else np.float32(gs2)
+    if not gs > 0:
+        raise ValueError("the global scale must be positive")
+    lo, hi = _f32_down(H - delta), _f32_up(H + delta)
+    a_small = np.where((lo <= 0) & (hi >= 0), np.float32(0), np.minimum(np.abs(lo), np.abs(hi)))
+    a_large = np.maximum(np.abs(lo), np.abs(hi))
+    amax_lo = a_small.reshape(M, I // g, g).max(axis=-1)
+    amax_hi = a_large.reshape(M, I // g, g).max(axis=-1)
+    six = np.float32(6.0)
+    code_lo = _scale_round_n(fmt, (amax_lo / six) / gs)
+    code_hi = _scale_round_n(fmt, (amax_hi / six) / gs)
+    sf_ok = (SF >= code_lo) & (SF <= code_hi)
+    table = np.array([scale_value(fmt, b) for b in range(256)], dtype=np.float64)
+    with np.errstate(invalid="ignore", divide="ignore", over="ignore"):
+        s = table[SF].astype(np.float32) * gs
+        s_el = np.repeat(s, g, axis=1)
+        zero = s_el == 0
+        safe = np.where(zero | ~np.isfinite(s_el), np.float32(1), s_el)
+        c_lo = _e2m1_round_n(lo / safe)
+        c_hi = _e2m1_round_n(hi / safe)
+    key = np.array([4.0 * e2m1_value(c) for c in range(16)])
+    key[8] = -1.0                                    # -0 sits just below +0
+    nib = np.stack([Q & 15, Q >> 4], axis=-1).reshape(M, I)
+    el_ok = np.where(zero, nib == 0, (key[c_lo] <= key[nib]) & (key[nib] <= key[c_hi]))
+    el_ok &= np.isfinite(s_el)
+    return sf_ok & el_ok.reshape(M, I // g, g).all(axis=-1)
 
 
 def num_threads() -> int:

@@ -471,6 +471,41 @@ int oracle_gemm_nt_scaled_entries(int fmt, int64_t K,
     return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* SwiGLU of the MoE up-projection's output, before its requantisation       */
+/* ------------------------------------------------------------------------ */
+
+/* H = silu(G) * U = G * U / (1 + exp(-G)), elementwise in fp64, from the
+ * exact gate and up outputs G and U of the up-projection.  [QB] "Accuracy
+ * (real models)": a fused SwiGLU quantiser between the GEMMs; [DG] "Summary":
+ * the MoE L1 output is requantised with the L2 activations' global scale
+ * (that step is the a2 quantiser applied to H, see oracle/__init__.py).
+ * READING: silu(x) = x * sigmoid(x) = x / (1 + exp(-x)), the gate being the
+ * first half of the pair.  exp(-G) may overflow to +inf for G < -709; the
+ * quotient is then a signed zero, the limit of the expression. */
+int oracle_swiglu_f64(const double *G, const double *U, int64_t n, double *H)
+{
+    if (n < 0) return -1;
+    for (int64_t i = 0; i < n; ++i) H[i] = G[i] * U[i] / (1.0 + exp(-G[i]));
+    return 0;
+}
+
+/* The format roundings over an array (one call of the scalar rule per
+ * element), for checks over many values at once. */
+int oracle_e2m1_round_n(const float *q, int64_t n, uint8_t *code)
+{
+    if (n < 0) return -1;
+    for (int64_t i = 0; i < n; ++i) code[i] = (uint8_t)oracle_e2m1_round(q[i]);
+    return 0;
+}
+
+int oracle_scale_round_n(int fmt, const float *t, int64_t n, uint8_t *code)
+{
+    if (n < 0) return -1;
+    for (int64_t i = 0; i < n; ++i) code[i] = (uint8_t)oracle_scale_round(fmt, t[i]);
+    return 0;
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP

@@ -70,6 +70,15 @@ MUTANTS = [
      "double gsab = (double)gs_a * (double)gs_b;"),
     ("gemm_global_scale_of_a_twice", "(double)gs_a * (double)gs_b", "(double)gs_a * (double)gs_a"),
     ("gemm_accumulates_in_fp32", "double acc = 0.0, tacc = 0.0;", "float acc = 0.0f; double tacc = 0.0;"),
+    # SwiGLU and the array roundings behind the requantisation check
+    ("swiglu_sigmoid_of_plus_g", "G[i] * U[i] / (1.0 + exp(-G[i]))", "G[i] * U[i] / (1.0 + exp(G[i]))"),
+    ("swiglu_sigmoid_of_up", "G[i] * U[i] / (1.0 + exp(-G[i]))", "G[i] * U[i] / (1.0 + exp(-U[i]))"),
+    ("swiglu_without_sigmoid", "G[i] * U[i] / (1.0 + exp(-G[i]))", "G[i] * U[i]"),
+    ("swiglu_half_sigmoid", "G[i] * U[i] / (1.0 + exp(-G[i]))", "G[i] * U[i] / (2.0 + exp(-G[i]))"),
+    ("e2m1_round_n_drops_sign", "code[i] = (uint8_t)oracle_e2m1_round(q[i]);",
+     "code[i] = (uint8_t)(oracle_e2m1_round(q[i]) & 7);"),
+    ("scale_round_n_other_format", "code[i] = (uint8_t)oracle_scale_round(fmt, t[i]);",
+     "code[i] = (uint8_t)oracle_scale_round(1 - fmt, t[i]);"),
     ("rescale_row_twice", "(cs ? (double)cs[n] : 1.0)", "(rs ? (double)rs[m] : 1.0)"),
     ("rescale_drops_column", "(cs ? (double)cs[n] : 1.0)", "1.0"),
 ]

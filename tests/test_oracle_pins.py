@@ -498,3 +498,121 @@ def test_sf_interleave_vs_numpy_reshape(rows, cols):
     assert got.size == oracle.sf_mma_bytes(rows, cols) == want.size
     assert np.array_equal(got, want)
     assert np.array_equal(oracle.sf_from_mma(got, rows, cols), sf)
+
+
+# --------------------------------------------------------------------------
+# SwiGLU of the up-projection, and the validity check of its requantisation
+# --------------------------------------------------------------------------
+
+def test_swiglu_closed_forms():
+    """silu(x) = x * sigmoid(x): its limits, one value worked from e, the
+    identity silu(x) - silu(-x) = x, and exact linearity in the up operand."""
+    U = np.array([3.0, -2.5, 0.75, 1e3])
+    assert np.all(oracle.swiglu(np.zeros(4), U) == 0.0)                    # silu(0) = 0
+    G = np.array([40.0, 100.0, 1e4, 3.5e38])
+    assert np.array_equal(oracle.swiglu(G, U), G * U)                    # sigmoid -> 1
+    assert np.all(oracle.swiglu(np.array([-746.0, -1e4, -3e38, -800.0]), U) == 0.0)   # -> 0
+    e = math.e
+    assert oracle.swiglu(np.array([1.0]), np.array([2.0]))[0] == pytest.approx(2 * e / (e + 1), rel=1e-15)
+    assert oracle.swiglu(np.array([-1.0]), np.array([1.0]))[0] == pytest.approx(-1 / (e + 1), rel=1e-15)
+    x = synth.rng(401).normal(0, 4, 1000)
+    odd = oracle.swiglu(x, np.ones_like(x)) - oracle.swiglu(-x, np.ones_like(x))
+    assert np.allclose(odd, x, rtol=1e-15, atol=1e-300)
+    u = synth.rng(402).normal(0, 1, 1000)
+    assert np.array_equal(oracle.swiglu(x, 2.0 * u), 2.0 * oracle.swiglu(x, u))
+
+
+def test_swiglu_up_gate_and_up_roles():
+    """G comes from the gate rows and U from the up rows: doubling the up
+    weights (one UE8M0 step on every scale byte) doubles H exactly, doubling
+    the gate weights does not; zero gate weights give H = 0."""
+    A, Asf, Wg, Wgsf = _random_operands(MX, 6, 8, 256, 403)
+    _, _, Wu, Wusf = _random_operands(MX, 6, 8, 256, 404)
+    H, G, U, TG, TU = oracle.swiglu_up(MX, A, Asf, Wg, Wgsf, Wu, Wusf)
+    assert np.array_equal(G, oracle.gemm_nt(MX, A, Asf, Wg, Wgsf)[0])
+    assert np.array_equal(U, oracle.gemm_nt(MX, A, Asf, Wu, Wusf)[0])
+    H2u = oracle.swiglu_up(MX, A, Asf, Wg, Wgsf, Wu, Wusf + 1)[0]
+    assert np.array_equal(H2u, 2.0 * H)
+    H2g = oracle.swiglu_up(MX, A, Asf, Wg, Wgsf + 1, Wu, Wusf)[0]
+    assert not np.allclose(H2g, 2.0 * H)
+    H0 = oracle.swiglu_up(MX, A, Asf, np.zeros_like(Wg), Wgsf, Wu, Wusf)[0]
+    assert np.all(H0 == 0.0)
+    # NVFP4: the global scales multiply G and U before the nonlinearity
+    A, Asf, Wg, Wgsf = _random_operands(NV, 4, 16, 256, 405)
+    _, _, Wu, Wusf = _random_operands(NV, 4, 16, 256, 406)
+    Hs, Gs, Us, _, _ = oracle.swiglu_up(NV, A, Asf, Wg, Wgsf, Wu, Wusf, 0.5, 0.25)
+    H1, G1, U1, _, _ = oracle.swiglu_up(NV, A, Asf, Wg, Wgsf, Wu, Wusf)
+    assert np.array_equal(Gs, G1 * 0.125) and np.array_equal(Us, U1 * 0.125)
+    assert np.array_equal(Hs, oracle.swiglu(G1 * 0.125, U1 * 0.125))
+
+
+def _requant_case(fmt, M, I, seed):
+    gen = synth.rng(seed)
+    H = gen.normal(0, 1, (M, I)) * np.exp(gen.normal(0, 1, (M, 1)))
+    gs2 = np.float32(np.abs(H).max() / 2688.0) if fmt == NV else np.float32(1.0)
+    return H, gs2
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_requant_valid_is_exact_at_zero_width(fmt):
+    """With delta = 0 and H already fp32, exactly the rule's own output
+    passes: any other scale byte or any other element code fails."""
+    H, gs2 = _requant_case(fmt, 8, 256, 407 + fmt)
+    H = H.astype(np.float32).astype(np.float64)
+    Q, SF = oracle.swiglu_requantize(fmt, H, gs2)
+    z = np.zeros_like(H)
+    assert oracle.requant_valid(fmt, Q, SF, H, z, gs2).all()
+    g = oracle.block_size(fmt)
+    gen = synth.rng(409)
+    for _ in range(40):
+        r, j = int(gen.integers(0, 8)), int(gen.integers(0, 256 // g))
+        SF2 = SF.copy()
+        SF2[r, j] = (int(SF[r, j]) + (1 if gen.integers(0, 2) else -1)) % 256
+        ok = oracle.requant_valid(fmt, Q, SF2, H, z, gs2)
+        assert not ok[r, j] and ok.sum() == ok.size - 1
+        k = int(gen.integers(0, 256))
+        Q2 = Q.copy()
+        Q2[r, k // 2] ^= np.uint8((1 + int(gen.integers(0, 15))) << (4 * (k % 2)))
+        ok = oracle.requant_valid(fmt, Q2, SF, H, z, gs2)
+        assert not ok[r, k // g] and ok.sum() == ok.size - 1
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_requant_valid_accepts_every_input_in_the_box(fmt):
+    """Whatever fp32 matrix inside [H - delta, H + delta] the rule is given,
+    its output passes (random points, and both corners of the box)."""
+    H, gs2 = _requant_case(fmt, 16, 512, 410 + fmt)
+    delta = 2e-3 * np.abs(H) + 1e-4 * np.abs(H).max()
+    gen = synth.rng(412 + fmt)
+    points = [H - delta, H + delta] + [H + delta * gen.uniform(-1, 1, H.shape) for _ in range(12)]
+    for h in points:
+        h32 = np.clip(h.astype(np.float32), oracle._f32_down(H - delta), oracle._f32_up(H + delta))
+        Q, SF = oracle.quantize(fmt, h32, gs2)
+        assert oracle.requant_valid(fmt, Q, SF, H, delta, gs2).all()
+
+
+def test_requant_valid_tie_and_zero_scale():
+    """A value on an E2M1 tie takes either neighbour once delta > 0, but not
+    a code two steps away; an all-zero NVFP4 block takes scale 0 and +0 codes
+    only."""
+    H = np.zeros((1, 16))
+    H[0, 0] = 6.0                 # amax 6 with gs 1: scale 1.0, so x / s = x
+    H[0, 1] = 0.25                # tie between codes 0 (0) and 1 (0.5)
+    Q, SF = oracle.swiglu_requantize(NV, H, 1.0)
+    assert SF[0, 0] == 0x38 and (Q[0, 0] >> 4) == 0
+    delta = np.full_like(H, 1e-6)
+    assert oracle.requant_valid(NV, Q, SF, H, delta, 1.0).all()
+    Q1 = Q.copy()
+    Q1[0, 0] = (Q[0, 0] & 15) | (1 << 4)                                   # 0.5
+    assert oracle.requant_valid(NV, Q1, SF, H, delta, 1.0).all()
+    assert not oracle.requant_valid(NV, Q1, SF, H, np.zeros_like(H), 1.0).any()
+    Q2 = Q.copy()
+    Q2[0, 0] = (Q[0, 0] & 15) | (2 << 4)                                   # 1.0
+    assert not oracle.requant_valid(NV, Q2, SF, H, delta, 1.0).any()
+    Z = np.zeros((1, 16))
+    Qz, SFz = oracle.swiglu_requantize(NV, Z, 1.0)
+    assert SFz[0, 0] == 0 and Qz.max() == 0
+    assert oracle.requant_valid(NV, Qz, SFz, Z, np.zeros_like(Z), 1.0).all()
+    Qn = Qz.copy()
+    Qn[0, 3] = 8                                                          # -0
+    assert not oracle.requant_valid(NV, Qn, SFz, Z, np.zeros_like(Z), 1.0).any()

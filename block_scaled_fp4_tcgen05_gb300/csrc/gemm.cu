@@ -629,3 +629,73 @@ extern "C" int qfp4_gemm_nt_grouped_scaled(int fmt, int64_t groups, const int32_
     return gemm_nt_grouped_impl(fmt, groups, row_offsets, total_rows, max_group_rows, N, K, A_packed, A_sf,
                                 B_packed, B_sf, gs_a, gs_b, row_scale, col_scale, D_bf16, stream);
 }
+
+// Up-projection with SwiGLU and requantisation: the pair GEMM over the
+// interleaved gate/up rows W, its epilogue writing H = silu(gate) * up
+// quantised (no D).  Dense (row_offsets NULL) or grouped.
+static int gemm_swiglu_impl(int fmt, int64_t groups, const int32_t *row_offsets, int64_t M, int64_t I,
+                            int64_t K, const void *A_packed, const void *A_sf, const void *W_packed,
+                            const void *W_sf, const float *gs_a, const float *gs_w, const float *gs_out,
+                            void *Q_out, void *SF_out, void *stream)
+{
+    const bool grouped = row_offsets != nullptr;
+    if (fmt != QFP4_MXFP4 && fmt != QFP4_NVFP4) return QFP4_ERR_INVALID_ARG;
+    if (M < 0 || I < 0 || K < 0 || (grouped && groups < 1)) return QFP4_ERR_INVALID_ARG;
+    if (grouped && groups > kMaxGroupsGemm) return QFP4_ERR_UNSUPPORTED;
+    if (I % 128 != 0 || K % 128 != 0 || M > INT32_MAX / 2 || 2 * I * (grouped ? groups : 1) > INT32_MAX / 2 ||
+        K > INT32_MAX / 2)
+        return QFP4_ERR_UNSUPPORTED;
+    if (M == 0 || I == 0) return QFP4_OK;           // empty H: nothing to do, nothing launched
+    const int g = fmt == QFP4_MXFP4 ? 32 : 16;
+    if (!Q_out || !SF_out || (fmt == QFP4_NVFP4 && !gs_out)) return QFP4_ERR_INVALID_ARG;
+    if (!aligned16(Q_out) || !aligned4(SF_out) || (gs_out && !aligned4(gs_out)) ||
+        (grouped && !aligned4(row_offsets)))
+        return QFP4_ERR_MISALIGNED;
+    if (K > 0) {
+        if (!A_packed || !A_sf || !W_packed || !W_sf) return QFP4_ERR_INVALID_ARG;
+        if (!aligned16(A_packed) || !aligned16(A_sf) || !aligned16(W_packed) || !aligned16(W_sf) ||
+            (gs_a && !aligned4(gs_a)) || (gs_w && !aligned4(gs_w)))
+            return QFP4_ERR_MISALIGNED;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t sf_bytes = grouped ? qfp4_sf_mma_grouped_bytes(M, groups, I / g) : qfp4_sf_mma_bytes(M, I / g);
+    // padding rows of the scale layout must read as zero scales downstream
+    if (cudaMemsetAsync(SF_out, 0, sf_bytes, s) != cudaSuccess) return QFP4_ERR_CUDA;
+    if (K == 0) {
+        // empty sums: G = U = 0, so H = 0, every scale byte 0 and every code +0
+        return cudaMemsetAsync(Q_out, 0, static_cast<size_t>(M) * static_cast<size_t>(I / 2), s) == cudaSuccess
+                   ? QFP4_OK
+                   : QFP4_ERR_CUDA;
+    }
+    GemmParams a{static_cast<const uint8_t *>(A_sf), static_cast<const uint8_t *>(W_sf), gs_a, gs_w, nullptr,
+                 static_cast<int32_t>(M), static_cast<int32_t>(2 * I), static_cast<int32_t>(K),
+                 static_cast<int32_t>(grouped ? groups : 0), row_offsets, nullptr, nullptr, gs_out,
+                 static_cast<uint8_t *>(Q_out), static_cast<uint8_t *>(SF_out), static_cast<int32_t>(I),
+                 static_cast<int32_t>(I / (4 * g))};
+    CUtensorMap ma, mb;
+    int rc = make_map(&ma, A_packed, K / 2, M, kBKBytes, 128);
+    if (rc == QFP4_OK) rc = make_map(&mb, W_packed, K / 2, 2 * I * (grouped ? groups : 1), kBKBytes, 128);
+    if (rc != QFP4_OK) return rc;
+    const int64_t m_tiles = (M + 255) / 256 + (grouped ? groups : 0);
+    return launch_gemm_pair_swiglu(fmt, grouped, ma, mb, a, m_tiles * (2 * I / 256), s);
+}
+
+extern "C" int qfp4_gemm_swiglu_quantize(int fmt, int64_t M, int64_t I, int64_t K, const void *A_packed,
+                                         const void *A_sf, const void *W_packed, const void *W_sf,
+                                         const float *gs_a, const float *gs_w, const float *gs_out, void *Q_out,
+                                         void *SF_out, void *stream)
+{
+    return gemm_swiglu_impl(fmt, 0, nullptr, M, I, K, A_packed, A_sf, W_packed, W_sf, gs_a, gs_w, gs_out, Q_out,
+                            SF_out, stream);
+}
+
+extern "C" int qfp4_gemm_swiglu_quantize_grouped(int fmt, int64_t groups, const int32_t *row_offsets,
+                                                 int64_t total_rows, int64_t I, int64_t K, const void *A_packed,
+                                                 const void *A_sf, const void *W_packed, const void *W_sf,
+                                                 const float *gs_a, const float *gs_w, const float *gs_out,
+                                                 void *Q_out, void *SF_out, void *stream)
+{
+    if (!row_offsets) return QFP4_ERR_INVALID_ARG;
+    return gemm_swiglu_impl(fmt, groups, row_offsets, total_rows, I, K, A_packed, A_sf, W_packed, W_sf, gs_a,
+                            gs_w, gs_out, Q_out, SF_out, stream);
+}

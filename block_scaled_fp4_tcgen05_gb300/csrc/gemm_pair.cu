@@ -44,6 +44,7 @@
 #include <cuda_runtime.h>
 
 #include "qfp4_common.cuh"
+#include "qfp4_fp4_codes.cuh"
 #include "qfp4_gemm_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -117,6 +118,46 @@ __device__ __forceinline__ void record_timeout()
     atomicOr(&g_status_gemm_pair, static_cast<uint32_t>(kStatusTimeout));
 }
 
+// silu(g) * u = g / (1 + exp(-g)) * u in fp32: CUDA's full-accuracy expf
+// (+inf for g below about -88.7, which makes the quotient a signed zero, the
+// limit), then a correctly rounded division and product.  quadbit README,
+// "Accuracy (real models)": the fused SwiGLU quantiser between the GEMMs.
+__device__ __forceinline__ float silu_mul(float g, float u)
+{
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
+// The quantiser's rule on one block of G values held by this thread, with
+// the same steps and roundings as the standalone quantiser: amax, t =
+// (amax / 6) / gs, the scale byte (UE8M0 for G = 32, where gs is 1; UE4M3
+// for G = 16), s = decode * gs, codes of h / s (all +0 when s is 0).
+// Returns the scale byte; writes G / 8 words of packed codes.
+template <int G>
+__device__ __forceinline__ uint32_t quant_block(const float (&h)[G], float gs, uint32_t *w)
+{
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < G; ++i) amax = fmaxf(amax, fabsf(h[i]));
+    uint32_t code;
+    float s;
+    if (G == 32) {
+        code = ue8m0_encode(__fdiv_rn(amax, 6.0f));
+        s = ue8m0_decode(code);
+    } else {
+        const float t = __fdiv_rn(__fdiv_rn(amax, 6.0f), gs);
+        code = t > 0.0f ? ue4m3_encode(t) : 0u;   // t is NaN for gs = 0
+        s = __fmul_rn(ue4m3_decode(code), gs);
+    }
+#pragma unroll
+    for (int b = 0; b < G / 8; ++b) {
+        float q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = s == 0.0f ? 0.0f : __fdiv_rn(h[8 * b + i], s);
+        w[b] = s == 0.0f ? 0u : e2m1x8(q);
+    }
+    return code;
+}
+
 struct PairTile {
     int32_t row0;      // first row of the pair's 256-row A tile
     int32_t row_end;   // rows of this tile's group end here (exclusive)
@@ -127,8 +168,10 @@ struct PairTile {
 
 // SCALED: the two-level epilogue (per-row and per-column rescale; grouped:
 // column scales [groups][N]); a separate instantiation so that the plain
-// kernels carry none of its registers.
-template <int FMT, bool GROUPED, bool DBL, bool SCALED>
+// kernels carry none of its registers.  SWIGLU: no D; the accumulator
+// columns are gate and up outputs interleaved in groups of G, and the
+// epilogue writes H = silu(gate) * up quantised (GemmParams Q_out, SF_out).
+template <int FMT, bool GROUPED, bool DBL, bool SCALED, bool SWIGLU = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmD, const GemmParams p)
@@ -463,6 +506,8 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         float gs_dense = 1.0f;
         if (FMT == QFP4_NVFP4 && !GROUPED)
             gs_dense = (p.gs_a ? p.gs_a[0] : 1.0f) * (p.gs_b ? p.gs_b[0] : 1.0f);
+        float gs_out_dense = 1.0f;          // SwiGLU: global scale of the requantised output
+        if (SWIGLU && FMT == QFP4_NVFP4 && !GROUPED) gs_out_dense = p.gs_out[0];
         for (int32_t t = pair_id; t < total_tiles; t += npairs) {
             const PairTile ti = tile_info(t);
             float gs = gs_dense;
@@ -480,6 +525,8 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 for (int j = 0; j < 4; ++j) csv[j] = p.col_scale ? p.col_scale[c0 + j * 32 + lane] : 1.0f;
             }
             const bool cscale = SCALED && p.col_scale != nullptr;   // uniform over the kernel
+            float gs_out = gs_out_dense;
+            if (SWIGLU && FMT == QFP4_NVFP4 && GROUPED) gs_out = p.gs_out[ti.group];
             // A warp whose wait runs out still takes part in this tile's
             // named barrier below (its drain reads are harmless); the barrier
             // ANDs every thread's view of "all well", so the eight warps
@@ -487,6 +534,69 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int got = __shfl_sync(0xffffffffu,
                                         lane == 0 ? (mbar_wait(smem_u32(acc_full), acc_phase) ? 1 : 0) : 0, 0);
             tc_fence_after();
+            if constexpr (SWIGLU) {
+                // This warp's 128 accumulator columns are W rows n0 + 128 half
+                // + [0, 128): groups of G gate rows followed by the G up rows
+                // of the same outputs, i.e. 64 columns of H starting at
+                // (n0 + 128 half) / 2.  NVFP4: chunk j (32 columns) is one
+                // block of 16; MXFP4: chunks 2k, 2k + 1 are one block of 32.
+                // Each lane (one row) quantises its own blocks: 32 bytes of
+                // codes and 4 (NVFP4) or 2 (MXFP4) scale bytes per tile half.
+                constexpr int G = C::G;
+                const int32_t hrow = ti.row0 + 128 * static_cast<int32_t>(rank) + quad * 32 + lane;
+                const uint32_t tcol = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + half * 128;
+                uint32_t qw[8];
+                uint32_t sfw = 0;
+                if (G == 16) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(tcol + j * 32, v);
+                        tmem_ld_wait();
+                        tmem_regs_after_wait(v);
+                        float h[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            h[i] = silu_mul(__fmul_rn(__uint_as_float(v[i]), gs),
+                                            __fmul_rn(__uint_as_float(v[16 + i]), gs));
+                        sfw |= quant_block<16>(h, gs_out, &qw[2 * j]) << (8 * j);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        uint32_t vg[32], vu[32];
+                        tmem_ld_32x32b_x32(tcol + k * 64, vg);
+                        tmem_ld_32x32b_x32(tcol + k * 64 + 32, vu);
+                        tmem_ld_wait();
+                        tmem_regs_after_wait(vg);
+                        tmem_regs_after_wait(vu);
+                        float h[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            h[i] = silu_mul(__uint_as_float(vg[i]), __uint_as_float(vu[i]));
+                        sfw |= quant_block<32>(h, 1.0f, &qw[4 * k]) << (8 * k);
+                    }
+                }
+                tc_fence_before();
+                if (!named_barrier_and(1, 256, got != 0 && *abort_flag == 0)) { ok = got != 0; break; }
+                if (warp == 12 && lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
+                if (hrow < ti.row_end) {
+                    uint8_t *qdst = p.Q_out + static_cast<size_t>(hrow) * static_cast<size_t>(p.I / 2) +
+                                    ti.n0 / 4 + half * 32;
+                    reinterpret_cast<uint4 *>(qdst)[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+                    reinterpret_cast<uint4 *>(qdst)[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+                    // MMA layout: 128-row tile (its index in A's layout), block
+                    // column c, row r of the tile at byte (r % 32) 16 + (r / 32) 4 + c % 4
+                    const int32_t c0 = G == 16 ? ti.n0 / 32 + half * 4 : ti.n0 / 64 + half * 2;
+                    const size_t off =
+                        (static_cast<size_t>(ti.sf_tile0 + static_cast<int32_t>(rank)) * p.kc_out + c0 / 4) * 512 +
+                        lane * 16 + quad * 4 + (c0 & 3);
+                    if (G == 16) *reinterpret_cast<uint32_t *>(p.SF_out + off) = sfw;
+                    else *reinterpret_cast<uint16_t *>(p.SF_out + off) = static_cast<uint16_t>(sfw);
+                }
+                acc_phase ^= 1;
+                continue;
+            }
             const int32_t row = ti.row0 + 128 * static_cast<int32_t>(rank) + quad * 32 + lane;
             const bool row_ok = row < ti.row_end;
             __nv_bfloat16 *dst = p.D + static_cast<size_t>(row_ok ? row : 0) * p.N + ti.n0 + half * 128;
@@ -595,12 +705,12 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     }
 }
 
-template <int FMT, bool GROUPED, bool DBL = false, bool SCALED = false>
+template <int FMT, bool GROUPED, bool DBL = false, bool SCALED = false, bool SWIGLU = false>
 int launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &md, const GemmParams &prm,
            int64_t pair_tiles, cudaStream_t s)
 {
     using C = PairCfg<FMT, GROUPED, DBL>;
-    auto kern = gemm_pair_kernel<FMT, GROUPED, DBL, SCALED>;
+    auto kern = gemm_pair_kernel<FMT, GROUPED, DBL, SCALED, SWIGLU>;
     static int configured_device = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return QFP4_ERR_CUDA;
@@ -643,6 +753,17 @@ int launch_gemm_pair(int fmt, bool grouped, const CUtensorMap &ma, const CUtenso
                        : launch<QFP4_NVFP4, false>(ma, mb, md, prm, pair_tiles, s);
     return grouped ? launch<QFP4_MXFP4, true>(ma, mb, md, prm, pair_tiles, s)
                    : launch<QFP4_MXFP4, false>(ma, mb, md, prm, pair_tiles, s);
+}
+
+int launch_gemm_pair_swiglu(int fmt, bool grouped, const CUtensorMap &ma, const CUtensorMap &mb,
+                            const GemmParams &prm, int64_t pair_tiles, cudaStream_t s)
+{
+    // there is no D: A's map stands in for the unused store map
+    if (fmt == QFP4_NVFP4)
+        return grouped ? launch<QFP4_NVFP4, true, false, false, true>(ma, mb, ma, prm, pair_tiles, s)
+                       : launch<QFP4_NVFP4, false, false, false, true>(ma, mb, ma, prm, pair_tiles, s);
+    return grouped ? launch<QFP4_MXFP4, true, false, false, true>(ma, mb, ma, prm, pair_tiles, s)
+                   : launch<QFP4_MXFP4, false, false, false, true>(ma, mb, ma, prm, pair_tiles, s);
 }
 
 }  // namespace qfp4

@@ -22,6 +22,15 @@ struct GemmParams {
     // bf16((acc * (gs_a*gs_b * row_scale[m])) * col_scale[n]); NULL = ones
     const float *row_scale;     // [M] or NULL
     const float *col_scale;     // [N] or NULL
+    // SwiGLU + requantisation epilogue (launch_gemm_pair_swiglu): the B rows
+    // are gate and up rows interleaved in groups of g (block size), N = 2 I;
+    // H = silu(gate) * up is quantised with gs_out into Q_out [M, I/2] and
+    // SF_out (MMA layout for [M, I/g]; per-group layout when grouped)
+    const float *gs_out;        // NVFP4: [1], or [groups] when grouped
+    uint8_t *Q_out;
+    uint8_t *SF_out;
+    int32_t I;                  // columns of H
+    int32_t kc_out;             // 512-byte SF atoms per 128 rows of H: I / (4 g)
 };
 
 // 2D byte matrix [rows, inner] tensor map with 128-byte swizzle and a box of
@@ -42,6 +51,12 @@ int make_map_kpairs(CUtensorMap *map, const void *base, uint64_t K, uint64_t row
 bool gemm_pair_double_stages(int fmt, bool grouped, int64_t K);
 int launch_gemm_pair(int fmt, bool grouped, const CUtensorMap &ma, const CUtensorMap &mb,
                      const CUtensorMap &md, const GemmParams &prm, int64_t pair_tiles, cudaStream_t s);
+
+// The same CTA-pair GEMM with the SwiGLU + requantisation epilogue instead
+// of a D store: ma and mb as for launch_gemm_pair (2-D, 128-row boxes), the
+// output described by prm.Q_out, prm.SF_out, prm.gs_out, prm.I, prm.kc_out.
+int launch_gemm_pair_swiglu(int fmt, bool grouped, const CUtensorMap &ma, const CUtensorMap &mb,
+                            const GemmParams &prm, int64_t pair_tiles, cudaStream_t s);
 
 int read_clear_status_gemm_pair(cudaStream_t s, uint32_t *out);
 

@@ -24,6 +24,7 @@
 #include <cuda_runtime.h>
 
 #include "qfp4_common.cuh"
+#include "qfp4_fp4_codes.cuh"
 #include "sm103_ptx.cuh"
 
 namespace qfp4 {
@@ -63,33 +64,6 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float &lo, float &hi)
 {
     lo = __uint_as_float(w << 16);
     hi = __uint_as_float(w & 0xFFFF0000u);
-}
-
-// UE4M3 scale byte of t >= 0: round to nearest even, saturate at 448 (0x7E).
-__device__ __forceinline__ uint32_t ue4m3_encode(float t)
-{
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(t));
-    return static_cast<uint32_t>(r) & 0xFFu;
-}
-
-// Value of a UE4M3 byte (0x00..0x7E) as fp32, exact.
-__device__ __forceinline__ float ue4m3_decode(uint32_t b)
-{
-    const uint32_t e = (b >> 3) & 15u, m = b & 7u;
-    return e == 0 ? static_cast<float>(m) * 0x1p-9f : __uint_as_float(((e + 120u) << 23) | (m << 20));
-}
-
-// UE8M0 code of t >= 0: nearest power of two 2^(c-127), ties (1.5 * 2^e) to
-// the even code, clamped to [0, 254]; t = 0 gives 0 (the format has no zero).
-__device__ __forceinline__ uint32_t ue8m0_encode(float t)
-{
-    const uint32_t bits = __float_as_uint(t);
-    const uint32_t E = bits >> 23, F = bits & 0x7FFFFFu;
-    if (E == 0) return F > 0x600000u ? 1u : 0u;   // subnormal: between 2^-127 and 2^-126
-    const uint32_t up = (F > 0x400000u) || (F == 0x400000u && (E & 1u));
-    const uint32_t c = E + up;
-    return c > 254u ? 254u : c;
 }
 
 // 2^(127 - c) as fp32 (exact; subnormal for c = 254).
@@ -231,21 +205,6 @@ __device__ __forceinline__ float block_amax(const uint32_t (&w)[W])
         for (int i = 0; i < n / 2; ++i)
             asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[i]) : "r"(m[2 * i]), "r"(m[2 * i + 1]));
     return fmaxf(fabsf(__uint_as_float(m[0] << 16)), fabsf(__uint_as_float(m[0] & 0xFFFF0000u)));
-}
-
-// Eight fp32 -> four packed bytes: element 2i in the low nibble of byte i.
-__device__ __forceinline__ uint32_t e2m1x8(const float (&q)[8])
-{
-    uint32_t w;
-    asm("{\n.reg .b8 b0, b1, b2, b3;\n"
-        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
-        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
-        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
-        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
-        "mov.b32 %0, {b0, b1, b2, b3};\n}"
-        : "=r"(w)
-        : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
-    return w;
 }
 
 // Four bf16 words (8 elements, element 2i in the low half of word i) -> four

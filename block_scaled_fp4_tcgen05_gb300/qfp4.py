@@ -44,6 +44,10 @@ SIGNATURES = {
     "qfp4_quantize_grouped_rows": (_i32, [_i32, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "qfp4_gemm_nt_grouped_scaled": (_i32, [_i32, _i64, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                            _vp, _vp, _vp, _vp, _vp, _vp]),
+    "qfp4_gemm_swiglu_quantize": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                         _vp]),
+    "qfp4_gemm_swiglu_quantize_grouped": (_i32, [_i32, _i64, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp,
+                                                 _vp, _vp, _vp, _vp, _vp]),
     "qfp4_quantize_grouped": (_i32, [_i32, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "qfp4_sf_interleave": (_i32, [_vp, _i64, _i64, _vp, _i32, _vp]),
     "qfp4_gemm_workspace_bytes": (_sz, [_i32, _i64, _i64, _i64]),
@@ -219,3 +223,23 @@ def gemm_nt_grouped_scaled(fmt, row_offsets, total_rows, max_group_rows, N, K, A
            load().qfp4_gemm_nt_grouped_scaled(fmt, groups, _p(row_offsets), total_rows, max_group_rows, N, K,
                                               _p(A), _p(A_sf), _p(B), _p(B_sf), _p(gs_a), _p(gs_b),
                                               _p(row_scale), _p(col_scale), _p(D), _stream(stream)))
+
+
+def gemm_swiglu_quantize(fmt, M, I, K, A, A_sf, W, W_sf, gs_a, gs_w, gs_out, Q_out, SF_out,
+                         stream=None) -> None:
+    """Up-projection with SwiGLU, requantised: W holds the gate and up rows
+    interleaved in groups of the block size; writes H = silu(gate) * up
+    quantised into Q_out [M, I/2] and SF_out (MMA layout for [M, I/g])."""
+    _check("qfp4_gemm_swiglu_quantize",
+           load().qfp4_gemm_swiglu_quantize(fmt, M, I, K, _p(A), _p(A_sf), _p(W), _p(W_sf), _p(gs_a), _p(gs_w),
+                                            _p(gs_out), _p(Q_out), _p(SF_out), _stream(stream)))
+
+
+def gemm_swiglu_quantize_grouped(fmt, row_offsets, total_rows, I, K, A, A_sf, W, W_sf, gs_a, gs_w, gs_out,
+                                 Q_out, SF_out, stream=None) -> None:
+    """Per-expert version; SF_out in the per-group MMA layout."""
+    groups = row_offsets.numel() - 1
+    _check("qfp4_gemm_swiglu_quantize_grouped",
+           load().qfp4_gemm_swiglu_quantize_grouped(fmt, groups, _p(row_offsets), total_rows, I, K, _p(A),
+                                                    _p(A_sf), _p(W), _p(W_sf), _p(gs_a), _p(gs_w), _p(gs_out),
+                                                    _p(Q_out), _p(SF_out), _stream(stream)))

@@ -284,6 +284,62 @@ int qfp4_gemm_nt_grouped_scaled(int fmt, int64_t groups, const int32_t *row_offs
                                 const float *row_scale, const float *col_scale,
                                 void *D_bf16, void *stream);
 
+/* ---------------------------------------------------------------------- */
+/* Up-projection with SwiGLU and requantisation                             */
+/* ---------------------------------------------------------------------- */
+
+/* The MoE / MLP up-projection fused with its SwiGLU and with the
+ * quantisation of the result for the next GEMM (DeepGEMM pull request
+ * "Summary": the L1 output is requantised with the L2 activations' global
+ * scale; quadbit README "Accuracy (real models)": fused SwiGLU quantiser):
+ *   G[m,j] = gs_a*gs_w * sum_k a[m,k] * w_gate[j,k]
+ *   U[m,j] = gs_a*gs_w * sum_k a[m,k] * w_up[j,k]          (fp32 accumulation)
+ *   H[m,j] = silu(G) * U = G / (1 + exp(-G)) * U            (fp32)
+ * and H [M, I] is quantised by the rule of qfp4_quantize with the global
+ * scale gs_out (NVFP4) or none (MXFP4), straight from the accumulator: no
+ * BF16 output is written.
+ *   A_packed  [M, K/2], A_sf MMA layout for [M, K/g] (as for qfp4_gemm_nt)
+ *   W_packed  [2I, K/2]: the gate and up rows INTERLEAVED in groups of g
+ *             (g = 16 NVFP4, 32 MXFP4): rows 2g b .. 2g b + g - 1 are gate
+ *             rows g b .. g b + g - 1, the next g rows the up rows of the same
+ *             outputs.  W_sf is the MMA layout for those [2I, K/g] rows.
+ *             (Quantise gate and up with one global scale, then permute rows.)
+ *   gs_a, gs_w DEVICE fp32 (NULL = 1.0; MXFP4 ignores them)
+ *   gs_out    DEVICE fp32, the global scale of H (required for NVFP4; MXFP4
+ *             ignores it).  It is an input, e.g. a calibrated value: an amax
+ *             of H over the batch would need a pass over H first.
+ *   Q_out     [M, I/2] packed codes of H, 16-byte aligned
+ *   SF_out    MMA layout for [M, I/g] (qfp4_sf_mma_bytes(M, I/g) bytes,
+ *             4-byte aligned); this call zeroes it first, so padding is 0.
+ * Requirements: I % 128 == 0, K % 128 == 0; M == 0 or I == 0 launches
+ * nothing; K == 0 gives H = 0 (all scale bytes and codes 0).  Kernel: the
+ * CTA-pair GEMM on 256 x 256 tiles of [M, 2I] for every M.
+ * Accuracy: each block of H is what the rule gives for some fp32 input
+ * within the accumulation error of G and U propagated through silu, plus a
+ * few fp32 roundings; a code can therefore differ from one computed from
+ * the exact H only where that value lies within this error of a rounding
+ * boundary. */
+int qfp4_gemm_swiglu_quantize(int fmt, int64_t M, int64_t I, int64_t K,
+                              const void *A_packed, const void *A_sf,
+                              const void *W_packed, const void *W_sf,
+                              const float *gs_a, const float *gs_w, const float *gs_out,
+                              void *Q_out, void *SF_out, void *stream);
+
+/* Grouped (per-expert) version for MoE batches: rows of group e (row_offsets
+ * as in qfp4_gemm_nt_grouped) use expert e's interleaved weights
+ * W_packed[e] ([groups, 2I, K/2], W_sf [groups] x MMA layout for [2I, K/g])
+ * and gs_a[e], gs_w[e], gs_out[e] (DEVICE fp32 [groups]).  A_sf and SF_out
+ * are per-group MMA layouts (as written by qfp4_quantize_grouped; SF_out
+ * holds qfp4_sf_mma_grouped_bytes(total_rows, groups, I/g) bytes), so H goes
+ * straight into the grouped down-projection.  1 <= groups <= 256; other
+ * requirements as qfp4_gemm_swiglu_quantize. */
+int qfp4_gemm_swiglu_quantize_grouped(int fmt, int64_t groups, const int32_t *row_offsets,
+                                      int64_t total_rows, int64_t I, int64_t K,
+                                      const void *A_packed, const void *A_sf,
+                                      const void *W_packed, const void *W_sf,
+                                      const float *gs_a, const float *gs_w, const float *gs_out,
+                                      void *Q_out, void *SF_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -80,3 +80,22 @@ def run_gemm(fmt, A, A_sf_rm, B, B_sf_rm, gs_a=None, gs_b=None):
     torch.cuda.synchronize()
     assert qfp4.poll_device_status() == 0
     return bf16_to_f64(D)
+
+
+def swiglu_delta(G, U, TG, TU, K):
+    """Bound on |H_kernel - H| for the fused SwiGLU epilogue, from the exact
+    G, U (fp64) and their sums of |a_k w_k| (TG, TU):
+      - the fp32 accumulation of G and U: at most one rounding per 64-K MMA
+        step of partial sums bounded by T, taken four times over for the
+        tensor core's internal sums, plus the rounding of acc * gs;
+      - silu's derivative lies in [-0.1, 1.1], so an error e_G in G moves
+        silu(G) * U by at most 1.1 e_G (|U| + e_U), and e_U moves it by
+        |silu(G)| e_U;
+      - exp, the division and the product in fp32: a few ulps of H."""
+    from oracle import swiglu
+    steps = max(1, K // 64)
+    e_g = 4.0 * steps * 2.0 ** -24 * TG + 2.0 ** -22 * np.abs(G)
+    e_u = 4.0 * steps * 2.0 ** -24 * TU + 2.0 ** -22 * np.abs(U)
+    silu = np.abs(swiglu(G, np.ones_like(G)))
+    H = swiglu(G, U)
+    return 1.1 * (np.abs(U) + e_u) * e_g + silu * e_u + 2.0 ** -19 * np.abs(H)

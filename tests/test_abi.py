@@ -158,3 +158,32 @@ def test_grouped_two_level_entry_points_reject_bad_arguments(lib):
     assert g(1, 0, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE, None, None, None, None, FAKE, None) == -1
     assert g(1, 2, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE, None, None, FAKE + 2, None, FAKE, None) == -3
     assert g(1, 2, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE + 2, FAKE, None) == -3
+
+
+def test_swiglu_entry_points_reject_bad_arguments(lib):
+    L = lib.qfp4_gemm_swiglu_quantize
+    ok_args = dict(fmt=1, M=300, I=256, K=512, A=FAKE, Asf=FAKE, W=FAKE, Wsf=FAKE, ga=None, gw=None,
+                   go=FAKE, Q=FAKE, SF=FAKE, stream=None)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return L(a["fmt"], a["M"], a["I"], a["K"], a["A"], a["Asf"], a["W"], a["Wsf"], a["ga"], a["gw"],
+                 a["go"], a["Q"], a["SF"], a["stream"])
+
+    assert call(fmt=2) == -1
+    assert call(M=-1) == -1
+    assert call(I=100) == -2                    # I % 128
+    assert call(K=200) == -2
+    assert call(M=0) == 0 and call(I=0) == 0     # empty H: nothing launched
+    assert call(go=None) == -1                  # NVFP4 needs the output's global scale
+    assert call(Q=None) == -1
+    assert call(Q=FAKE + 8) == -3
+    assert call(SF=FAKE + 2) == -3
+    assert call(A=None) == -1
+    assert call(W=FAKE + 4) == -3
+    G = lib.qfp4_gemm_swiglu_quantize_grouped
+    assert G(1, 2, None, 300, 256, 512, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, None) == -1
+    assert G(1, 0, FAKE, 300, 256, 512, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, None) == -1
+    assert G(1, 257, FAKE, 300, 256, 512, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, None) == -2
+    assert G(1, 2, FAKE + 2, 300, 256, 512, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, None) == -3
+    assert G(0, 2, FAKE, 0, 256, 512, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, FAKE, None) == 0

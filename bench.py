@@ -434,6 +434,12 @@ def sweep(device, l2_bytes, peaks):
     out.append(grouped_time(device, fp4_peak))
     # two-level NVFP4 (per-row global scales, row/column rescale in the epilogue)
     out.append(two_level_time(device, l2_bytes, fp4_peak))
+    # up-projection with SwiGLU and requantisation in the epilogue
+    for grouped in (False, True):
+        try:
+            out.append(swiglu_time(device, l2_bytes, fp4_peak, grouped))
+        except Exception as exc:       # keep the rest of the line if this entry fails
+            out.append({"workload": f"nvfp4_swiglu_up{'_grouped' if grouped else ''}", "error": repr(exc)[:200]})
     torch.cuda.empty_cache()
     return out
 
@@ -481,6 +487,95 @@ def two_level_time(device, l2_bytes, fp4_peak):
            "frac_fp4_peak_gemm": round(flop / (scaled_ms * 1e-3) / 1e12 / fp4_peak, 3)}
     del Qs, SFs, X, W
     return res
+
+
+def swiglu_time(device, l2_bytes, fp4_peak, grouped):
+    """Up-projection with SwiGLU and NVFP4 requantisation fused into the
+    epilogue, against the plain GEMM writing BF16 on the same operands:
+    dense 4096 tokens x I = 7168 x K = 4096 (W: 14336 gate/up rows), or the
+    top-2-of-8 MoE batch of the grouped workload with I = 7168 per expert.
+    Weights rotated past the L2 (dense) or the L2 flushed (grouped)."""
+    import torch
+    from block_scaled_fp4_tcgen05_gb300 import qfp4
+    fmt, g, K = qfp4.NVFP4, 16, 4096
+    I = synth.MOE_UP.N // 2
+    if grouped:
+        case = synth.MOE_UP
+        counts = synth.moe_counts(case.seed, case.tokens, case.experts, case.topk)
+        E = case.experts
+    else:
+        counts = np.array([4096])
+        E = 1
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows = int(offs[-1])
+    X = torch.from_numpy(synth.activations_bf16(synth.SEED_BASE + 7, rows, K).view(np.int16).copy()).view(
+        torch.bfloat16).to(device)
+    W = torch.from_numpy(synth.weights_bf16(synth.SEED_BASE + 8, E * 2 * I, K).view(np.int16).copy()).view(
+        torch.bfloat16).to(device)
+    d_offs = torch.from_numpy(offs).to(device)
+    w_offs = torch.arange(0, (E + 1) * 2 * I, 2 * I, dtype=torch.int32, device=device)
+    gs_a = torch.empty(E, dtype=torch.float32, device=device)
+    gs_w = torch.empty(E, dtype=torch.float32, device=device)
+    gs_o = torch.full((E,), 0.01, dtype=torch.float32, device=device)
+    Qa = torch.empty((rows, K // 2), dtype=torch.uint8, device=device)
+    SFa = torch.empty(qfp4.sf_mma_grouped_bytes(rows, E, K // g), dtype=torch.uint8, device=device)
+    Qw = torch.empty((E * 2 * I, K // 2), dtype=torch.uint8, device=device)
+    SFw = torch.empty(qfp4.sf_mma_grouped_bytes(E * 2 * I, E, K // g), dtype=torch.uint8, device=device)
+    qfp4.global_scale_grouped(X, d_offs, gs_a)
+    qfp4.quantize_grouped(fmt, X, d_offs, gs_a, Qa, SFa)
+    qfp4.global_scale_grouped(W, w_offs, gs_w)
+    qfp4.quantize_grouped(fmt, W, w_offs, gs_w, Qw, SFw)
+    del X, W
+    Qh = torch.empty((rows, I // 2), dtype=torch.uint8, device=device)
+    SFh = torch.empty(qfp4.sf_mma_grouped_bytes(rows, E, I // g), dtype=torch.uint8, device=device)
+    D = torch.empty((rows, 2 * I), dtype=torch.bfloat16, device=device)
+    if grouped:
+        def fused(i):
+            qfp4.gemm_swiglu_quantize_grouped(fmt, d_offs, rows, I, K, Qa, SFa, Qw, SFw, gs_a, gs_w, gs_o, Qh, SFh)
+
+        def plain(i):
+            qfp4.gemm_nt_grouped(fmt, d_offs, rows, int(counts.max()), 2 * I, K, Qa, SFa, Qw, SFw, gs_a, gs_w, D)
+        copies = 1
+    else:
+        copies = max(1, min(16, int(np.ceil(2 * l2_bytes / (Qw.numel() + SFw.numel()))) + 1))
+        Qs = [Qw] + [Qw.clone() for _ in range(copies - 1)]
+        SFs = [SFw] + [SFw.clone() for _ in range(copies - 1)]
+
+        def fused(i):
+            qfp4.gemm_swiglu_quantize(fmt, rows, I, K, Qa, SFa, Qs[i], SFs[i], gs_a, gs_w, gs_o, Qh, SFh)
+
+        def plain(i):
+            qfp4.gemm_nt(fmt, rows, 2 * I, K, Qa, SFa, Qs[i], SFs[i], gs_a, gs_w, D)
+    if grouped:
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+        def timed(fn):
+            for _ in range(3):
+                fn(0)
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(5):
+                flush.zero_()
+                s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s0.record()
+                fn(0)
+                e0.record()
+                torch.cuda.synchronize()
+                ts.append(s0.elapsed_time(e0))
+            return statistics.median(ts)
+        fused_ms, plain_ms = timed(fused), timed(plain)
+    else:
+        fused_ms = graph_time([(lambda i=i: fused(i)) for i in range(copies)], 5)
+        plain_ms = graph_time([(lambda i=i: plain(i)) for i in range(copies)], 5)
+    assert qfp4.poll_device_status() == 0
+    flop = 2.0 * rows * 2 * I * K
+    name = (synth.MOE_UP.name.replace("grouped_up", "grouped_swiglu_up") if grouped
+            else f"nvfp4_swiglu_up_{rows}x{I}x{K}")
+    return {"workload": name, "us_fused": round(fused_ms * 1e3, 2), "us_gemm_bf16_out": round(plain_ms * 1e3, 2),
+            "fused_cost": round(fused_ms / plain_ms - 1.0, 3),
+            "TFLOP/s_fused": round(flop / (fused_ms * 1e-3) / 1e12, 1),
+            "frac_fp4_peak_fused": round(flop / (fused_ms * 1e-3) / 1e12 / fp4_peak, 3),
+            "bytes_out_fused": int(Qh.numel() + SFh.numel()), "bytes_out_bf16": int(D.numel() * 2)}
 
 
 def grouped_time(device, fp4_peak):

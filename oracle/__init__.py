@@ -90,6 +90,7 @@ def _load():
             "oracle_gemm_nt_scaled_entries": (c_int, [c_int, c_i64, c_p, c_p, c_p, c_p, c_f, c_f, c_p, c_p,
                                                       c_i64, c_p, c_p, c_p, c_p]),
             "oracle_swiglu_f64": (c_int, [c_p, c_p, c_i64, c_p]),
+            "oracle_residual_rmsnorm": (c_int, [c_p, c_p, c_p, c_i64, c_i64, c_d, c_p, c_p, c_p]),
             "oracle_e2m1_round_n": (c_int, [c_p, c_i64, c_p]),
             "oracle_scale_round_n": (c_int, [c_int, c_p, c_i64, c_p]),
             "oracle_num_threads": (c_int, []),
@@ -368,22 +369,27 @@ def _f32_up(x: np.ndarray) -> np.ndarray:
 
 
 def requant_valid(fmt: int, Q: np.ndarray, SF: np.ndarray, H: np.ndarray, delta: np.ndarray,
-                  gs2: float = 1.0) -> np.ndarray:
+                  gs2=1.0, gs2_hi=None) -> np.ndarray:
     """Which blocks of a quantised matrix are what the quantiser's rule gives
-    for SOME fp32 matrix within delta of H (elementwise)?
+    for SOME fp32 matrix within delta of H (elementwise), and some global
+    scale in [gs2, gs2_hi]?
 
-    Where the value being quantised comes out of an fp32 accumulation, only H
+    Where the value being quantised comes out of an fp32 computation, only H
     (exact) and a bound delta on the distance are known; any fp32 value in
-    [H - delta, H + delta] is then a correct input.  The rule is monotone in
-    every step, so a block passes when
+    [H - delta, H + delta] is then a correct input.  Where the global scale is
+    itself computed that way (an amax over the row), it is known only to lie
+    in an interval; gs2_hi = None means it is exactly gs2.  The rule is
+    monotone in every step, so a block passes when
       - its scale byte lies between the codes the rule gives for the smallest
-        and the largest block amax that the box allows, and
-      - with the scale s that byte decodes to, each element's code lies
-        between the codes of the smallest and the largest value of its own
-        range divided by s (codes ordered along the real line, -0 just
-        below +0); if s is 0 every code must be 0.
-    Q [M, I/2] packed, SF row-major [M, I/g], H and delta fp64 [M, I],
-    gs2 > 0 (NVFP4; ignored for MXFP4).  Returns a bool mask [M, I/g]."""
+        block amax over the largest scale and the largest amax over the
+        smallest scale, and
+      - with the scales s that byte gives over the interval, each element's
+        code lies between the codes of the smallest and the largest quotient
+        of its range by s (codes ordered along the real line, -0 just below
+        +0); if s is 0 every code must be 0.
+    Q [M, I/2] packed, SF row-major [M, I/g], H and delta fp64 [M, I]; gs2
+    and gs2_hi scalars or per-row arrays [M], > 0 (NVFP4; ignored for
+    MXFP4).  Returns a bool mask [M, I/g]."""
     g = block_size(fmt)
     H = np.asarray(H, dtype=np.float64)
     delta = np.asarray(delta, dtype=np.float64)
@@ -392,32 +398,80 @@ def requant_valid(fmt: int, Q: np.ndarray, SF: np.ndarray, H: np.ndarray, delta:
         raise ValueError("shapes")
     if np.any(delta < 0) or not np.all(np.isfinite(H)):
         raise ValueError("delta must be >= 0 and H finite")
-    gs = np.float32(1.0) if fmt == MXFP4 else np.float32(gs2)
-    if not gs > 0:
-        raise ValueError("the global scale must be positive")
+
+    def per_row(v):
+        a = np.asarray(v, dtype=np.float32)
+        return np.broadcast_to(a.reshape(-1, 1) if a.ndim else a, (M, 1)).astype(np.float32)
+
+    if fmt == MXFP4:
+        gs_lo = gs_hi = per_row(1.0)
+    else:
+        gs_lo = per_row(gs2)
+        gs_hi = gs_lo if gs2_hi is None else per_row(gs2_hi)
+    if not (np.all(gs_lo > 0) and np.all(gs_hi >= gs_lo)):
+        raise ValueError("the global scales must be positive and gs2 <= gs2_hi")
     lo, hi = _f32_down(H - delta), _f32_up(H + delta)
     a_small = np.where((lo <= 0) & (hi >= 0), np.float32(0), np.minimum(np.abs(lo), np.abs(hi)))
     a_large = np.maximum(np.abs(lo), np.abs(hi))
     amax_lo = a_small.reshape(M, I // g, g).max(axis=-1)
     amax_hi = a_large.reshape(M, I // g, g).max(axis=-1)
     six = np.float32(6.0)
-    code_lo = _scale_round_n(fmt, (amax_lo / six) / gs)
-    code_hi = _scale_round_n(fmt, (amax_hi / six) / gs)
+    code_lo = _scale_round_n(fmt, (amax_lo / six) / gs_hi)
+    code_hi = _scale_round_n(fmt, (amax_hi / six) / gs_lo)
     sf_ok = (SF >= code_lo) & (SF <= code_hi)
     table = np.array([scale_value(fmt, b) for b in range(256)], dtype=np.float64)
     with np.errstate(invalid="ignore", divide="ignore", over="ignore"):
-        s = table[SF].astype(np.float32) * gs
-        s_el = np.repeat(s, g, axis=1)
-        zero = s_el == 0
-        safe = np.where(zero | ~np.isfinite(s_el), np.float32(1), s_el)
-        c_lo = _e2m1_round_n(lo / safe)
-        c_hi = _e2m1_round_n(hi / safe)
+        dec = table[SF].astype(np.float32)
+        s_lo = np.repeat(dec * gs_lo, g, axis=1)
+        s_hi = np.repeat(dec * gs_hi, g, axis=1)
+        zero = s_hi == 0
+        finite = np.isfinite(s_lo) & np.isfinite(s_hi)
+        one = np.float32(1)
+        sl = np.where(zero | ~finite, one, s_lo)
+        sh = np.where(zero | ~finite, one, s_hi)
+        corners = np.stack([lo / sl, lo / sh, hi / sl, hi / sh])
+        c_lo = _e2m1_round_n(corners.min(axis=0))
+        c_hi = _e2m1_round_n(corners.max(axis=0))
     key = np.array([4.0 * e2m1_value(c) for c in range(16)])
     key[8] = -1.0                                    # -0 sits just below +0
     nib = np.stack([Q & 15, Q >> 4], axis=-1).reshape(M, I)
     el_ok = np.where(zero, nib == 0, (key[c_lo] <= key[nib]) & (key[nib] <= key[c_hi]))
-    el_ok &= np.isfinite(s_el)
+    el_ok &= finite
     return sf_ok & el_ok.reshape(M, I // g, g).all(axis=-1)
+
+
+# ---- residual add and RMSNorm in front of the quantiser ------------------------
+
+def residual_rmsnorm(x: np.ndarray, r, gamma: np.ndarray, eps: float = 1e-6):
+    """y = bf16(x + r) (the new residual stream; r may be None), and
+    z = y / sqrt(mean(y^2) + eps) * gamma in fp64.  x, r: bf16 bits [M, K];
+    gamma: bf16 bits [K].  Returns (y bf16 bits [M, K], z fp64 [M, K],
+    1/rms fp64 [M])."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    M, K = x.shape
+    gamma = np.ascontiguousarray(gamma, dtype=np.uint16)
+    if gamma.shape != (K,):
+        raise ValueError("gamma must be [K]")
+    rp = None
+    if r is not None:
+        r = np.ascontiguousarray(r, dtype=np.uint16)
+        if r.shape != x.shape:
+            raise ValueError("residual shape")
+        rp = _ptr(r)
+    y = np.zeros((M, K), dtype=np.uint16)
+    z = np.zeros((M, K), dtype=np.float64)
+    inv = np.zeros(M, dtype=np.float64)
+    if lib.oracle_residual_rmsnorm(_ptr(x), rp, _ptr(gamma), M, K, float(eps), _ptr(y), _ptr(z), _ptr(inv)) != 0:
+        raise ValueError("bad arguments")
+    return y, z, inv
+
+
+def rows_global_scale_exact(z: np.ndarray) -> np.ndarray:
+    """The two-level rule's per-row global scale of an exact fp64 matrix:
+    amax over the row / (6 * 448), in fp64 (a kernel computes it in fp32
+    from its own z)."""
+    return np.abs(np.asarray(z, dtype=np.float64)).max(axis=1) / 2688.0
 
 
 def num_threads() -> int:

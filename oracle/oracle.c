@@ -490,6 +490,51 @@ int oracle_swiglu_f64(const double *G, const double *U, int64_t n, double *H)
     return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Residual add and RMSNorm in front of a quantiser                         */
+/* ------------------------------------------------------------------------ */
+
+/* Round an fp32 value to the nearest bf16 bit pattern, ties to even (the
+ * bf16 format is the top 16 bits of fp32).  NaN stays NaN. */
+static uint16_t float_to_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x40u);
+    const uint32_t lsb = (u >> 16) & 1u;
+    return (uint16_t)((u + 0x7FFFu + lsb) >> 16);
+}
+
+/* [QB] "Accuracy (real models)": fused RMSNorm and residual-add quantisers
+ * around the GEMMs of a transformer block.  Row m of the bf16 inputs:
+ *   y[k] = bf16(x[k] + r[k])            one fp32 addition, rounded to bf16
+ *                                       (the new residual stream; r may be
+ *                                       NULL, then y = x)
+ *   z[k] = y[k] / sqrt(mean_k y[k]^2 + eps) * gamma[k]       in fp64
+ * READING: the pages name the fusion only; this is the usual RMSNorm with a
+ * learned bf16 weight gamma, on the bf16 sum that the residual path keeps.
+ * Writes y (bf16 bits), z (fp64) and 1/rms per row (fp64). */
+int oracle_residual_rmsnorm(const uint16_t *x, const uint16_t *r, const uint16_t *gamma, int64_t M, int64_t K,
+                            double eps, uint16_t *y, double *z, double *inv_rms)
+{
+    if (M < 0 || K <= 0 || !(eps >= 0.0)) return -1;
+    for (int64_t m = 0; m < M; ++m) {
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const float xv = bf16_bits_to_float(x[m * K + k]);
+            const float s = r ? xv + bf16_bits_to_float(r[m * K + k]) : xv;
+            y[m * K + k] = float_to_bf16_rne(s);
+            const double yv = (double)bf16_bits_to_float(y[m * K + k]);
+            ss += yv * yv;
+        }
+        const double inv = 1.0 / sqrt(ss / (double)K + eps);
+        inv_rms[m] = inv;
+        for (int64_t k = 0; k < K; ++k)
+            z[m * K + k] = (double)bf16_bits_to_float(y[m * K + k]) * inv * (double)bf16_bits_to_float(gamma[k]);
+    }
+    return 0;
+}
+
 /* The format roundings over an array (one call of the scalar rule per
  * element), for checks over many values at once. */
 int oracle_e2m1_round_n(const float *q, int64_t n, uint8_t *code)

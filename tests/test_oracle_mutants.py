@@ -79,6 +79,14 @@ MUTANTS = [
      "code[i] = (uint8_t)(oracle_e2m1_round(q[i]) & 7);"),
     ("scale_round_n_other_format", "code[i] = (uint8_t)oracle_scale_round(fmt, t[i]);",
      "code[i] = (uint8_t)oracle_scale_round(1 - fmt, t[i]);"),
+    # residual add and RMSNorm
+    ("bf16_round_truncates", "return (uint16_t)((u + 0x7FFFu + lsb) >> 16);", "return (uint16_t)(u >> 16);"),
+    ("bf16_round_ties_up", "return (uint16_t)((u + 0x7FFFu + lsb) >> 16);", "return (uint16_t)((u + 0x8000u) >> 16);"),
+    ("rmsnorm_sum_not_mean", "1.0 / sqrt(ss / (double)K + eps)", "1.0 / sqrt(ss + eps)"),
+    ("rmsnorm_eps_outside_sqrt", "1.0 / sqrt(ss / (double)K + eps)", "1.0 / (sqrt(ss / (double)K) + eps)"),
+    ("rmsnorm_gamma_dropped", "* inv * (double)bf16_bits_to_float(gamma[k]);", "* inv;"),
+    ("rmsnorm_residual_ignored", "const float s = r ? xv + bf16_bits_to_float(r[m * K + k]) : xv;",
+     "const float s = xv;"),
     ("rescale_row_twice", "(cs ? (double)cs[n] : 1.0)", "(rs ? (double)rs[m] : 1.0)"),
     ("rescale_drops_column", "(cs ? (double)cs[n] : 1.0)", "1.0"),
 ]

@@ -616,3 +616,106 @@ def test_requant_valid_tie_and_zero_scale():
     Qn = Qz.copy()
     Qn[0, 3] = 8                                                          # -0
     assert not oracle.requant_valid(NV, Qn, SFz, Z, np.zeros_like(Z), 1.0).any()
+
+
+# --------------------------------------------------------------------------
+# residual add and RMSNorm in front of the quantiser
+# --------------------------------------------------------------------------
+
+def _bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+
+
+def _bits(t):
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_residual_add_rounds_like_torch_bf16():
+    """y = bf16(x + r): torch's float -> bfloat16 conversion (nearest even)
+    of the fp32 sum, on random values and on sums placed exactly halfway
+    between two bf16 values."""
+    gen = synth.rng(501)
+    x = synth.f32_to_bf16_bits(gen.normal(0, 1, (64, 128)).astype(np.float32))
+    r = synth.f32_to_bf16_bits(gen.normal(0, 3, (64, 128)).astype(np.float32))
+    # ties: x = 1 + 2^-7 (bf16), r = 2^-8 -> x + r sits between two bf16 values
+    x[0, :4] = synth.f32_to_bf16_bits(np.array([1 + 2 ** -7, 1.0, 1 + 2 ** -6, 3.0], np.float32))
+    r[0, :4] = synth.f32_to_bf16_bits(np.array([2 ** -8, 2 ** -8, 2 ** -8, 2 ** -7 * 3 / 2], np.float32))
+    y, _, _ = oracle.residual_rmsnorm(x, r, np.full(128, 0x3F80, np.uint16))
+    want = _bits((_bf16(x).float() + _bf16(r).float()).to(torch.bfloat16))
+    assert np.array_equal(y, want)
+    y0, _, _ = oracle.residual_rmsnorm(x, None, np.full(128, 0x3F80, np.uint16))
+    assert np.array_equal(y0, x)
+
+
+def test_rmsnorm_closed_forms():
+    """Rows worked by hand: [3, 4] has mean square 12.5, so z = [3, 4] * sqrt(2)
+    / 5; a constant row c = 0.5 with eps = 0.25 gives sqrt(0.5); with eps = 0
+    every row has mean square 1 after the norm; gamma scales z linearly and
+    doubling the input leaves z unchanged."""
+    one = np.full(2, 0x3F80, np.uint16)
+    x = synth.f32_to_bf16_bits(np.array([[3.0, 4.0]], np.float32))
+    _, z, inv = oracle.residual_rmsnorm(x, None, one, 0.0)
+    assert z[0] == pytest.approx(np.array([3.0, 4.0]) * math.sqrt(2) / 5, rel=1e-15)
+    c = synth.f32_to_bf16_bits(np.full((1, 16), 0.5, np.float32))
+    _, z, _ = oracle.residual_rmsnorm(c, None, np.full(16, 0x3F80, np.uint16), 0.25)
+    assert np.allclose(z, math.sqrt(0.5), rtol=1e-15, atol=0)
+    xb = synth.activations_bf16(502, 8, 256)
+    ones = np.full(256, 0x3F80, np.uint16)
+    _, z, _ = oracle.residual_rmsnorm(xb, None, ones, 0.0)
+    assert np.allclose((z ** 2).mean(axis=1), 1.0, rtol=1e-13)
+    x2 = synth.f32_to_bf16_bits(2.0 * synth.bf16_bits_to_f32(xb))
+    _, z2, _ = oracle.residual_rmsnorm(x2, None, ones, 0.0)
+    assert np.array_equal(z2, z)
+    twos = np.full(256, 0x4000, np.uint16)
+    _, zg, _ = oracle.residual_rmsnorm(xb, None, twos, 0.0)
+    assert np.array_equal(zg, 2.0 * z)
+    # the residual enters before the norm: x + r with r = x is x doubled
+    _, zr, _ = oracle.residual_rmsnorm(xb, xb, ones, 0.0)
+    assert np.array_equal(zr, z)
+    _, zr1, _ = oracle.residual_rmsnorm(xb, xb, ones, 1.0)
+    _, z1, _ = oracle.residual_rmsnorm(xb, None, ones, 1.0)
+    assert not np.allclose(zr1, z1)             # eps does not scale with the input
+
+
+def test_rows_global_scale_exact_matches_the_bf16_rule():
+    xb = synth.activations_bf16(503, 16, 512)
+    got = oracle.rows_global_scale_exact(synth.bf16_bits_to_f32(xb).astype(np.float64))
+    want = oracle.global_scale_rows(xb)
+    assert np.all(np.abs(got - want) <= np.spacing(want.astype(np.float32)))
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_requant_valid_per_row_scales_and_intervals(fmt):
+    """Per-row global scales check each row with its own scale; with an
+    interval [lo, hi] the rule's output for any scale inside it passes, and
+    an output made with a scale outside a point interval can fail."""
+    H, _ = _requant_case(fmt, 12, 256, 504 + fmt)
+    gen = synth.rng(506 + fmt)
+    gs = np.float32(np.abs(H).max(axis=1) / 2688.0)
+    z = np.zeros_like(H)
+    H32 = H.astype(np.float32).astype(np.float64)
+    Q = np.zeros((12, 128), np.uint8)
+    SF = np.zeros((12, 256 // oracle.block_size(fmt)), np.uint8)
+    for m in range(12):
+        Q[m:m + 1], SF[m:m + 1] = oracle.quantize(fmt, H32[m:m + 1].astype(np.float32), gs[m])
+    assert oracle.requant_valid(fmt, Q, SF, H32, z, gs).all()
+    for m in (0, 5, 11):
+        ok_m = oracle.requant_valid(fmt, Q[m:m + 1], SF[m:m + 1], H32[m:m + 1], z[m:m + 1], gs[m])
+        assert ok_m.all()
+    if fmt == MX:
+        return
+    lo = (gs * np.float32(0.97)).astype(np.float32)
+    hi = (gs * np.float32(1.05)).astype(np.float32)
+    for _ in range(6):
+        gsx = np.where(gen.uniform(size=12) < 0.5, lo, hi) if _ < 2 else \
+            (lo + (hi - lo) * gen.uniform(size=12).astype(np.float32)).astype(np.float32)
+        Qx = np.zeros_like(Q)
+        SFx = np.zeros_like(SF)
+        for m in range(12):
+            Qx[m:m + 1], SFx[m:m + 1] = oracle.quantize(NV, H32[m:m + 1].astype(np.float32), gsx[m])
+        assert oracle.requant_valid(NV, Qx, SFx, H32, z, lo, hi).all()
+    Qh = np.zeros_like(Q)
+    SFh = np.zeros_like(SF)
+    for m in range(12):
+        Qh[m:m + 1], SFh[m:m + 1] = oracle.quantize(NV, H32[m:m + 1].astype(np.float32), hi[m])
+    assert not oracle.requant_valid(NV, Qh, SFh, H32, z, gs).all()

@@ -91,6 +91,8 @@ def _load():
                                                       c_i64, c_p, c_p, c_p, c_p]),
             "oracle_swiglu_f64": (c_int, [c_p, c_p, c_i64, c_p]),
             "oracle_residual_rmsnorm": (c_int, [c_p, c_p, c_p, c_i64, c_i64, c_d, c_p, c_p, c_p]),
+            "oracle_sparse24_decompress": (c_int, [c_p, c_p, c_i64, c_i64, c_p]),
+            "oracle_sparse24_compress": (c_int, [c_p, c_i64, c_i64, c_p, c_p]),
             "oracle_e2m1_round_n": (c_int, [c_p, c_i64, c_p]),
             "oracle_scale_round_n": (c_int, [c_int, c_p, c_i64, c_p]),
             "oracle_num_threads": (c_int, []),
@@ -472,6 +474,41 @@ def rows_global_scale_exact(z: np.ndarray) -> np.ndarray:
     amax over the row / (6 * 448), in fp64 (a kernel computes it in fp32
     from its own z)."""
     return np.abs(np.asarray(z, dtype=np.float64)).max(axis=1) / 2688.0
+
+
+# ---- 2:4 pair-granular sparse operand ------------------------------------------
+
+def sparse24_decompress(Wc: np.ndarray, meta: np.ndarray, K: int) -> np.ndarray:
+    """Compressed rows Wc [rows, K/4] and metadata [rows, K/16] -> the dense
+    packed operand [rows, K/2] (two kept pairs of every four, see oracle.c)."""
+    Wc = np.ascontiguousarray(Wc, dtype=np.uint8)
+    meta = np.ascontiguousarray(meta, dtype=np.uint8)
+    rows = Wc.shape[0]
+    if Wc.shape != (rows, K // 4) or meta.shape != (rows, K // 16):
+        raise ValueError("shapes")
+    W = np.zeros((rows, K // 2), dtype=np.uint8)
+    if _load().oracle_sparse24_decompress(_ptr(Wc), _ptr(meta), rows, K, _ptr(W)) != 0:
+        raise ValueError("bad metadata (needs i0 < i1 in every group) or K % 16 != 0")
+    return W
+
+
+def sparse24_compress(W: np.ndarray):
+    """Dense packed operand [rows, K/2] with at most two non-zero pairs in
+    every group of four -> (Wc [rows, K/4], meta [rows, K/16])."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    rows, K = W.shape[0], W.shape[1] * 2
+    Wc = np.zeros((rows, K // 4), dtype=np.uint8)
+    meta = np.zeros((rows, K // 16), dtype=np.uint8)
+    if _load().oracle_sparse24_compress(_ptr(W), rows, K, _ptr(Wc), _ptr(meta)) != 0:
+        raise ValueError("a group holds more than two non-zero pairs, or K % 16 != 0")
+    return Wc, meta
+
+
+def gemm_nt_sparse24(fmt: int, A, A_sf, Wc, meta, W_sf, gs_a: float = 1.0, gs_w: float = 1.0):
+    """D = A @ W^T with W given 2:4 pair-sparse: the dense GEMM of the
+    decompressed operand (its scale factors are those of the dense K)."""
+    K = np.asarray(A).shape[1] * 2
+    return gemm_nt(fmt, A, A_sf, sparse24_decompress(Wc, meta, K), W_sf, gs_a, gs_w)
 
 
 def num_threads() -> int:

@@ -535,6 +535,66 @@ int oracle_residual_rmsnorm(const uint16_t *x, const uint16_t *r, const uint16_t
     return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* 2:4 pair-granular sparse operand                                          */
+/* ------------------------------------------------------------------------ */
+
+/* [QB] "Accuracy (real models)": Blackwell FP4 2:4 sparsity is pair-granular,
+ * the MMA keeping 2 of every 4 consecutive fp4 pairs along K.
+ * READING: a pair is the two E2M1 elements of one packed byte, so each group
+ * of four bytes (eight elements) of a row keeps two bytes, at pair indices
+ * i0 < i1, stored in that order in the compressed row [K/4 bytes].  The
+ * group's metadata nibble is i0 | (i1 << 2); two groups per metadata byte,
+ * the even group in the low nibble ([K/16] bytes per row).  The scale
+ * factors are those of the dense K.  A pair is zero when both of its
+ * elements decode to 0 (codes 0 or 8). */
+static int pair_is_zero(uint8_t b) { return (b & 7) == 0 && ((b >> 4) & 7) == 0; }
+
+int oracle_sparse24_decompress(const uint8_t *Wc, const uint8_t *meta, int64_t rows, int64_t K, uint8_t *W)
+{
+    if (rows < 0 || K < 0 || K % 16 != 0) return -1;
+    const int64_t groups = K / 8;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t j = 0; j < groups; ++j) {
+            const int nib = (meta[r * (K / 16) + j / 2] >> (4 * (j & 1))) & 15;
+            const int i0 = nib & 3, i1 = nib >> 2;
+            if (i0 >= i1) return -1;
+            uint8_t *w = W + r * (K / 2) + 4 * j;
+            for (int i = 0; i < 4; ++i) w[i] = 0;
+            w[i0] = Wc[r * (K / 4) + 2 * j];
+            w[i1] = Wc[r * (K / 4) + 2 * j + 1];
+        }
+    return 0;
+}
+
+/* The inverse for a dense packed matrix with at most two non-zero pairs per
+ * group: the non-zero pairs are kept, and a group with fewer keeps its
+ * lowest-indexed zero pairs as well, so that i0 < i1 always.  -1 if a group
+ * has more than two non-zero pairs. */
+int oracle_sparse24_compress(const uint8_t *W, int64_t rows, int64_t K, uint8_t *Wc, uint8_t *meta)
+{
+    if (rows < 0 || K < 0 || K % 16 != 0) return -1;
+    const int64_t groups = K / 8;
+    memset(meta, 0, (size_t)(rows * (K / 16)));
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t j = 0; j < groups; ++j) {
+            const uint8_t *w = W + r * (K / 2) + 4 * j;
+            int keep[4] = {0, 0, 0, 0}, n = 0;
+            for (int i = 0; i < 4; ++i)
+                if (!pair_is_zero(w[i])) { keep[i] = 1; ++n; }
+            if (n > 2) return -1;
+            for (int i = 0; i < 4 && n < 2; ++i)
+                if (!keep[i]) { keep[i] = 1; ++n; }
+            int idx[2], c = 0;
+            for (int i = 0; i < 4; ++i)
+                if (keep[i]) idx[c++] = i;
+            Wc[r * (K / 4) + 2 * j] = w[idx[0]];
+            Wc[r * (K / 4) + 2 * j + 1] = w[idx[1]];
+            meta[r * (K / 16) + j / 2] |= (uint8_t)((idx[0] | (idx[1] << 2)) << (4 * (j & 1)));
+        }
+    return 0;
+}
+
 /* The format roundings over an array (one call of the scalar rule per
  * element), for checks over many values at once. */
 int oracle_e2m1_round_n(const float *q, int64_t n, uint8_t *code)

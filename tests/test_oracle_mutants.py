@@ -87,6 +87,17 @@ MUTANTS = [
     ("rmsnorm_gamma_dropped", "* inv * (double)bf16_bits_to_float(gamma[k]);", "* inv;"),
     ("rmsnorm_residual_ignored", "const float s = r ? xv + bf16_bits_to_float(r[m * K + k]) : xv;",
      "const float s = xv;"),
+    # 2:4 pair-granular sparse operand
+    ("sparse24_even_group_high_nibble", "(meta[r * (K / 16) + j / 2] >> (4 * (j & 1))) & 15",
+     "(meta[r * (K / 16) + j / 2] >> (4 - 4 * (j & 1))) & 15"),
+    ("sparse24_kept_bytes_swapped",
+     "w[i0] = Wc[r * (K / 4) + 2 * j];\n            w[i1] = Wc[r * (K / 4) + 2 * j + 1];",
+     "w[i1] = Wc[r * (K / 4) + 2 * j];\n            w[i0] = Wc[r * (K / 4) + 2 * j + 1];"),
+    ("sparse24_negative_zero_is_nonzero", "return (b & 7) == 0 && ((b >> 4) & 7) == 0;", "return b == 0;"),
+    ("sparse24_group_stride_halved", "uint8_t *w = W + r * (K / 2) + 4 * j;\n            for (int i = 0; i < 4; ++i) w[i] = 0;",
+     "uint8_t *w = W + r * (K / 2) + 2 * j;\n            for (int i = 0; i < 4; ++i) w[i] = 0;"),
+    ("sparse24_meta_indices_swapped", "(uint8_t)((idx[0] | (idx[1] << 2)) << (4 * (j & 1)))",
+     "(uint8_t)((idx[1] | (idx[0] << 2)) << (4 * (j & 1)))"),
     ("rescale_row_twice", "(cs ? (double)cs[n] : 1.0)", "(rs ? (double)rs[m] : 1.0)"),
     ("rescale_drops_column", "(cs ? (double)cs[n] : 1.0)", "1.0"),
 ]

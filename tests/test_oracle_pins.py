@@ -719,3 +719,79 @@ def test_requant_valid_per_row_scales_and_intervals(fmt):
     for m in range(12):
         Qh[m:m + 1], SFh[m:m + 1] = oracle.quantize(NV, H32[m:m + 1].astype(np.float32), hi[m])
     assert not oracle.requant_valid(NV, Qh, SFh, H32, z, gs).all()
+
+
+# --------------------------------------------------------------------------
+# 2:4 pair-granular sparse operand
+# --------------------------------------------------------------------------
+
+def test_sparse24_hand_worked_groups():
+    """Two groups worked by hand: [00 21 00 43] keeps pairs 1 and 3 (nibble
+    1 | 3 << 2 = 0xD); [10 00 00 00] keeps pair 0 and the lowest zero pair 1
+    (nibble 4); the even group sits in the low nibble of the metadata byte."""
+    W = np.array([[0x00, 0x21, 0x00, 0x43, 0x10, 0x00, 0x00, 0x00]], np.uint8)
+    Wc, meta = oracle.sparse24_compress(W)
+    assert Wc.tolist() == [[0x21, 0x43, 0x10, 0x00]]
+    assert meta.tolist() == [[0xD | (0x4 << 4)]]
+    assert np.array_equal(oracle.sparse24_decompress(Wc, meta, 16), W)
+    # -0 codes count as zero pairs: 0x88 and 0x08 do not take a slot
+    W2 = np.array([[0x88, 0x31, 0x08, 0x75, 0, 0, 0, 0]], np.uint8)
+    Wc2, meta2 = oracle.sparse24_compress(W2)
+    assert Wc2[0, :2].tolist() == [0x31, 0x75] and (meta2[0, 0] & 15) == (1 | 3 << 2)
+    with pytest.raises(ValueError):
+        oracle.sparse24_compress(np.array([[0x11, 0x22, 0x33, 0, 0, 0, 0, 0]], np.uint8))
+    with pytest.raises(ValueError):                          # i0 >= i1 is not a valid group
+        oracle.sparse24_decompress(np.zeros((1, 4), np.uint8), np.array([[0x3 | (0x1 << 2)]], np.uint8), 16)
+
+
+def _random_sparse24(rows, K, seed):
+    """Random 2:4 operand: in every group of four bytes, two random pair
+    positions hold bytes whose elements are both non-zero."""
+    gen = synth.rng(seed)
+    W = np.zeros((rows, K // 2), np.uint8)
+    nz = lambda size: gen.integers(1, 8, size) | (gen.integers(0, 2, size) << 3)   # non-zero E2M1 codes
+    for r in range(rows):
+        for j in range(K // 8):
+            i = gen.choice(4, 2, replace=False)
+            W[r, 4 * j + i] = (nz(2) | (nz(2) << 4)).astype(np.uint8)
+    return W
+
+
+def test_sparse24_round_trips():
+    W = _random_sparse24(16, 256, 511)
+    Wc, meta = oracle.sparse24_compress(W)
+    assert np.array_equal(oracle.sparse24_decompress(Wc, meta, 256), W)
+    gen = synth.rng(512)
+    pairs = np.array([(a, b) for a in range(4) for b in range(a + 1, 4)])
+    sel = pairs[gen.integers(0, 6, (16, 32))]
+    nibs = (sel[..., 0] | (sel[..., 1] << 2)).astype(np.uint8)
+    meta2 = (nibs[:, 0::2] | (nibs[:, 1::2] << 4)).astype(np.uint8)
+    Wc2 = _random_sparse24(16, 128, 513)[:, :64]                            # bytes with non-zero elements
+    Wc2 = np.where(Wc2 == 0, np.uint8(0x11), Wc2)
+    W2 = oracle.sparse24_decompress(Wc2, meta2, 256)
+    Wc3, meta3 = oracle.sparse24_compress(W2)
+    assert np.array_equal(Wc3, Wc2) and np.array_equal(meta3, meta2)
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_sparse24_gemm_keeps_exactly_the_selected_positions(fmt):
+    """All kept elements 1.0 (code 2) with unit scales: D[m, n] is the sum of
+    a[m, k] over the positions k that row n keeps, found here from the
+    metadata by hand-written indexing."""
+    g = oracle.block_size(fmt)
+    M, N, K = 5, 6, 128
+    W = _random_sparse24(N, K, 514 + fmt)
+    W = np.where(W != 0, np.uint8(0x22), W)                   # both elements 1.0
+    Wc, meta = oracle.sparse24_compress(W)
+    one = 127 if fmt == MX else 0x38
+    Wsf = np.full((N, K // g), one, np.uint8)
+    A, Asf, _, _ = _random_operands(fmt, M, 1, K, 515 + fmt)
+    D, _ = oracle.gemm_nt_sparse24(fmt, A, Asf, Wc, meta, Wsf)
+    a = oracle.dequantize(fmt, A, Asf)
+    want = np.zeros((M, N))
+    for n in range(N):
+        for j in range(K // 8):
+            nib = (meta[n, j // 2] >> (4 * (j % 2))) & 15
+            for p in (nib & 3, nib >> 2):
+                want[:, n] += a[:, 8 * j + 2 * p] + a[:, 8 * j + 2 * p + 1]
+    assert np.allclose(D, want, rtol=1e-15, atol=0)

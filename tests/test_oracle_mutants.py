@@ -10,6 +10,7 @@ and not to the harness.  Only the CPU is used; the real oracle library is not
 touched.
 """
 import os
+import shutil
 import subprocess
 import sys
 from concurrent.futures import ThreadPoolExecutor
@@ -103,6 +104,57 @@ MUTANTS = [
 ]
 
 
+# The same for the Python half of the oracle (oracle/__init__.py): the
+# marshalling wrappers and the requantisation check.  Left out: rounding the
+# box ends to nearest instead of outward (equivalent: an fp32 value inside
+# the real box is never outside its nearest-rounded ends).
+PY_MUTANTS = [
+    ("py_quantize_bf16_read_as_fp32",
+     "    if x.dtype == np.uint16:\n        rc = lib.oracle_quantize_bf16(",
+     "    if x.dtype == np.int64:\n        rc = lib.oracle_quantize_bf16("),
+    ("py_quantize_per_row_scales_ignored", "    if np.ndim(gs) == 1:\n        if x.dtype != np.uint16:",
+     "    if False:\n        if x.dtype != np.uint16:"),
+    ("py_swiglu_gate_and_up_swapped",
+     "    G, TG = gemm_nt(fmt, A, A_sf, Wg, Wg_sf, gs_a, gs_w)\n    U, TU = gemm_nt(fmt, A, A_sf, Wu, Wu_sf, gs_a, gs_w)",
+     "    G, TG = gemm_nt(fmt, A, A_sf, Wu, Wu_sf, gs_a, gs_w)\n    U, TU = gemm_nt(fmt, A, A_sf, Wg, Wg_sf, gs_a, gs_w)"),
+    ("py_requant_negative_zero_equals_positive", "key[8] = -1.0", "key[8] = 0.0"),
+    ("py_requant_scale_range_ignores_interval", "code_lo = _scale_round_n(fmt, (amax_lo / six) / gs_hi)",
+     "code_lo = _scale_round_n(fmt, (amax_lo / six) / gs_lo)"),
+    ("py_requant_element_range_ignores_interval", "corners.min(axis=0)", "corners[0]"),
+    ("py_requant_box_never_spans_zero",
+     "a_small = np.where((lo <= 0) & (hi >= 0), np.float32(0), np.minimum(np.abs(lo), np.abs(hi)))",
+     "a_small = np.minimum(np.abs(lo), np.abs(hi))"),
+    ("py_requant_zero_scale_not_special", "el_ok = np.where(zero, nib == 0,", "el_ok = np.where(False, nib == 0,"),
+    ("py_rows_global_scale_without_6", "max(axis=1) / 2688.0", "max(axis=1) / 448.0"),
+]
+
+PKG = os.path.join(ROOT, "oracle")
+
+
+def _run_py(workdir, init_text):
+    """Run the pin suite against a copy of the oracle package whose Python
+    half is init_text: the copy and a copy of the pin suite (with its
+    conftest, which puts the copy first on sys.path) live in workdir."""
+    os.makedirs(os.path.join(workdir, "oracle"), exist_ok=True)
+    shutil.copy(os.path.join(PKG, "oracle.c"), os.path.join(workdir, "oracle", "oracle.c"))
+    with open(os.path.join(workdir, "oracle", "__init__.py"), "w") as f:
+        f.write(init_text)
+    tdir = os.path.join(workdir, "tests")
+    shutil.copytree(os.path.join(ROOT, "tests", "golden"), os.path.join(tdir, "golden"), dirs_exist_ok=True)
+    for name in ("conftest.py", "test_oracle_pins.py"):
+        shutil.copy(os.path.join(ROOT, "tests", name), os.path.join(tdir, name))
+    env = dict(os.environ, PYTHONPATH=ROOT, OMP_NUM_THREADS="2")
+    env.pop("QFP4_ORACLE_SOURCE", None)
+    b = subprocess.run([sys.executable, "-c", "import oracle; print(oracle.__file__); oracle.build(force=True)"],
+                       cwd=workdir, env=env, capture_output=True, text=True, timeout=300)
+    if b.returncode != 0 or not b.stdout.strip().startswith(os.path.join(workdir, "oracle")):
+        return b.returncode or -1, None, (b.stdout + b.stderr)[-2000:]
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(tdir, "test_oracle_pins.py"), "-x", "-q",
+                        "-p", "no:cacheprovider"], cwd=workdir, env=env, capture_output=True, text=True,
+                       timeout=300)
+    return 0, r.returncode, r.stdout[-2000:]
+
+
 def _run(workdir, text):
     """Build the given oracle source in workdir and run the pin suite on it.
     Returns (build returncode, pin-suite returncode, pin-suite output)."""
@@ -140,6 +192,29 @@ def test_planted_mistakes_are_caught(tmp_path):
     assert not not_built, f"mutants that did not build: {not_built}"
     # pytest exit code 1 = some pin failed; 0 = survived; anything else (a
     # usage error or a crash) does not count as caught
+    survived = {n: r[2] for n, r in results.items() if r[1] != 1}
+    assert not survived, "mistakes the pins let through:\n" + "\n".join(
+        f"{n}:\n{out}" for n, out in survived.items())
+
+
+def test_unmodified_python_copy_passes(tmp_path):
+    with open(os.path.join(PKG, "__init__.py")) as f:
+        brc, rc, out = _run_py(str(tmp_path), f.read())
+    assert brc == 0, out
+    assert rc == 0, out
+
+
+def test_planted_python_mistakes_are_caught(tmp_path):
+    with open(os.path.join(PKG, "__init__.py")) as f:
+        text = f.read()
+    for name, old, new in PY_MUTANTS:
+        assert old in text, f"{name}: text to mutate not found in oracle/__init__.py"
+    jobs = {name: (str(tmp_path / name), text.replace(old, new)) for name, old, new in PY_MUTANTS}
+    workers = max(1, min(8, (os.cpu_count() or 2) // 2))
+    with ThreadPoolExecutor(workers) as pool:
+        results = dict(zip(jobs, pool.map(lambda j: _run_py(*j), jobs.values())))
+    not_built = {n: r[2] for n, r in results.items() if r[0] != 0}
+    assert not not_built, f"copies that did not import or build: {not_built}"
     survived = {n: r[2] for n, r in results.items() if r[1] != 1}
     assert not survived, "mistakes the pins let through:\n" + "\n".join(
         f"{n}:\n{out}" for n, out in survived.items())

@@ -795,3 +795,33 @@ def test_sparse24_gemm_keeps_exactly_the_selected_positions(fmt):
             for p in (nib & 3, nib >> 2):
                 want[:, n] += a[:, 8 * j + 2 * p] + a[:, 8 * j + 2 * p + 1]
     assert np.allclose(D, want, rtol=1e-15, atol=0)
+
+
+def test_requant_valid_box_across_zero():
+    """When every element's range spans zero, an all-zero input lies in the
+    box, so the all-zero output (scale byte 0, +0 codes) must pass."""
+    for fmt in (MX, NV):
+        H = np.full((1, 32), 1e-3) * synth.rng(520 + fmt).choice([-1.0, 1.0], (1, 32))
+        delta = np.full_like(H, 2e-3)
+        g = oracle.block_size(fmt)
+        Q0 = np.zeros((1, 16), np.uint8)
+        SF0 = np.zeros((1, 32 // g), np.uint8)
+        assert oracle.requant_valid(fmt, Q0, SF0, H, delta, 1.0).all()
+        Qr, SFr = oracle.quantize(fmt, H.astype(np.float32), 1.0)
+        assert oracle.requant_valid(fmt, Qr, SFr, H, delta, 1.0).all()
+
+
+def test_requant_valid_underflowing_scale():
+    """A non-zero NVFP4 block far below the global scale takes scale byte 0,
+    which decodes to 0, so the rule writes +0 for every element, negative
+    ones included: that output passes, and -0 codes for the negative
+    elements do not."""
+    H = np.array([[3e-12, -2e-12, 1e-12, -4e-12] * 4])
+    Q, SF = oracle.swiglu_requantize(NV, H, 1.0)
+    assert SF.tolist() == [[0]] and Q.max() == 0
+    z = np.zeros_like(H)
+    assert oracle.requant_valid(NV, Q, SF, H, z, 1.0).all()
+    neg = np.stack([Q & 15, Q >> 4], axis=-1).reshape(1, 16)
+    neg[H < 0] = 8
+    Qn = (neg[:, 0::2] | (neg[:, 1::2] << 4)).astype(np.uint8)
+    assert not oracle.requant_valid(NV, Qn, SF, H, z, 1.0).any()

@@ -808,6 +808,9 @@ def main():
             "prologue_us": round(pro_ms * 1e3, 2),
             "peak_note": f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} TFLOP/s x {FP4_OVER_BF16:g} "
                          f"(nominal dense FP4:BF16 ratio), of {peaks['source']}"}
+    if traffic is None:
+        roof["traffic_note"] = ("no DRAM counters for the current source of this kernel's file "
+                                "(profiles/dram_traffic.json is keyed to the source it was captured on)")
     del pipe
     torch.cuda.empty_cache()
     extra = [] if args.no_sweep else sweep(device, l2_bytes, peaks)

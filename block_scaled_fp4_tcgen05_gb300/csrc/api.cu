@@ -2,9 +2,30 @@
 // device check and the device status poll.
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <mutex>
+#include <set>
+#include <utility>
 
 #include "qfp4_common.cuh"
 #include "qfp4_gemm_internal.cuh"
+
+namespace qfp4 {
+
+int ensure_smem_attr(const void *kern, int bytes)
+{
+    static std::mutex mu;
+    static std::set<std::pair<const void *, int>> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QFP4_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({kern, dev})) return QFP4_OK;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return QFP4_ERR_CUDA;
+    done.insert({kern, dev});
+    return QFP4_OK;
+}
+
+}  // namespace qfp4
 
 extern "C" int qfp4_version(void) { return 100; }   // 0.1.0
 

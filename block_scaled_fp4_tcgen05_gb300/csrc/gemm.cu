@@ -130,9 +130,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     if (GROUPED) pdl_wait();
     int32_t total_tiles;
     if (GROUPED) {
+        __shared__ int s_bad;
         for (int i = threadIdx.x; i <= args.groups; i += blockDim.x) s_offs[i] = args.row_offsets[i];
         __syncthreads();
         if (threadIdx.x == 0) {
+            // offsets that do not describe the rows the launch was sized
+            // for: no tile is processed and nothing is written
+            s_bad = group_offsets_valid(s_offs, args.groups, args.M, args.max_group_rows) ? 0 : 1;
+            if (s_bad && blockIdx.x == 0) atomicOr(&g_status_gemm, static_cast<uint32_t>(kStatusBadGroup));
             int32_t acc = 0;
             for (int e = 0; e < args.groups; ++e) {
                 s_tile_start[e] = acc;
@@ -142,7 +147,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             s_tile_start[args.groups] = acc;
         }
         __syncthreads();
-        total_tiles = s_tile_start[args.groups] * ntiles_n;
+        total_tiles = s_bad ? 0 : s_tile_start[args.groups] * ntiles_n;
     } else {
         total_tiles = ((args.M + kBM - 1) / kBM) * ntiles_n;
     }
@@ -459,13 +464,9 @@ int launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &a,
 {
     using C = Cfg<FMT, BN, STAGES>;
     auto kern = gemm_kernel<FMT, BN, STAGES, GROUPED>;
-    static int configured_device = -1;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return QFP4_ERR_CUDA;
-    if (configured_device != dev) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-            return QFP4_ERR_CUDA;
-        configured_device = dev;
+    {
+        const int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM);
+        if (rc != QFP4_OK) return rc;
     }
     const int sms = sm_count();
     if (sms <= 0) return QFP4_ERR_CUDA;
@@ -584,27 +585,34 @@ static int gemm_nt_grouped_impl(int fmt, int64_t groups, const int32_t *row_offs
         (gs_b && !aligned4(gs_b)) || (row_scale && !aligned4(row_scale)) || (col_scale && !aligned4(col_scale)))
         return QFP4_ERR_MISALIGNED;
     if (total_rows == 0) return QFP4_OK;
+    if (max_group_rows > INT32_MAX / 2) max_group_rows = 0;     // no bound worth checking
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     GemmParams a{static_cast<const uint8_t *>(A_sf), static_cast<const uint8_t *>(B_sf), gs_a, gs_b,
                  static_cast<__nv_bfloat16 *>(D_bf16), static_cast<int32_t>(total_rows),
                  static_cast<int32_t>(N), static_cast<int32_t>(K), static_cast<int32_t>(groups),
                  row_offsets, row_scale, col_scale};
+    a.max_group_rows = static_cast<int32_t>(max_group_rows);
+    // Upper bound on the row tiles of all groups, for the grid: every group
+    // may add one partial tile, and no group has more than max_group_rows
+    // rows (the kernels check both bounds against the offsets).
+    auto tile_bound = [&](int64_t rows_per_tile) {
+        const int64_t by_total = (total_rows + rows_per_tile - 1) / rows_per_tile + groups;
+        const int64_t by_max = groups * ((max_group_rows + rows_per_tile - 1) / rows_per_tile);
+        return max_group_rows > 0 && by_max < by_total ? by_max : by_total;
+    };
     CUtensorMap ma, mb;
-    (void)max_group_rows;
     if (N % 256 == 0) {
         CUtensorMap md;
         int rc = make_map(&ma, A_packed, K / 2, total_rows, kBKBytes, 128);
         if (rc == QFP4_OK) rc = make_map(&mb, B_packed, K / 2, groups * N, kBKBytes, 128);
         if (rc == QFP4_OK) rc = make_map_bf16(&md, D_bf16, N, total_rows, 16, 32);
         if (rc != QFP4_OK) return rc;
-        // upper bound on pair tiles: every group may add one partial tile
-        return launch_gemm_pair(fmt, true, ma, mb, md, a, ((total_rows + 255) / 256 + groups) * (N / 256), s);
+        return launch_gemm_pair(fmt, true, ma, mb, md, a, tile_bound(256) * (N / 256), s);
     }
     int rc = make_map(&ma, A_packed, K / 2, total_rows, kBKBytes, kBM);
     if (rc == QFP4_OK) rc = make_map(&mb, B_packed, K / 2, groups * N, kBKBytes, 128);
     if (rc != QFP4_OK) return rc;
-    const int64_t mt_bound = (total_rows + kBM - 1) / kBM + groups;
-    const int32_t tiles = static_cast<int32_t>(mt_bound * (N / 128));
+    const int32_t tiles = static_cast<int32_t>(tile_bound(kBM) * (N / 128));
     if (fmt == QFP4_NVFP4) return launch_gemm<QFP4_NVFP4, 128, 6, true>(ma, mb, a, tiles, s);
     return launch_gemm<QFP4_MXFP4, 128, 6, true>(ma, mb, a, tiles, s);
 }
@@ -613,8 +621,9 @@ extern "C" int qfp4_gemm_nt_grouped(int fmt, int64_t groups, const int32_t *row_
                                     int64_t total_rows, int64_t max_group_rows, int64_t N, int64_t K,
                                     const void *A_packed, const void *A_sf, const void *B_packed,
                                     const void *B_sf, const float *gs_a, const float *gs_b,
-                                    void *D_bf16, void *stream)
+                                    void *D_bf16, void *workspace, size_t ws_bytes, void *stream)
 {
+    (void)workspace; (void)ws_bytes;    // the grouped kernels need no scratch
     return gemm_nt_grouped_impl(fmt, groups, row_offsets, total_rows, max_group_rows, N, K, A_packed, A_sf,
                                 B_packed, B_sf, gs_a, gs_b, nullptr, nullptr, D_bf16, stream);
 }
@@ -624,8 +633,9 @@ extern "C" int qfp4_gemm_nt_grouped_scaled(int fmt, int64_t groups, const int32_
                                            const void *A_packed, const void *A_sf, const void *B_packed,
                                            const void *B_sf, const float *gs_a, const float *gs_b,
                                            const float *row_scale, const float *col_scale, void *D_bf16,
-                                           void *stream)
+                                           void *workspace, size_t ws_bytes, void *stream)
 {
+    (void)workspace; (void)ws_bytes;
     return gemm_nt_grouped_impl(fmt, groups, row_offsets, total_rows, max_group_rows, N, K, A_packed, A_sf,
                                 B_packed, B_sf, gs_a, gs_b, row_scale, col_scale, D_bf16, stream);
 }

@@ -372,13 +372,9 @@ int launch_decode(const CUtensorMap &mw, const CUtensorMap &mt, const CUtensorMa
 {
     using C = DecCfg<FMT>;
     auto kern = gemm_decode_kernel<FMT>;
-    static int configured_device = -1;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return QFP4_ERR_CUDA;
-    if (configured_device != dev) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-            return QFP4_ERR_CUDA;
-        configured_device = dev;
+    {
+        const int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM);
+        if (rc != QFP4_OK) return rc;
     }
     const int pairs = (g.N + 255) / 256;
     return launch_status(launch_pdl(kern, dim3(2 * pairs), dim3(kThreads), C::SMEM, s, mw, mt, md, g));

@@ -145,7 +145,10 @@ __device__ __forceinline__ uint32_t quant_block(const float (&h)[G], float gs, u
         s = ue8m0_decode(code);
     } else {
         const float t = __fdiv_rn(__fdiv_rn(amax, 6.0f), gs);
-        code = t > 0.0f ? ue4m3_encode(t) : 0u;   // t is NaN for gs = 0
+        // t is NaN only when amax and gs are both 0 (0/0) and then takes
+        // code 0 like t = 0; a non-zero block with gs = 0 has t = +inf and
+        // saturates to 0x7E, and s = 448 * 0 = 0 still makes its codes +0
+        code = t > 0.0f ? ue4m3_encode(t) : 0u;
         s = __fmul_rn(ue4m3_decode(code), gs);
     }
 #pragma unroll
@@ -211,9 +214,14 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (GROUPED) pdl_wait();
     int32_t total_tiles;
     if (GROUPED) {
+        __shared__ int s_bad;
         for (int i = threadIdx.x; i <= p.groups; i += blockDim.x) s_offs[i] = p.row_offsets[i];
         __syncthreads();
         if (threadIdx.x == 0) {
+            // offsets that do not describe the rows the launch was sized
+            // for: no tile is processed and nothing is written
+            s_bad = group_offsets_valid(s_offs, p.groups, p.M, p.max_group_rows) ? 0 : 1;
+            if (s_bad && blockIdx.x == 0) atomicOr(&g_status_gemm_pair, static_cast<uint32_t>(kStatusBadGroup));
             int32_t pt = 0, st = 0;
             for (int e = 0; e < p.groups; ++e) {
                 s_ptile[e] = pt;
@@ -226,7 +234,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             s_sftile[p.groups] = st;
         }
         __syncthreads();
-        total_tiles = s_ptile[p.groups] * ntiles_n;
+        total_tiles = s_bad ? 0 : s_ptile[p.groups] * ntiles_n;
     } else {
         total_tiles = ((p.M + 255) / 256) * ntiles_n;
     }
@@ -711,13 +719,9 @@ int launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &md, 
 {
     using C = PairCfg<FMT, GROUPED, DBL>;
     auto kern = gemm_pair_kernel<FMT, GROUPED, DBL, SCALED, SWIGLU>;
-    static int configured_device = -1;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return QFP4_ERR_CUDA;
-    if (configured_device != dev) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-            return QFP4_ERR_CUDA;
-        configured_device = dev;
+    {
+        const int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM);
+        if (rc != QFP4_OK) return rc;
     }
     const int sms = sm_count();
     if (sms < 2) return QFP4_ERR_CUDA;

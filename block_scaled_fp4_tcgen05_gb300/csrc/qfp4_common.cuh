@@ -23,6 +23,27 @@ inline int launch_status(cudaError_t e)
     return e == cudaSuccess ? QFP4_OK : QFP4_ERR_CUDA;
 }
 
+// Raises `kern`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device); later calls only look the pair up.
+// Safe to call from several host threads (a mutex guards the record).
+int ensure_smem_attr(const void *kern, int bytes);
+
+// Grouped launches read per-group row offsets from device memory.  They are
+// usable only if they start at 0, never decrease, end at the row count the
+// host sized the launch for and, when max_rows > 0, give no group more than
+// max_rows rows.  A kernel that finds them otherwise records kStatusBadGroup
+// and writes nothing.
+__device__ __forceinline__ bool group_offsets_valid(const int32_t *offs, int groups, int64_t total_rows,
+                                                    int64_t max_rows)
+{
+    if (offs[0] != 0 || offs[groups] != total_rows) return false;
+    for (int e = 0; e < groups; ++e) {
+        const int64_t rows = static_cast<int64_t>(offs[e + 1]) - offs[e];
+        if (rows < 0 || (max_rows > 0 && rows > max_rows)) return false;
+    }
+    return true;
+}
+
 inline int sm_count()
 {
     int dev = 0, n = 0;

@@ -31,6 +31,9 @@ struct GemmParams {
     uint8_t *SF_out;
     int32_t I;                  // columns of H
     int32_t kc_out;             // 512-byte SF atoms per 128 rows of H: I / (4 g)
+    // grouped launches: upper bound on any group's rows (0 = no bound); the
+    // kernels check the offsets against it and against M (= total rows)
+    int32_t max_group_rows;
 };
 
 // 2D byte matrix [rows, inner] tensor map with 128-byte swizzle and a box of

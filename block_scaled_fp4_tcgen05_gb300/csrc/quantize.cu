@@ -121,8 +121,10 @@ __device__ __forceinline__ BlockScale block_scale(float amax, float gs, float in
         b.mode = 1;
     } else {
         const float t = scale_target(amax, gs, inv_gs);
-        // t is NaN only for gs = 0 (an all-zero tensor: 0/0); like t = 0 it
-        // takes scale code 0, and the block then encodes as zeros
+        // t is NaN only when amax and gs are both 0 (0/0: an all-zero
+        // block under a zero global scale) and then takes code 0 like t = 0;
+        // a non-zero block with gs = 0 has t = +inf and saturates to 0x7E,
+        // and s = 448 * 0 = 0 still encodes it as zeros
         b.code = t > 0.0f ? ue4m3_encode(t) : 0u;
         b.s = __fmul_rn(ue4m3_decode(b.code), gs);
         if (b.s == 0.0f) {
@@ -311,7 +313,12 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
         fence_mbar_init();
     }
     __syncthreads();
+    __shared__ int s_bad;
     if (GROUPED && threadIdx.x == 0) {
+        // offsets that do not cover exactly the M rows of X: nothing is
+        // written (the scale buffer keeps the zeros the host wrote)
+        s_bad = group_offsets_valid(s_offs, groups, M, 0) ? 0 : 1;
+        if (s_bad && blockIdx.x == 0) atomicOr(&g_status_quant, static_cast<uint32_t>(kStatusBadGroup));
         int32_t acc = 0;
         for (int e = 0; e < groups; ++e) {
             s_tile0[e] = acc;
@@ -319,6 +326,7 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
         }
     }
     __syncthreads();
+    if (GROUPED && s_bad) return;
     const float gs_one = (FMT == QFP4_MXFP4 || GROUPED || ROWGS) ? 1.0f : *gs_ptr;
     const float inv_gs_one = __frcp_rn(gs_one);
 
@@ -448,6 +456,7 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
 // maximum folded into its group's word with atomicMax on the bit pattern
 // (non-negative floats order like unsigned integers); a warp keeps a running
 // maximum while its rows stay in one group.  One tensor uses amax_flat_kernel.
+// rows < 0: the row count is row_offsets[groups], read on the device.
 __global__ void __launch_bounds__(kThreads)
 amax_rows_kernel(const uint4 *__restrict__ X, int64_t rows, int64_t chunks_per_row, int groups,
                  const int32_t *__restrict__ row_offsets, uint32_t *__restrict__ amax_bits)
@@ -455,8 +464,16 @@ amax_rows_kernel(const uint4 *__restrict__ X, int64_t rows, int64_t chunks_per_r
     __shared__ int32_t s_offs[kMaxGroups + 1];
     pdl_wait();
     pdl_launch_dependents();
+    __shared__ int s_bad;
     for (int i = threadIdx.x; i <= groups; i += blockDim.x) s_offs[i] = row_offsets[i];
     __syncthreads();
+    if (rows < 0) rows = s_offs[groups];
+    if (threadIdx.x == 0) {
+        s_bad = group_offsets_valid(s_offs, groups, rows, 0) ? 0 : 1;
+        if (s_bad && blockIdx.x == 0) atomicOr(&g_status_quant, static_cast<uint32_t>(kStatusBadGroup));
+    }
+    __syncthreads();
+    if (s_bad) return;
     const int lane = threadIdx.x & 31;
     const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -669,14 +686,7 @@ cudaError_t launch_quantize(const void *X, int64_t M, int64_t K, const float *gs
     const int64_t chunks = (blocks * 2 * G + kChunkBytes - 1) / kChunkBytes;
     constexpr int smem = kQStages * kChunkBytes + 2 * kQStages * 8;
     auto kern = quantize_kernel<FMT, LAYOUT, GROUPED, ROWGS>;
-    static int configured_device = -1;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorUnknown;
-    if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-    }
+    if (ensure_smem_attr(reinterpret_cast<const void *>(kern), smem) != QFP4_OK) return cudaErrorUnknown;
     const int sms = sm_count();
     // five CTAs (40 consumer warps) per SM with a two-stage ring each: the
     // per-block scale arithmetic is a dependent chain, and more warps hide
@@ -753,6 +763,30 @@ extern "C" int qfp4_global_scale_grouped(const void *X_bf16, int64_t total_rows,
     }
     return launch_status(launch_pdl(gs_finalize_kernel, dim3((static_cast<unsigned>(groups) + 127) / 128), dim3(128),
                                     0, s, reinterpret_cast<uint32_t *>(gs_out), static_cast<int>(groups)));
+}
+
+extern "C" int qfp4_absmax_gs(int64_t groups, const int32_t *row_offsets, const void *X_bf16, int64_t K,
+                              float *gs_out, void *stream)
+{
+    if (!X_bf16 || !gs_out || !row_offsets || K < 0 || groups < 1) return QFP4_ERR_INVALID_ARG;
+    if (groups > kMaxGroups || K % 8 != 0) return QFP4_ERR_UNSUPPORTED;
+    if (!aligned16(X_bf16) || !aligned4(gs_out) || !aligned4(row_offsets)) return QFP4_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const unsigned gblocks = (static_cast<unsigned>(groups) + 127) / 128;
+    if (launch_pdl(gs_init_kernel, dim3(gblocks), dim3(128), 0, s, reinterpret_cast<uint32_t *>(gs_out),
+                   static_cast<int>(groups)) != cudaSuccess)
+        return QFP4_ERR_CUDA;
+    if (K > 0) {
+        // the row count lives on the device: a full grid of row-walking warps
+        const int sms = sm_count();
+        const int grid = (sms > 0 ? sms : 148) * 8;
+        if (launch_pdl(amax_rows_kernel, dim3(grid), dim3(kThreads), 0, s, static_cast<const uint4 *>(X_bf16),
+                       int64_t{-1}, K / 8, static_cast<int>(groups), row_offsets,
+                       reinterpret_cast<uint32_t *>(gs_out)) != cudaSuccess)
+            return QFP4_ERR_CUDA;
+    }
+    return launch_status(launch_pdl(gs_finalize_kernel, dim3(gblocks), dim3(128), 0, s,
+                                    reinterpret_cast<uint32_t *>(gs_out), static_cast<int>(groups)));
 }
 
 extern "C" int qfp4_global_scale_rows(const void *X_bf16, int64_t rows, int64_t cols, float *gs_out,

@@ -43,7 +43,8 @@ SIGNATURES = {
                                    _sz, _vp]),
     "qfp4_quantize_grouped_rows": (_i32, [_i32, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "qfp4_gemm_nt_grouped_scaled": (_i32, [_i32, _i64, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
-                                           _vp, _vp, _vp, _vp, _vp, _vp]),
+                                           _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "qfp4_absmax_gs": (_i32, [_i64, _vp, _vp, _i64, _vp, _vp]),
     "qfp4_gemm_swiglu_quantize": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                          _vp]),
     "qfp4_gemm_swiglu_quantize_grouped": (_i32, [_i32, _i64, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp,
@@ -53,7 +54,7 @@ SIGNATURES = {
     "qfp4_gemm_workspace_bytes": (_sz, [_i32, _i64, _i64, _i64]),
     "qfp4_gemm_nt": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "qfp4_gemm_nt_grouped": (_i32, [_i32, _i64, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
-                                    _vp, _vp, _vp, _vp]),
+                                    _vp, _vp, _vp, _vp, _sz, _vp]),
 }
 
 
@@ -146,6 +147,15 @@ def global_scale_grouped(X, row_offsets, gs_out, stream=None) -> None:
                                             _stream(stream)))
 
 
+def absmax_gs(row_offsets, X, gs_out, stream=None) -> None:
+    """Per-group global scales with the row count read on the device from
+    row_offsets[groups]; X is [>= that many rows, K]."""
+    K = X.shape[1]
+    groups = row_offsets.numel() - 1
+    _check("qfp4_absmax_gs",
+           load().qfp4_absmax_gs(groups, _p(row_offsets), _p(X), K, _p(gs_out), _stream(stream)))
+
+
 def quantize(fmt, X, gs, Q, SF, sf_layout=SF_ROWMAJOR, stream=None) -> None:
     M, K = X.shape
     _check("qfp4_quantize",
@@ -206,23 +216,25 @@ def gemm_nt(fmt, M, N, K, A, A_sf, B, B_sf, gs_a, gs_b, D, workspace=None, ws_by
 
 
 def gemm_nt_grouped(fmt, row_offsets, total_rows, max_group_rows, N, K, A, A_sf, B, B_sf,
-                    gs_a, gs_b, D, stream=None) -> None:
+                    gs_a, gs_b, D, workspace=None, ws_bytes=0, stream=None) -> None:
     groups = row_offsets.numel() - 1
     _check("qfp4_gemm_nt_grouped",
            load().qfp4_gemm_nt_grouped(fmt, groups, _p(row_offsets), total_rows, max_group_rows, N, K,
                                        _p(A), _p(A_sf), _p(B), _p(B_sf), _p(gs_a), _p(gs_b), _p(D),
-                                       _stream(stream)))
+                                       _p(workspace), ws_bytes, _stream(stream)))
 
 
 def gemm_nt_grouped_scaled(fmt, row_offsets, total_rows, max_group_rows, N, K, A, A_sf, B, B_sf,
-                           gs_a, gs_b, row_scale, col_scale, D, stream=None) -> None:
+                           gs_a, gs_b, row_scale, col_scale, D, workspace=None, ws_bytes=0,
+                           stream=None) -> None:
     """Grouped GEMM with the two-level epilogue: row m times row_scale[m],
     column n of group e times col_scale[e*N + n] (either may be None)."""
     groups = row_offsets.numel() - 1
     _check("qfp4_gemm_nt_grouped_scaled",
            load().qfp4_gemm_nt_grouped_scaled(fmt, groups, _p(row_offsets), total_rows, max_group_rows, N, K,
                                               _p(A), _p(A_sf), _p(B), _p(B_sf), _p(gs_a), _p(gs_b),
-                                              _p(row_scale), _p(col_scale), _p(D), _stream(stream)))
+                                              _p(row_scale), _p(col_scale), _p(D), _p(workspace), ws_bytes,
+                                              _stream(stream)))
 
 
 def gemm_swiglu_quantize(fmt, M, I, K, A, A_sf, W, W_sf, gs_a, gs_w, gs_out, Q_out, SF_out,

@@ -113,3 +113,5 @@ COMPUTE_SWEEP = tuple(
 )
 MOE_UP = GroupedCase("nvfp4_grouped_up_4096tok_top2_8exp", NVFP4, 4096, 8, 2, 14336, 4096,
                      SEED_BASE + 4)
+# the square NVFP4 GEMM of the compute sweep (quadbit README, "Headline result": square 8192)
+SQUARE_NV = next(c for c in COMPUTE_SWEEP if c.fmt == NVFP4 and c.M == c.N == c.K == 8192)

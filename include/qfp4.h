@@ -77,8 +77,10 @@ const char *qfp4_status_string(int status);
 int qfp4_device_check(void);
 
 /* Synchronise `stream`, then return and clear the device status word:
- * QFP4_OK, or QFP4_ERR_TIMEOUT if any kernel of this library gave up on a
- * bounded wait since the last poll (its outputs are then undefined). */
+ * QFP4_OK; QFP4_ERR_TIMEOUT if any kernel of this library gave up on a
+ * bounded wait since the last poll (its outputs are then undefined); or
+ * QFP4_ERR_INVALID_ARG if a grouped call found its device row_offsets
+ * unusable (see qfp4_global_scale_grouped) and wrote nothing. */
 int qfp4_poll_device_status(void *stream);
 
 /* ---------------------------------------------------------------------- */
@@ -112,10 +114,27 @@ int qfp4_global_scale(const void *X_bf16, int64_t rows, int64_t cols, float *gs_
  * of X (row_offsets is a DEVICE int32 array of groups+1 non-decreasing
  * entries, row_offsets[0] = 0, row_offsets[groups] = total_rows).
  * gs_out[e] = amax over group e / (6 * 448).  Same requirements, and
- * 1 <= groups <= 256. */
+ * 1 <= groups <= 256.
+ * Every grouped call of this library checks its row_offsets on the device
+ * (row_offsets[0] == 0, non-decreasing, row_offsets[groups] == the row count
+ * passed on the host, and for the GEMMs no group above max_group_rows).
+ * Offsets that fail make the kernels skip all work and make the next
+ * qfp4_poll_device_status return QFP4_ERR_INVALID_ARG: the GEMMs and the
+ * quantiser's codes are left untouched, the grouped quantiser's scale buffer
+ * keeps the zeros it is cleared to, and the global scales read 0. */
 int qfp4_global_scale_grouped(const void *X_bf16, int64_t total_rows, int64_t cols,
                               int64_t groups, const int32_t *row_offsets, float *gs_out,
                               void *stream);
+
+/* The same per-group global scales with the row count taken from the device:
+ * X has row_offsets[groups] rows of K BF16 elements, a value the host need not
+ * know (MoE routing writes the offsets on the device).  Launches a full grid
+ * of row-walking warps.  DeepGEMM pull request "Known limitations /
+ * follow-ups": per-expert global scales as device tensors.  Requirements:
+ * 1 <= groups <= 256, K % 8 == 0, X 16-byte aligned; the offsets are checked
+ * on the device as for qfp4_global_scale_grouped. */
+int qfp4_absmax_gs(int64_t groups, const int32_t *row_offsets, const void *X_bf16, int64_t K,
+                   float *gs_out, void *stream);
 
 /* Per-row global scales (two-level NVFP4; quadbit README, "Accuracy (real
  * models)": per-16 UE4M3 local scales under a per-row fp32 global scale):
@@ -257,17 +276,22 @@ int qfp4_gemm_nt_scaled(int fmt, int64_t M, int64_t N, int64_t K,
  *              qfp4_quantize_grouped)
  *   B_packed   [groups, N, K/2];   B_sf  [groups] x MMA layout for [N, K/g]
  *   gs_a, gs_b DEVICE fp32 [groups] (NULL = all 1.0)
- *   row_offsets DEVICE int32 [groups + 1]; max_group_rows is an upper bound
- *              on any group's rows (sizes the launch; rows beyond it are an
- *              error recorded in the device status word).
- * Requirements as qfp4_gemm_nt, with 1 <= groups <= 256; no workspace is
- * needed. */
+ *   row_offsets DEVICE int32 [groups + 1], checked on the device (see
+ *              qfp4_global_scale_grouped)
+ *   total_rows the rows of A and D; the host needs it for the tensor maps
+ *   max_group_rows  upper bound on any group's rows, or 0 for none.  It
+ *              bounds the grid (groups * ceil(max_group_rows / tile rows)
+ *              when that is below the bound from total_rows); a group above
+ *              it is reported like any other bad offsets.
+ *   workspace, ws_bytes  DEVICE scratch; the grouped kernels use none
+ *              (qfp4_gemm_workspace_bytes is 0 for them), NULL is fine.
+ * Requirements as qfp4_gemm_nt, with 1 <= groups <= 256. */
 int qfp4_gemm_nt_grouped(int fmt, int64_t groups, const int32_t *row_offsets,
                          int64_t total_rows, int64_t max_group_rows, int64_t N, int64_t K,
                          const void *A_packed, const void *A_sf,
                          const void *B_packed, const void *B_sf,
                          const float *gs_a, const float *gs_b,
-                         void *D_bf16, void *stream);
+                         void *D_bf16, void *workspace, size_t ws_bytes, void *stream);
 
 /* Grouped GEMM with the two-level epilogue of qfp4_gemm_nt_scaled:
  *   D[m,n] = bf16_rne( (acc[m,n] * (gs_a[e]*gs_b[e] * row_scale[m])) * col_scale[e*N + n] )
@@ -282,7 +306,7 @@ int qfp4_gemm_nt_grouped_scaled(int fmt, int64_t groups, const int32_t *row_offs
                                 const void *B_packed, const void *B_sf,
                                 const float *gs_a, const float *gs_b,
                                 const float *row_scale, const float *col_scale,
-                                void *D_bf16, void *stream);
+                                void *D_bf16, void *workspace, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------- */
 /* Up-projection with SwiGLU and requantisation                             */

@@ -97,19 +97,51 @@ def test_gemm_rejects_bad_arguments(lib):
 
 def test_grouped_and_interleave_reject_bad_arguments(lib):
     assert lib.qfp4_gemm_nt_grouped(1, 0, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE,
-                                    None, None, FAKE, None) == -1
+                                    None, None, FAKE, None, 0, None) == -1
     assert lib.qfp4_gemm_nt_grouped(1, 300, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE,
-                                    None, None, FAKE, None) == -2
+                                    None, None, FAKE, None, 0, None) == -2
     assert lib.qfp4_quantize_grouped(1, FAKE, 10, 256, 2, FAKE, None, FAKE, FAKE, None) == -1
     assert lib.qfp4_quantize_grouped(1, FAKE, 10, 256, 257, FAKE, FAKE, FAKE, FAKE, None) == -2
     assert lib.qfp4_gemm_nt_grouped(1, 257, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE,
-                                    None, None, FAKE, None) == -2
+                                    None, None, FAKE, None, 0, None) == -2
+    assert lib.qfp4_gemm_nt_grouped(1, 2, FAKE, 10, -1, 256, 256, FAKE, FAKE, FAKE, FAKE,
+                                    None, None, FAKE, None, 0, None) == -1     # max_group_rows < 0
     assert lib.qfp4_global_scale_grouped(FAKE, 10, 16, 257, FAKE, FAKE, None) == -2
     assert lib.qfp4_sf_interleave(FAKE, 10, 10, FAKE, 7, None) == -1
     assert lib.qfp4_sf_interleave(FAKE, 10, 10, FAKE + 1, 1, None) == -3
     assert lib.qfp4_sf_interleave(FAKE, 0, 10, FAKE, 1, None) == 0
     assert lib.qfp4_global_scale(FAKE, 10, 12, FAKE, None) == -2
     assert lib.qfp4_global_scale(FAKE + 2, 10, 16, FAKE, None) == -3
+
+
+def test_absmax_gs_rejects_bad_arguments(lib):
+    a = lib.qfp4_absmax_gs
+    assert a(0, FAKE, FAKE, 256, FAKE, None) == -1             # groups
+    assert a(257, FAKE, FAKE, 256, FAKE, None) == -2           # at most 256 groups
+    assert a(2, None, FAKE, 256, FAKE, None) == -1             # offsets required
+    assert a(2, FAKE, None, 256, FAKE, None) == -1
+    assert a(2, FAKE, FAKE, 256, None, None) == -1
+    assert a(2, FAKE, FAKE, 12, FAKE, None) == -2              # K % 8
+    assert a(2, FAKE, FAKE + 8, 256, FAKE, None) == -3
+    assert a(2, FAKE + 2, FAKE, 256, FAKE, None) == -3
+    assert a(2, FAKE, FAKE, 256, FAKE + 2, None) == -3
+
+
+def test_boundary_names_of_the_scope_table(lib):
+    """The entry points the scope of this library names, with the argument
+    counts given there: the three core calls, the per-expert global scale
+    (row count on the device), the grouped quantiser and the grouped GEMM
+    with its workspace pair, the workspace size query and the status calls."""
+    want = {"qfp4_quantize": 9, "qfp4_sf_interleave": 6, "qfp4_gemm_nt": 14,
+            "qfp4_gemm_workspace_bytes": 4, "qfp4_sf_mma_bytes": 2, "qfp4_absmax_gs": 6,
+            "qfp4_quantize_grouped": 10, "qfp4_gemm_nt_grouped": 17, "qfp4_poll_device_status": 1,
+            "qfp4_status_string": 1}
+    for name, nargs in want.items():
+        assert hasattr(lib, name), name
+        assert len(qfp4.SIGNATURES[name][1]) == nargs, name
+    # the grouped GEMM carries (workspace, ws_bytes) right before the stream
+    args = qfp4.SIGNATURES["qfp4_gemm_nt_grouped"][1]
+    assert args[-3] is qfp4._vp and args[-2] is qfp4._sz
 
 
 def test_two_level_entry_points_reject_bad_arguments(lib):
@@ -155,9 +187,12 @@ def test_grouped_two_level_entry_points_reject_bad_arguments(lib):
     assert q(1, FAKE, 10, 256, 2, FAKE, None, FAKE, FAKE, None) == -1          # NVFP4 needs gs_rows
     assert q(1, FAKE, 10, 256, 2, FAKE, FAKE + 2, FAKE, FAKE, None) == -3
     g = lib.qfp4_gemm_nt_grouped_scaled
-    assert g(1, 0, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE, None, None, None, None, FAKE, None) == -1
-    assert g(1, 2, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE, None, None, FAKE + 2, None, FAKE, None) == -3
-    assert g(1, 2, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE + 2, FAKE, None) == -3
+    assert g(1, 0, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE, None, None, None, None, FAKE, None, 0,
+             None) == -1
+    assert g(1, 2, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE, None, None, FAKE + 2, None, FAKE, None, 0,
+             None) == -3
+    assert g(1, 2, FAKE, 10, 10, 256, 256, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE + 2, FAKE, None, 0,
+             None) == -3
 
 
 def test_swiglu_entry_points_reject_bad_arguments(lib):

@@ -68,7 +68,7 @@ def test_reference_arm_json_line():
               "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
         assert k in d, k
     assert d["impl"] == "reference" and d["value"] > 0 and d["warmup"] >= 3
-    assert d["config"]["workload"] == "nvfp4_gemm_nt_4096x4096x4096"
+    assert d["config"]["workload"] == "nvfp4_gemm_nt_8192x8192x8192"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
     assert d["e2e"]["value"] == d["value"]

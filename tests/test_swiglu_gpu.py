@@ -119,7 +119,8 @@ def test_swiglu_quantize_vs_oracle(fmt, M, I, K):
 
 def test_swiglu_quantize_full_size_sampled_rows():
     """Llama-3-8B ffn-up shape (4096 tokens, I = 14336, K = 4096), NVFP4,
-    checked on whole sampled rows."""
+    checked on 64 whole rows: the tile edges (0, 255/256, 4095) and a seeded
+    sample spread over every 256-row pair tile."""
     fmt, M, I, K = NV, 4096, 14336, 4096
     g = 16
     xa = synth.activations_bf16(8300, M, K)
@@ -127,7 +128,9 @@ def test_swiglu_quantize_full_size_sampled_rows():
     SFa_m = to_mma(SFa)
     W, W_sf, gw, (qg, sfg, qu, sfu, gw_ref) = weights(fmt, I, K, 8400)
     ga_ref = oracle.global_scale(xa)
-    rows = np.array([0, 1, 255, 256, 2047, 3001, 4095])
+    edges = [0, 1, 127, 128, 255, 256, 2047, 4095]
+    pick = synth.rng(8301).choice(np.setdiff1d(np.arange(M), edges), 64 - len(edges), replace=False)
+    rows = np.sort(np.concatenate([edges, pick]))
     qa_ref, sfa_ref = oracle.quantize(fmt, xa[rows], ga_ref)
     torch.cuda.synchronize()
     assert np.float32(ga.item()) == ga_ref
@@ -213,3 +216,29 @@ def test_swiglu_quantize_empty_sum():
     qfp4.gemm_swiglu_quantize(NV, M, I, 0, None, None, None, None, None, None, dev_scalar(1.0), Qh, SFh)
     torch.cuda.synchronize()
     assert int(Qh.max()) == 0 and int(SFh.max()) == 0
+
+
+def test_swiglu_quantize_zero_output_scale():
+    """gs_out = 0 with a non-zero H: every block target is (amax/6)/0 = +inf,
+    which saturates the UE4M3 scale byte to 0x7E (448), and the element scale
+    s = 448 * 0 = 0 makes every code +0 (the zero-scale reading); the oracle
+    gives the same bytes."""
+    fmt, M, I, K = NV, 77, 128, 256
+    g = 16
+    xa = synth.activations_bf16(8700, M, K)
+    Qa, SFa, ga = quantize_dev(fmt, xa)
+    W, W_sf, gw, (qg, sfg, qu, sfu, gw_ref) = weights(fmt, I, K, 8800)
+    ga_ref = oracle.global_scale(xa)
+    qa_ref, sfa_ref = oracle.quantize(fmt, xa, ga_ref)
+    H = oracle.swiglu_up(fmt, qa_ref, sfa_ref, qg, sfg, qu, sfu, ga_ref, gw_ref)[0]
+    q_ref, sf_ref = oracle.swiglu_requantize(fmt, H, np.float32(0.0))
+    nonzero = np.abs(H).reshape(M, I // g, g).max(axis=-1) > 0
+    assert nonzero.all(), "the case wants every block of H non-zero"
+    assert np.all(sf_ref == 0x7E) and not q_ref.any()
+    Qh = torch.full((M, I // 2), 0x5A, dtype=torch.uint8, device="cuda")
+    SFh = torch.full((qfp4.sf_mma_bytes(M, I // g),), 0xA5, dtype=torch.uint8, device="cuda")
+    qfp4.gemm_swiglu_quantize(fmt, M, I, K, Qa, to_mma(SFa), W, W_sf, ga, gw, dev_scalar(0.0), Qh, SFh)
+    torch.cuda.synchronize()
+    assert qfp4.poll_device_status() == 0
+    assert not to_host(Qh).any(), "codes must all be +0 under a zero element scale"
+    assert np.array_equal(oracle.sf_from_mma(to_host(SFh), M, I // g), sf_ref)

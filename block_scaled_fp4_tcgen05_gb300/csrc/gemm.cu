@@ -481,13 +481,16 @@ using namespace qfp4;
 
 extern "C" size_t qfp4_gemm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K)
 {
-    (void)fmt; (void)M; (void)N; (void)K;
-    return 0;   // every kernel keeps its partial sums on chip
+    if ((fmt != QFP4_MXFP4 && fmt != QFP4_NVFP4) || M < 1 || M > 128 || N < 1 || K < 1 || N % 128 != 0 ||
+        K % 128 != 0 || N > INT32_MAX / 2 || K > INT32_MAX / 2)
+        return 0;   // only the decode kernel splits K; the others keep their sums on chip
+    return decode_workspace_bytes(M, N, K, decode_splits(M, N, K));
 }
 
 static int gemm_nt_impl(int fmt, int64_t M, int64_t N, int64_t K, const void *A_packed, const void *A_sf,
                         const void *B_packed, const void *B_sf, const float *gs_a, const float *gs_b,
-                        const float *row_scale, const float *col_scale, void *D_bf16, void *stream)
+                        const float *row_scale, const float *col_scale, void *D_bf16, void *workspace,
+                        size_t ws_bytes, void *stream)
 {
     if (fmt != QFP4_MXFP4 && fmt != QFP4_NVFP4) return QFP4_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0) return QFP4_ERR_INVALID_ARG;
@@ -514,11 +517,22 @@ static int gemm_nt_impl(int fmt, int64_t M, int64_t N, int64_t K, const void *A_
                  static_cast<int32_t>(K), 0, nullptr, row_scale, col_scale};
     CUtensorMap ma, mb;
     if (M <= 128) {
-        // decode shapes: swap AB on CTA pairs, weights in the MMA's M slot
+        // decode shapes: swap AB on CTA pairs, weights in the MMA's M slot;
+        // K split over more pairs when the weight tiles alone leave SMs idle
+        // and the caller's workspace holds the partial sums
+        int splits = decode_splits(M, N, K);
+        if (splits > 1 && !(workspace && aligned16(workspace) &&
+                            ws_bytes >= decode_workspace_bytes(M, N, K, splits)))
+            splits = 1;
+        a.splits = splits;
+        if (splits > 1) {
+            a.ws_count = static_cast<uint32_t *>(workspace);
+            a.ws_partial = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + decode_counter_bytes(N));
+        }
         CUtensorMap md;
         int rc = make_map(&mb, B_packed, K / 2, N, kBKBytes, 128);
         if (rc == QFP4_OK) rc = make_map(&ma, A_packed, K / 2, M, kBKBytes, 64);
-        if (rc == QFP4_OK) rc = make_map_bf16(&md, D_bf16, N, M, 128, 128);
+        if (rc == QFP4_OK) rc = make_map_bf16(&md, D_bf16, N, M, 128, 128);   // (split-K stores D directly)
         if (rc != QFP4_OK) return rc;
         return launch_gemm_decode(fmt, mb, ma, md, a, s);
     }
@@ -551,9 +565,8 @@ extern "C" int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K, const void
                             const float *gs_a, const float *gs_b, void *D_bf16, void *workspace,
                             size_t ws_bytes, void *stream)
 {
-    (void)workspace; (void)ws_bytes;
     return gemm_nt_impl(fmt, M, N, K, A_packed, A_sf, B_packed, B_sf, gs_a, gs_b, nullptr, nullptr, D_bf16,
-                        stream);
+                        workspace, ws_bytes, stream);
 }
 
 extern "C" int qfp4_gemm_nt_scaled(int fmt, int64_t M, int64_t N, int64_t K, const void *A_packed,
@@ -562,9 +575,8 @@ extern "C" int qfp4_gemm_nt_scaled(int fmt, int64_t M, int64_t N, int64_t K, con
                                    const float *col_scale, void *D_bf16, void *workspace, size_t ws_bytes,
                                    void *stream)
 {
-    (void)workspace; (void)ws_bytes;
     return gemm_nt_impl(fmt, M, N, K, A_packed, A_sf, B_packed, B_sf, gs_a, gs_b, row_scale, col_scale,
-                        D_bf16, stream);
+                        D_bf16, workspace, ws_bytes, stream);
 }
 
 static int gemm_nt_grouped_impl(int fmt, int64_t groups, const int32_t *row_offsets, int64_t total_rows,

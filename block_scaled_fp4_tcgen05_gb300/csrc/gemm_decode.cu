@@ -27,6 +27,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <mutex>
 
 #include "qfp4_common.cuh"
 #include "qfp4_gemm_internal.cuh"
@@ -93,7 +94,62 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&pr);
 }
 
-template <int FMT>
+// Split-K reduction of one weight tile's 128 rows (this CTA's rank) over
+// the S CTAs that computed its K ranges: this CTA (split `split`) sums
+// columns [split * 128/S, +128/S) of all S fp32 partials in split order
+// 0..S-1 (the same order whichever CTA runs it, so results repeat bit for
+// bit), applies the epilogue scales, rounds to BF16 and writes them to D,
+// where they are columns col0.. of token rows 0..M-1.  A partial is
+// [mpad tokens][128 weight rows] fp32, written by other SMs, so the loads
+// bypass L1; each thread takes four neighbouring weight rows of one token
+// and writes them as one 8-byte piece of a D row.
+template <int S>
+__device__ __forceinline__ void decode_reduce_slice(const float *part0, size_t part_stride, int split, int M,
+                                                    float gs, const float *row_scale, const float *col_scale,
+                                                    int col0, __nv_bfloat16 *D, int ldd)
+{
+    constexpr int R = 128 / S;               // weight rows (D columns) of the slice
+    constexpr int V = R / 4;                 // float4 per token in the slice
+    constexpr int U = 16 / S;                // float4 positions per thread per round (16 loads in flight)
+    const int nvec = M * V;
+    const float *src0 = part0 + split * R;
+    for (int f0 = threadIdx.x; f0 < nvec; f0 += U * kThreads) {
+        float4 v[S][U];
+#pragma unroll
+        for (int q = 0; q < S; ++q)
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int f = f0 + u * kThreads;
+                const int t = f / V, c = f - t * V;
+                v[q][u] = f < nvec ? __ldcg(reinterpret_cast<const float4 *>(src0 + q * part_stride + t * 128) + c)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int f = f0 + u * kThreads;
+            if (f >= nvec) break;
+            float4 a = v[0][u];
+#pragma unroll
+            for (int q = 1; q < S; ++q) {
+                a.x = __fadd_rn(a.x, v[q][u].x);
+                a.y = __fadd_rn(a.y, v[q][u].y);
+                a.z = __fadd_rn(a.z, v[q][u].z);
+                a.w = __fadd_rn(a.w, v[q][u].w);
+            }
+            const int t = f / V, n = col0 + 4 * (f - t * V);     // token row of D, first D column
+            const float g = row_scale ? gs * row_scale[t] : gs;
+            float o[4] = {a.x * g, a.y * g, a.z * g, a.w * g};
+            if (col_scale) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[i] = o[i] * col_scale[n + i];
+            }
+            *reinterpret_cast<uint2 *>(D + static_cast<size_t>(t) * ldd + n) =
+                make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
+        }
+    }
+}
+
+template <int FMT, bool SPLITK>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT,
                    const __grid_constant__ CUtensorMap tmD, const GemmParams p)
@@ -115,11 +171,19 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
-    const int32_t pair = blockIdx.x >> 1;
     const int K = p.K;
     const int kc = (K / C::G) / 4;
     const int kblocks = (K + 255) / 256;
-    const int32_t wtile = 2 * pair + static_cast<int32_t>(rank);   // this CTA's 128-row weight tile
+    // split-K: pair = split * pair_tiles + pair tile; split s owns K-blocks
+    // [s * kblocks / S, (s + 1) * kblocks / S) (at least one: S <= kblocks)
+    const int32_t pair_tiles = (p.N + 255) / 256;
+    const int32_t pair = blockIdx.x >> 1;
+    const int32_t ptile = SPLITK ? pair % pair_tiles : pair;
+    const int split = SPLITK ? pair / pair_tiles : 0;
+    const int nsplit = SPLITK ? p.splits : 1;
+    const int kb_begin = SPLITK ? (split * kblocks) / nsplit : 0;
+    const int nkb = SPLITK ? ((split + 1) * kblocks) / nsplit - kb_begin : kblocks;
+    const int32_t wtile = 2 * ptile + static_cast<int32_t>(rank);   // this CTA's 128-row weight tile
     const bool w_valid = wtile < p.N / 128;
 
     if (threadIdx.x == 0) {
@@ -152,8 +216,13 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     // everything above overlaps the previous kernel's tail; global memory
     // is touched only from here on
     pdl_wait();
+    // (the next kernel launches only once every CTA of this grid has passed
+    // this point, so all of them are resident before any waits on another
+    // in the split-K reduction)
     pdl_launch_dependents();
 
+    // j counts this CTA's K-blocks (ring slots and phases), kb = kb_begin + j
+    // is the K-block's position in K
     if (warp == 0 || warp == 3) {
         // ------------------------------------------------ weight (warp 0) / token (warp 3) TMA producers
         // (two issuing warps: the copy engine serves one issuing thread's
@@ -162,9 +231,10 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             const bool is_w = warp == 0;
             const uint32_t full0_leader = mapa_shared(smem_u32(&full[0]), 0);
             bool ok = true;
-            for (int kb = 0; kb < kblocks; ++kb) {
-                const uint32_t s = kb % SAB;
-                if (!mbar_wait(smem_u32(&empty[s]), ((kb / SAB) & 1) ^ 1)) { ok = false; break; }
+            for (int j = 0; j < nkb; ++j) {
+                const int kb = kb_begin + j;
+                const uint32_t s = j % SAB;
+                if (!mbar_wait(smem_u32(&empty[s]), ((j / SAB) & 1) ^ 1)) { ok = false; break; }
                 const uint32_t dst = smem_u32(smem + s * C::AB_BYTES);
                 const uint32_t fb = full0_leader + s * 8;
                 if (is_w) {
@@ -182,9 +252,10 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         if (lane == 0) {
             const uint8_t *sfw_g = p.B_sf + static_cast<size_t>(wtile) * kc * 512;
             bool ok = true;
-            for (int kb = 0; kb < kblocks; ++kb) {
-                const uint32_t s = kb % SSF;
-                if (!mbar_wait(smem_u32(&sf_empty[s]), ((kb / SSF) & 1) ^ 1)) { ok = false; break; }
+            for (int j = 0; j < nkb; ++j) {
+                const int kb = kb_begin + j;
+                const uint32_t s = j % SSF;
+                if (!mbar_wait(smem_u32(&sf_empty[s]), ((j / SSF) & 1) ^ 1)) { ok = false; break; }
                 const int chunks = min(C::CPS, kc - kb * C::CPS);
                 const uint32_t bar = smem_u32(&sf_full[s]);
                 mbar_arrive_expect_tx(bar, (w_valid ? 2 : 1) * chunks * 512);
@@ -203,7 +274,8 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             constexpr uint64_t kStageDesc = static_cast<uint64_t>(C::AB_BYTES >> 4);
             bool ok = true;
             uint32_t s = 0, phase = 0;
-            for (int kb = 0; kb < kblocks; ++kb) {
+            for (int j = 0; j < nkb; ++j) {
+                const int kb = kb_begin + j;
                 if (!mbar_wait(smem_u32(&full[s]), phase)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t wd = w_desc0 + s * kStageDesc;
@@ -212,7 +284,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 const uint32_t sft_t = sfw_t + C::SFW_COLS;
                 const int ksteps = min(4, (K - kb * 256) / 64);
                 for (int kk = 0; kk < ksteps; ++kk) {
-                    const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                    const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
                     if (FMT == QFP4_NVFP4) {
                         constexpr uint32_t id = idesc_block_scaled(256, kTok, false, 0, 0);
                         tc_mma_nvf4_pair(tmem_base, wd + 2 * kk, td + 2 * kk, id, sfw_t + kk * 4, sft_t + kk * 4,
@@ -244,10 +316,10 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         // tile is written in full and the weight word q into all four
         // columns.  The shared-memory slot is handed back only after the
         // values reached tensor memory.
-        for (int kb = set; kb < kblocks; kb += 2) {
-            const uint32_t s = kb % SSF, slot = kb % SAB;
+        for (int j = set; j < nkb; j += 2) {
+            const uint32_t s = j % SSF, slot = j % SAB;
             int got = __shfl_sync(0xffffffffu,
-                                  lane == 0 ? (mbar_wait(smem_u32(&sf_full[s]), (kb / SSF) & 1) ? 1 : 0) : 0, 0);
+                                  lane == 0 ? (mbar_wait(smem_u32(&sf_full[s]), (j / SSF) & 1) ? 1 : 0) : 0, 0);
             if (!got) { ok = false; break; }
             const uint8_t *sf_s = smem + C::OFF_SF + s * C::SF_BYTES;
             uint32_t vw[C::SFW_COLS];
@@ -261,7 +333,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 vt[4 * c + 0] = t4.x; vt[4 * c + 1] = t4.y; vt[4 * c + 2] = t4.z; vt[4 * c + 3] = t4.w;
             }
             got = __shfl_sync(0xffffffffu,
-                              lane == 0 ? (mbar_wait(smem_u32(&empty[slot]), ((kb / SAB) & 1) ^ 1) ? 1 : 0) : 0, 0);
+                              lane == 0 ? (mbar_wait(smem_u32(&empty[slot]), ((j / SAB) & 1) ^ 1) ? 1 : 0) : 0, 0);
             if (!got) { ok = false; break; }
             tc_fence_after();
             const uint32_t col = tmem_base + C::COL_SF + slot * C::SLOT_COLS;
@@ -275,13 +347,42 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 mbar_arrive_cluster_relaxed(ready0_leader + slot * 8);
             }
         }
+        if (SPLITK && set == 0) {
+        // -------------------------------------------- split-K: partial sums out
+        // Lane 32q + i is weight row n = 32q + i of this CTA and holds tokens
+        // 32j .. 32j+31 of chunk j; partial[t][n] is stored token by token,
+        // so each warp store fills one 128-byte line.
+        const int got = ok ? __shfl_sync(0xffffffffu,
+                                         lane == 0 ? (mbar_wait(smem_u32(acc_full), 0) ? 1 : 0) : 0, 0)
+                           : 0;
+        if (got && w_valid) {
+            tc_fence_after();
+            const int nchunks = (p.M + 31) / 32;
+            const int mpad = nchunks * 32;
+            const int n = quad * 32 + lane;
+            float *dst = p.ws_partial +
+                         ((static_cast<size_t>(ptile) * nsplit + split) * 2 + rank) * (128u * mpad) + n;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+            for (int j = 0; j < nchunks; ++j) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(taddr + j * 32, v);
+                tmem_ld_wait();
+                tmem_regs_after_wait(v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) dst[(j * 32 + i) * 128] = __uint_as_float(v[i]);
+            }
+        } else if (!got && lane == 0) {
+            record_timeout();
+            *abort_flag = 1;
+        }
+        }
+        if (!SPLITK && set == 0) {
         // -------------------------------------------- accumulator drain
         // Lane 32q + i of tensor memory is weight row n = 32q + i of this
         // CTA; column m is token m.  Each thread writes D[m][n] for its n
         // into a row-major [128 tokens][128 columns] BF16 tile in shared
         // memory (a warp writes 64 consecutive bytes per token), and one
         // TMA store moves the tile to D; rows m >= M are clipped by it.
-        if (set == 0) {
         // two-level epilogue: D[m][n] = bf16((acc * (gs * row_scale[m])) *
         // col_scale[n]); here n is this lane's weight row and the tokens m
         // are the columns, so the column scale is per lane and lane i holds
@@ -344,8 +445,66 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         if (warp == 4 && lane == 0 && !*abort_flag && w_valid) {
             tma_store_2d(&tmD, smem_u32(smem), wtile * 128, 0);
             bulk_commit_group();
-            bulk_wait_group<0>();
+            // the staging tile must outlive the copy engine's reads of it;
+            // the writes themselves complete with the grid
+            bulk_wait_group_read<0>();
         }
+        }
+    }
+
+    if constexpr (SPLITK) {
+        // ---- split-K reduction.  The S CTAs holding this CTA's rank of the
+        // same weight tile meet at a sense-reversing barrier in the
+        // workspace: an arrival count and a generation word.  Each reads the
+        // generation, adds 1 to the count once its partial is out (release);
+        // the last arrival sets the count back to 0 and advances the
+        // generation, and the others wait (acquire, bounded) for that.  Every
+        // call thus leaves the counts at 0, whatever S the next call uses.
+        // All S CTAs are resident: the launch is sized to fit the GPU's
+        // clusters at once, and nothing after this kernel can take an SM
+        // before all of them started.
+        __shared__ int s_go;
+        __syncwarp();
+        __syncthreads();
+        uint32_t *cnt = p.ws_count + 2 * (2 * ptile + rank);
+        uint32_t *gen = cnt + 1;
+        if (threadIdx.x == 0) {
+            int go = (!*abort_flag && w_valid) ? 1 : 0;
+            if (go) {
+                const uint32_t g = ld_acquire_gpu(gen);
+                if (atom_add_acq_rel_gpu(cnt, 1u) == static_cast<uint32_t>(nsplit) - 1u) {
+                    st_relaxed_gpu(cnt, 0u);
+                    st_release_gpu(gen, g + 1u);
+                } else {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (ld_acquire_gpu(gen) == g) {
+                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                            go = 0;
+                            record_timeout();
+                            *abort_flag = 1;
+                            break;
+                        }
+                    }
+                }
+            }
+            s_go = go;
+        }
+        __syncthreads();
+        if (s_go) {
+            const int mpad = ((p.M + 31) / 32) * 32;
+            const size_t part_stride = 2u * 128u * mpad;                  // floats from split q to q + 1
+            const float *part0 = p.ws_partial + (static_cast<size_t>(ptile) * nsplit * 2 + rank) * (128u * mpad);
+            float gs = 1.0f;
+            if (FMT == QFP4_NVFP4) gs = (p.gs_a ? *p.gs_a : 1.0f) * (p.gs_b ? *p.gs_b : 1.0f);
+            const int col0 = wtile * 128 + split * (128 / nsplit);
+            switch (nsplit) {
+            case 2: decode_reduce_slice<2>(part0, part_stride, split, p.M, gs, p.row_scale, p.col_scale, col0,
+                                           p.D, p.N); break;
+            case 4: decode_reduce_slice<4>(part0, part_stride, split, p.M, gs, p.row_scale, p.col_scale, col0,
+                                           p.D, p.N); break;
+            default: decode_reduce_slice<8>(part0, part_stride, split, p.M, gs, p.row_scale, p.col_scale, col0,
+                                            p.D, p.N); break;
+            }
         }
     }
 
@@ -366,17 +525,17 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     }
 }
 
-template <int FMT>
+template <int FMT, bool SPLITK>
 int launch_decode(const CUtensorMap &mw, const CUtensorMap &mt, const CUtensorMap &md, const GemmParams &g,
                   cudaStream_t s)
 {
     using C = DecCfg<FMT>;
-    auto kern = gemm_decode_kernel<FMT>;
+    auto kern = gemm_decode_kernel<FMT, SPLITK>;
     {
         const int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM);
         if (rc != QFP4_OK) return rc;
     }
-    const int pairs = (g.N + 255) / 256;
+    const int pairs = ((g.N + 255) / 256) * (SPLITK ? g.splits : 1);
     return launch_status(launch_pdl(kern, dim3(2 * pairs), dim3(kThreads), C::SMEM, s, mw, mt, md, g));
 }
 
@@ -385,8 +544,78 @@ int launch_decode(const CUtensorMap &mw, const CUtensorMap &mt, const CUtensorMa
 int launch_gemm_decode(int fmt, const CUtensorMap &mw, const CUtensorMap &mt, const CUtensorMap &md,
                        const GemmParams &g, cudaStream_t s)
 {
-    return fmt == QFP4_NVFP4 ? launch_decode<QFP4_NVFP4>(mw, mt, md, g, s)
-                             : launch_decode<QFP4_MXFP4>(mw, mt, md, g, s);
+    if (g.splits > 1)
+        return fmt == QFP4_NVFP4 ? launch_decode<QFP4_NVFP4, true>(mw, mt, md, g, s)
+                                 : launch_decode<QFP4_MXFP4, true>(mw, mt, md, g, s);
+    return fmt == QFP4_NVFP4 ? launch_decode<QFP4_NVFP4, false>(mw, mt, md, g, s)
+                             : launch_decode<QFP4_MXFP4, false>(mw, mt, md, g, s);
+}
+
+// Clusters of this kernel the current device holds at once (queried once
+// per device; the split-K grid must fit, since its CTAs wait on each other).
+static int decode_max_clusters()
+{
+    static std::mutex mu;
+    static int cached[64];
+    static bool have[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev]) {
+        using C = DecCfg<QFP4_NVFP4>;
+        static_assert(DecCfg<QFP4_MXFP4>::SMEM <= C::SMEM, "the NVFP4 kernel bounds both");
+        auto kern = gemm_decode_kernel<QFP4_NVFP4, true>;
+        int n = 0;
+        if (ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM) == QFP4_OK) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = C::SMEM;
+            if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void *>(kern), &cfg) != cudaSuccess) {
+                n = 0;
+                cudaGetLastError();
+            }
+        }
+        cached[dev] = n;
+        have[dev] = true;
+    }
+    return cached[dev];
+}
+
+// Split-K pays only when it removes enough K-blocks from each pair: the
+// partials' trip through L2 (write, the barrier, the reduction) costs about
+// as much as streaming 12-13 K-blocks (traced on GB300: ~4.5 us against
+// ~0.36 us per 256-K block), so a split must save at least 16 of them.
+constexpr int kSplitMinSavedKBlocks = 16;
+
+int decode_splits(int64_t M, int64_t N, int64_t K)
+{
+    if (M < 1 || M > 128 || N < 128 || K < 256) return 1;
+    const int64_t pair_tiles = (N + 255) / 256, kblocks = (K + 255) / 256;
+    const int sms = sm_count();
+    int64_t cap = sms / 2;
+    const int clusters = decode_max_clusters();
+    if (clusters > 0 && clusters < cap) cap = clusters;
+    for (int s : {8, 4, 2})
+        if (pair_tiles * s <= cap && s <= kblocks && kblocks - (kblocks + s - 1) / s >= kSplitMinSavedKBlocks)
+            return s;
+    return 1;
+}
+
+size_t decode_counter_bytes(int64_t N)
+{
+    // an arrival count and a generation word per (pair tile, CTA rank)
+    const size_t pair_tiles = static_cast<size_t>((N + 255) / 256);
+    return (pair_tiles * 2 * 2 * sizeof(uint32_t) + 255) / 256 * 256;
+}
+
+size_t decode_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits)
+{
+    (void)K;
+    if (splits <= 1) return 0;
+    const size_t pair_tiles = static_cast<size_t>((N + 255) / 256);
+    const size_t mpad = static_cast<size_t>((M + 31) / 32) * 32;
+    return decode_counter_bytes(N) + pair_tiles * splits * 2 * 128 * mpad * sizeof(float);
 }
 
 }  // namespace qfp4

@@ -34,6 +34,13 @@ struct GemmParams {
     // grouped launches: upper bound on any group's rows (0 = no bound); the
     // kernels check the offsets against it and against M (= total rows)
     int32_t max_group_rows;
+    // decode split-K (launch_gemm_decode with splits > 1): K is cut into
+    // `splits` ranges, one per CTA pair of a weight tile; the fp32 partial
+    // sums go to ws_partial and ws_count holds an arrival count (zero
+    // between calls) and a generation word per (weight tile pair, CTA rank)
+    int32_t splits;
+    uint32_t *ws_count;
+    float *ws_partial;
 };
 
 // 2D byte matrix [rows, inner] tensor map with 128-byte swizzle and a box of
@@ -66,9 +73,18 @@ int read_clear_status_gemm_pair(cudaStream_t s, uint32_t *out);
 // Decode GEMM for M <= 128 (N % 128 == 0), swap AB on CTA pairs: the
 // weights (B, map mw with 128-row boxes) fill the MMA's M slot, the tokens
 // (A, map mt with 64-row boxes) its N slot; D is written through md (BF16,
-// 128 x 128 boxes, no swizzle).
+// 128 x 128 boxes, no swizzle), or directly from registers with split-K.
+// g.splits > 1 selects split-K (g.ws_count and g.ws_partial set, sized by
+// decode_workspace_bytes).
 int launch_gemm_decode(int fmt, const CUtensorMap &mw, const CUtensorMap &mt, const CUtensorMap &md,
                        const GemmParams &g, cudaStream_t s);
+// Split count the decode kernel uses for this shape on the current device
+// (1, 2, 4 or 8; 1 = no split-K and no workspace), and the workspace bytes
+// it then needs: an arrival count and a generation word (32-bit) per (pair
+// tile, CTA) in the first 256-byte aligned block, then the fp32 partials [pairs][splits][2][ceil32(M)][128].
+int decode_splits(int64_t M, int64_t N, int64_t K);
+size_t decode_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits);
+size_t decode_counter_bytes(int64_t N);
 // 2D BF16 matrix [rows, cols] (row stride cols * 2 bytes), box of
 // box_cols x box_rows elements, no swizzle: the TMA store map of D.
 int make_map_bf16(CUtensorMap *map, void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,

@@ -15,8 +15,9 @@
  *     re-interleave of rank-2 scale factors into the 5D TCGEN layout, and the
  *     grouped per-expert quantiser and matmul.
  *   "quadbit" README, "End-to-end serving": the decode GEMM at small M (the
- *     page fills the GPU with split-K; this library needs none, see
- *     qfp4_gemm_nt) and the one-launch segmented MoE kernel.
+ *     page fills the GPU with split-K; here the weights' CTA pairs are split
+ *     over K when that pays, see qfp4_gemm_nt) and the one-launch segmented
+ *     MoE kernel.
  *
  * Conventions for every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller; the library
@@ -217,10 +218,14 @@ int qfp4_sf_interleave(const void *SF_in, int64_t rows, int64_t cols, void *SF_o
 /* GEMM                                                                     */
 /* ---------------------------------------------------------------------- */
 
-/* Workspace bytes qfp4_gemm_nt uses for this shape.  Every kernel keeps its
- * partial sums on chip (tensor memory), so this is 0; the argument is kept
- * so that a caller written against it needs no change if a future kernel
- * uses scratch. */
+/* Workspace bytes qfp4_gemm_nt and qfp4_gemm_nt_scaled use for this shape
+ * on the current device: 0 unless M <= 128 and the decode kernel splits K
+ * (quadbit README, "End-to-end serving": split-K fills the GPU at decode).
+ * It splits K over S = 2, 4 or 8 CTA pairs per 256 weight rows when
+ * ceil(N/256) * S pairs fit on the GPU at once and each pair then streams
+ * at least 16 fewer 256-K blocks; the workspace then holds an arrival count
+ * and a generation word per 128 weight rows (first 256-byte block) and the
+ * fp32 partial sums, ceil(N/256) * S * 2 * 128 * ceil32(M) floats. */
 size_t qfp4_gemm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K);
 
 /* D[M,N] (BF16, row-major) = bf16_rne(gs_a * gs_b * sum_k a[m,k] * b[n,k]),
@@ -229,14 +234,22 @@ size_t qfp4_gemm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K);
  *   A_packed  [M, K/2] bytes, K-major;  A_sf  MMA layout for [M, K/g]
  *   B_packed  [N, K/2] bytes, K-major;  B_sf  MMA layout for [N, K/g]
  *   gs_a, gs_b DEVICE pointers to one fp32 each (NULL = 1.0; MXFP4 ignores)
- *   workspace  DEVICE scratch of ws_bytes >= qfp4_gemm_workspace_bytes(...);
- *              currently unused (NULL is fine).
+ *   workspace  DEVICE scratch, 16-byte aligned, of ws_bytes >=
+ *              qfp4_gemm_workspace_bytes(...), ZERO-FILLED before its first
+ *              use; every call leaves its arrival counts at zero again, so
+ *              it is reused as it is (re-zero it after a reported timeout).
+ *              One call at a time per workspace: calls that overlap on the
+ *              GPU race on it.  NULL or a smaller one makes the decode
+ *              kernel run without split-K (same result bounds, slower).
  * Tensor cores: tcgen05.mma kind::mxf4 (MXFP4) / kind::mxf4nvf4 scale_vec::4X
  * (NVFP4), fp32 accumulation in tensor memory.  Kernels: M <= 128: CTA
  * pairs with A and B swapped (256 weight rows per pair in the MMA's M slot,
- * the tokens in its N slot, all of K per pair, no split-K); M > 128 and
- * N % 256 == 0: CTA pairs (cta_group::2) on 256 x 256 tiles; otherwise
- * single-CTA 128 x 128 tiles.
+ * the tokens in its N slot), each pair over all of K or, with split-K, over
+ * its K range, the partials summed in a fixed order (results repeat bit for
+ * bit; the split CTAs wait on each other, so the call expects the GPU's SMs
+ * to be free for it at once, as other work on the stream leaves them);
+ * M > 128 and N % 256 == 0: CTA pairs (cta_group::2) on 256 x 256 tiles;
+ * otherwise single-CTA 128 x 128 tiles.
  * Requirements: N % 128 == 0, K % 128 == 0, all pointers 16-byte aligned.
  * Degenerate shapes: M == 0 or N == 0 returns QFP4_OK with nothing launched
  * (no pointer is read); K == 0 is an empty sum and writes D = 0.

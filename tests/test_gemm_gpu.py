@@ -255,18 +255,53 @@ def test_grouped_moe_up_projection():
 
 # ----------------------------------------------------------------- decode (M <= 128)
 
+def expected_splits(M, N, K):
+    """The split count the decode kernel picks: the largest of 8, 4, 2 with
+    ceil(N/256) * S CTA pairs on the GPU at once, S <= ceil(K/256), and at
+    least 16 of the ceil(K/256) K-blocks taken off each pair."""
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    tiles, kblocks = -(-N // 256), -(-K // 256)
+    if M > 128 or K < 256:
+        return 1
+    for s in (8, 4, 2):
+        if tiles * s <= pairs and s <= kblocks and kblocks - -(-kblocks // s) >= 16:
+            return s
+    return 1
+
+
+def decode_workspace(fmt, M, N, K):
+    """Zero-filled workspace for the decode split-K (None when it needs none)."""
+    ws_bytes = qfp4.gemm_workspace_bytes(fmt, M, N, K)
+    splits = expected_splits(M, N, K)
+    if splits == 1:
+        assert ws_bytes == 0
+        return None, 0
+    tiles, mpad = -(-N // 256), -(-M // 32) * 32
+    counters = -(-(tiles * 2 * 2 * 4) // 256) * 256        # (count, generation) per pair tile and CTA
+    assert ws_bytes == counters + tiles * splits * 2 * 128 * mpad * 4
+    return torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda"), ws_bytes
+
+
 @pytest.mark.parametrize("fmt", [MX, NV])
 @pytest.mark.parametrize("M,N,K", [(1, 128, 256), (37, 384, 1024), (128, 1024, 4096), (100, 2048, 2304),
-                                   (128, 4096, 128), (64, 256, 8192)])
+                                   (128, 4096, 128), (64, 256, 8192), (128, 4096, 512), (77, 1024, 5120),
+                                   (64, 256, 4736), (33, 640, 5248), (128, 4096, 14336), (5, 384, 16384),
+                                   (128, 2048, 8192)])
 def test_decode_shapes(fmt, M, N, K):
     """M <= 128 runs the decode kernel (A and B swapped on CTA pairs; ragged
     token counts, a weight tile of only 128 rows, and a trailing half K-block
-    among the shapes): must match the oracle and be bit-identical across
-    repeated calls."""
+    among the shapes), with K split over 2, 4 or 8 CTA pairs per weight tile
+    when that saves enough K-blocks and a workspace is given: S = 8 at
+    77 x 1024 x 5120 (ranges of 2 and 3 K-blocks), 64 x 256 x 4736 (the half
+    K-block in the last range), 33 x 640 x 5248 (an empty second weight tile
+    in the last pair), 5 x 384 x 16384, 64 x 256 x 8192 and 128 x 2048 x 8192;
+    S = 4 at 128 x 4096 x 14336; one range for the rest.
+    Both paths must match the oracle, and each must be bit-identical across
+    repeated calls (the split partials are summed in a fixed order)."""
     A, Asf, B, Bsf = random_operands(fmt, M, N, K, M + N + K + 3 * fmt)
     gs_a, gs_b = (None, None) if fmt == MX else (0.125, 3.0)
     g = qfp4.block_size(fmt)
-    assert qfp4.gemm_workspace_bytes(fmt, M, N, K) == 0
+    ws, ws_bytes = decode_workspace(fmt, M, N, K)
     dA, dB = to_dev_u8(A), to_dev_u8(B)
     sfa = torch.zeros(qfp4.sf_mma_bytes(M, K // g), dtype=torch.uint8, device="cuda")
     sfb = torch.zeros(qfp4.sf_mma_bytes(N, K // g), dtype=torch.uint8, device="cuda")
@@ -274,16 +309,55 @@ def test_decode_shapes(fmt, M, N, K):
     qfp4.sf_interleave(to_dev_u8(Bsf), N, K // g, sfb, qfp4.SF_MMA)
     ga = dev_scalar(gs_a) if gs_a else None
     gb = dev_scalar(gs_b) if gs_b else None
-    outs = []
-    for _ in range(3):
-        D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-        qfp4.gemm_nt(fmt, M, N, K, dA, sfa, dB, sfb, ga, gb, D)
-        torch.cuda.synchronize()
-        outs.append(bf16_to_f64(D))
-    assert qfp4.poll_device_status() == 0
-    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
     d_ref, t_ref = oracle.gemm_nt(fmt, A, Asf, B, Bsf, gs_a or 1.0, gs_b or 1.0)
-    assert_gemm_close(outs[0], d_ref, t_ref, f"decode {M}x{N}x{K}")
+    paths = [(None, 0)] + ([(ws, ws_bytes)] if ws is not None else [])
+    for w, wb in paths:
+        outs = []
+        for _ in range(3):
+            D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            qfp4.gemm_nt(fmt, M, N, K, dA, sfa, dB, sfb, ga, gb, D, w, wb)
+            torch.cuda.synchronize()
+            outs.append(bf16_to_f64(D))
+        assert qfp4.poll_device_status() == 0
+        what = f"decode {M}x{N}x{K} {'split-K' if w is not None else 'one range'}"
+        assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2]), what
+        assert_gemm_close(outs[0], d_ref, t_ref, what)
+    if ws is not None:
+        # every call leaves the arrival counts at zero for the next one; the
+        # generation word beside each count advanced once per call (3 calls)
+        # for the 128-row weight tiles that exist (N % 256 == 128 leaves the
+        # last pair's second tile empty)
+        words = ws[:-(-N // 256) * 2 * 2 * 4].view(torch.int32).cpu().numpy()
+        assert not words[0::2].any()
+        tiles_exist = np.arange(words.size // 2) < N // 128
+        assert np.array_equal(words[1::2], np.where(tiles_exist, 3, 0))
+
+
+@pytest.mark.parametrize("fmt", [MX, NV])
+def test_decode_split_k_two_level(fmt):
+    """The split-K reduction applies the two-level epilogue (row scale per
+    token, column scale per weight row) like the single-range drain."""
+    M, N, K = 96, 2048, 8192
+    A, Asf, B, Bsf = random_operands(fmt, M, N, K, 4242 + fmt)
+    g = qfp4.block_size(fmt)
+    ws, ws_bytes = decode_workspace(fmt, M, N, K)
+    assert ws is not None
+    gen = synth.rng(77 + fmt)
+    rs = (2.0 ** gen.integers(-3, 4, M)).astype(np.float32) * np.float32(1.25)
+    cs = (2.0 ** gen.integers(-3, 4, N)).astype(np.float32) * np.float32(0.75)
+    sfa = torch.zeros(qfp4.sf_mma_bytes(M, K // g), dtype=torch.uint8, device="cuda")
+    sfb = torch.zeros(qfp4.sf_mma_bytes(N, K // g), dtype=torch.uint8, device="cuda")
+    qfp4.sf_interleave(to_dev_u8(Asf), M, K // g, sfa, qfp4.SF_MMA)
+    qfp4.sf_interleave(to_dev_u8(Bsf), N, K // g, sfb, qfp4.SF_MMA)
+    ga, gb = (dev_scalar(0.5), dev_scalar(1.5)) if fmt == NV else (None, None)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    qfp4.gemm_nt_scaled(fmt, M, N, K, to_dev_u8(A), sfa, to_dev_u8(B), sfb, ga, gb,
+                        torch.from_numpy(rs).cuda(), torch.from_numpy(cs).cuda(), D, ws, ws_bytes)
+    torch.cuda.synchronize()
+    assert qfp4.poll_device_status() == 0
+    d_ref, t_ref = oracle.gemm_nt(fmt, A, Asf, B, Bsf, 0.5 if fmt == NV else 1.0, 1.5 if fmt == NV else 1.0,
+                                  row_scale=rs, col_scale=cs)
+    assert_gemm_close(bf16_to_f64(D), d_ref, t_ref, "split-K two-level")
 
 
 # ----------------------------------------------------------------- grouped vs dense

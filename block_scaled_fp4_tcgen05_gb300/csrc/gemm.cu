@@ -579,6 +579,55 @@ extern "C" int qfp4_gemm_nt_scaled(int fmt, int64_t M, int64_t N, int64_t K, con
                         D_bf16, workspace, ws_bytes, stream);
 }
 
+// ---------------------------------------------------------------------------
+// qfp4_gemm_nt_noalloc: qfp4_gemm_nt for callers that cannot allocate device
+// memory.  The scratch the decode split-K needs lives in this file-scope
+// array instead of a caller-provided workspace.  Every GPU that loads the
+// library holds the array until the process exits; every call shares it.
+constexpr size_t kNoAllocScratchBytes = (size_t{8} << 20) + 4096;   // 8 MiB of partial sums + 4 KiB of counters
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name is only a stand-in for the symbol, never an address a
+// kernel may be given, so the address is asked of the runtime: once per
+// device, with that device current, cached behind a mutex.
+static int noalloc_scratch_address(void **out)
+{
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static void *addr[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QFP4_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return QFP4_ERR_CUDA;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return QFP4_OK;
+}
+
+extern "C" int qfp4_gemm_nt_noalloc(int fmt, int64_t M, int64_t N, int64_t K, const void *A_packed,
+                                    const void *A_sf, const void *B_packed, const void *B_sf,
+                                    const float *gs_a, const float *gs_b, void *D_bf16, void *stream)
+{
+    const size_t need = qfp4_gemm_workspace_bytes(fmt, M, N, K);
+    if (need > kNoAllocScratchBytes) return QFP4_ERR_WORKSPACE;
+    if (need == 0)
+        return gemm_nt_impl(fmt, M, N, K, A_packed, A_sf, B_packed, B_sf, gs_a, gs_b, nullptr, nullptr, D_bf16,
+                            nullptr, 0, stream);
+    void *scratch = nullptr;
+    const int rc = noalloc_scratch_address(&scratch);
+    if (rc != QFP4_OK) return rc;
+    // the arrival counts must start at zero; the array keeps whatever the
+    // last call (or one that timed out) left there
+    if (cudaMemsetAsync(scratch, 0, decode_counter_bytes(N), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return QFP4_ERR_CUDA;
+    return gemm_nt_impl(fmt, M, N, K, A_packed, A_sf, B_packed, B_sf, gs_a, gs_b, nullptr, nullptr, D_bf16,
+                        scratch, kNoAllocScratchBytes, stream);
+}
+
 static int gemm_nt_grouped_impl(int fmt, int64_t groups, const int32_t *row_offsets, int64_t total_rows,
                                 int64_t max_group_rows, int64_t N, int64_t K, const void *A_packed,
                                 const void *A_sf, const void *B_packed, const void *B_sf, const float *gs_a,

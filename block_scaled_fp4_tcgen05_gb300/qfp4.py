@@ -53,6 +53,7 @@ SIGNATURES = {
     "qfp4_sf_interleave": (_i32, [_vp, _i64, _i64, _vp, _i32, _vp]),
     "qfp4_gemm_workspace_bytes": (_sz, [_i32, _i64, _i64, _i64]),
     "qfp4_gemm_nt": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "qfp4_gemm_nt_noalloc": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "qfp4_gemm_nt_grouped": (_i32, [_i32, _i64, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                     _vp, _vp, _vp, _vp, _sz, _vp]),
 }

@@ -260,6 +260,30 @@ int qfp4_gemm_nt(int fmt, int64_t M, int64_t N, int64_t K,
                  const float *gs_a, const float *gs_b,
                  void *D_bf16, void *workspace, size_t ws_bytes, void *stream);
 
+/* qfp4_gemm_nt for callers that cannot allocate device memory: code that runs
+ * under a fixed device-memory budget planned ahead of time, or inside a host
+ * framework whose allocator must own every allocation, and so can neither
+ * call cudaMalloc nor hand over a workspace.  (It has no counterpart in the
+ * pages: it only changes where the decode split-K keeps its scratch.)
+ * Same arguments, result and accuracy as qfp4_gemm_nt without the workspace
+ * pair.  The scratch is a static device array of 8 MiB + 4 KiB inside this
+ * library, which every GPU that loads the library holds until the process
+ * exits: room for the partial sums of 64 CTA pairs at 128 tokens.  A shape
+ * whose split-K needs more (qfp4_gemm_workspace_bytes(...) above that size)
+ * is rejected with QFP4_ERR_WORKSPACE before anything is launched; shapes
+ * that need no scratch run as in qfp4_gemm_nt.  The call allocates and frees
+ * nothing.  Its first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Each call that splits K clears the array's
+ * arrival counts on `stream` first.  All calls share the one array, so two
+ * calls whose kernels overlap on the GPU (different streams, no ordering
+ * between them) race on it: order them on one stream. */
+int qfp4_gemm_nt_noalloc(int fmt, int64_t M, int64_t N, int64_t K,
+                         const void *A_packed, const void *A_sf,
+                         const void *B_packed, const void *B_sf,
+                         const float *gs_a, const float *gs_b,
+                         void *D_bf16, void *stream);
+
 /* Two-level epilogue (quadbit README, "Accuracy (real models)": a per-row and
  * per-column fp32 global rescale in the MMA epilogue, the deploy path of
  * NVFP4 with per-row global scales):

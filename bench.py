@@ -470,6 +470,26 @@ def sweep(device, l2_bytes, peaks):
         out.append({"workload": f"{'nv' if fmt else 'mx'}fp4_quantize_{M}x{K}", "us": round(ms * 1e3, 2),
                     "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 3)})
         del X, Q, SF
+    # residual add + RMSNorm + NVFP4 quantisation (per-row global scales) on X[16384, 4096]
+    M, K = synth.QUANT_ROWS, synth.QUANT_COLS
+    X = torch.from_numpy(synth.activations_bf16(synth.QUANT_SEED, M, K).view(np.int16).copy()).view(
+        torch.bfloat16).to(device)
+    R = torch.from_numpy(synth.activations_bf16(synth.QUANT_SEED + 1, M, K).view(np.int16).copy()).view(
+        torch.bfloat16).to(device)
+    gamma = torch.from_numpy(synth.norm_weight_bf16(synth.QUANT_SEED + 2, K).view(np.int16).copy()).view(
+        torch.bfloat16).to(device)
+    Y = torch.empty_like(X)
+    gs_rows = torch.empty(M, dtype=torch.float32, device=device)
+    Q = torch.empty((M, K // 2), dtype=torch.uint8, device=device)
+    SF = torch.empty(qfp4.sf_mma_bytes(M, K // 16), dtype=torch.uint8, device=device)
+    # X, R and Y (400 MB) exceed the L2, so back-to-back launches stream from HBM
+    ms = graph_time([lambda: qfp4.residual_rmsnorm_quantize(qfp4.NVFP4, X, R, gamma, 1e-6, Y, gs_rows, Q, SF,
+                                                            qfp4.SF_MMA)] * 8)
+    byts = 3 * 2 * M * K + M * K / 2 + M * K / 16 + 4 * M
+    gbs = byts / (ms * 1e-3) / 1e9
+    out.append({"workload": f"nvfp4_residual_rmsnorm_quantize_{M}x{K}", "us": round(ms * 1e3, 2),
+                "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 3)})
+    del X, R, gamma, Y, gs_rows, Q, SF
     # the step on the prefill-attention shape 4096^3 (global scale, quantise, GEMM), L2 flushed
     pipe = Pipeline(synth.PREFILL_NV, device)
     flush = Flush(device)

@@ -66,132 +66,11 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float &lo, float &hi)
     hi = __uint_as_float(w & 0xFFFF0000u);
 }
 
-// 2^(127 - c) as fp32 (exact; subnormal for c = 254).
-__device__ __forceinline__ float ue8m0_inverse(uint32_t c)
-{
-    const int e = 127 - static_cast<int>(c);                 // -127 .. 127
-    return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23)
-                     : __uint_as_float(0x00400000u);          // 2^-127
-}
-
-struct BlockScale {
-    float inv;      // MXFP4: exact 2^-e; NVFP4: RN(1/s)
-    float s;        // NVFP4 scale s = decode(sf) * gs
-    uint32_t code;  // scale byte
-    int mode;       // 0: zero block, 1: fast path, 2: IEEE division
-};
-
-// RN(a / b) from y = RN(1 / b) with two fused corrections (Markstein); the
-// caller guarantees a, b and the quotient stay well inside the normal range.
-// The remainder is formed negated, e = b*q - a, and applied as q - e*y: the
-// same values, but a = -0 keeps its sign (-0 - (+0) = -0) where the
-// a - b*q form would turn it into +0.
-__device__ __forceinline__ float div_markstein(float a, float b, float y)
-{
-    float q = __fmul_rn(a, y);
-    q = __fmaf_rn(-__fmaf_rn(b, q, -a), y, q);
-    q = __fmaf_rn(-__fmaf_rn(b, q, -a), y, q);
-    return q;
-}
-
-__device__ __forceinline__ bool normal_range(float v) { return v >= 0x1p-100f && v <= 0x1p100f; }
-
-// t = (amax / 6) / gs, each division correctly rounded.  inv_gs = RN(1/gs).
-__device__ __forceinline__ float scale_target(float amax, float gs, float inv_gs)
-{
-    constexpr float kInv6 = 0x1.555556p-3f;          // RN(1/6)
-    if (normal_range(amax)) {
-        const float t1 = div_markstein(amax, 6.0f, kInv6);
-        if (gs == 1.0f) return t1;
-        if (normal_range(t1) && gs >= 0x1p-60f && gs <= 0x1p60f) return div_markstein(t1, gs, inv_gs);
-        return __fdiv_rn(t1, gs);
-    }
-    return gs == 1.0f ? __fdiv_rn(amax, 6.0f) : __fdiv_rn(__fdiv_rn(amax, 6.0f), gs);
-}
-
-template <int FMT>
-__device__ __forceinline__ BlockScale block_scale(float amax, float gs, float inv_gs)
-{
-    BlockScale b;
-    if (FMT == QFP4_MXFP4) {
-        const float t = scale_target(amax, 1.0f, 1.0f);
-        b.code = ue8m0_encode(t);
-        b.inv = ue8m0_inverse(b.code);
-        b.s = 0.0f;
-        b.mode = 1;
-    } else {
-        const float t = scale_target(amax, gs, inv_gs);
-        // t is NaN only when amax and gs are both 0 (0/0: an all-zero
-        // block under a zero global scale) and then takes code 0 like t = 0;
-        // a non-zero block with gs = 0 has t = +inf and saturates to 0x7E,
-        // and s = 448 * 0 = 0 still encodes it as zeros
-        b.code = t > 0.0f ? ue4m3_encode(t) : 0u;
-        b.s = __fmul_rn(ue4m3_decode(b.code), gs);
-        if (b.s == 0.0f) {
-            b.mode = 0;
-            b.inv = 0.0f;
-        } else {
-            b.inv = __frcp_rn(b.s);
-            const bool fast = b.s >= 0x1p-64f && b.s <= 0x1p64f && amax <= b.s * 0x1p60f;
-            b.mode = fast ? 1 : 2;
-        }
-    }
-    return b;
-}
-
-// ---- packed fp32 pairs: one f32x2 instruction works on both halves of a
-// 64-bit register pair, halving the arithmetic issue slots of the quotient.
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
-{
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-
-__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi)
-{
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
-{
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
-{
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-
 // bf16 pair in a 32-bit word -> both values as one fp32 pair (exact).
 __device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w)
 {
     return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
-
-// RN(-x / s) on both halves of x2, from s2 = (s, s) and ny2 = (-y, -y) with
-// y = RN(1/s): the two Markstein corrections of div_markstein applied to the
-// dividend -x.  q0 = x*(-y) = (-x)*y, e = s*q + x = s*q - (-x) and
-// q + e*(-y) = q - e*y are the same roundings as for -x, so the result is
-// div_markstein(-x, s, y) = -RN(x/s), and no negation is ever issued.  Signed
-// zeros come out right: x = +0 gives -0 and x = -0 gives +0.
-__device__ __forceinline__ uint64_t f2_neg_quotient(uint64_t x2, uint64_t s2, uint64_t ny2)
-{
-    uint64_t q = f2_mul(x2, ny2);
-    uint64_t e = f2_fma(s2, q, x2);
-    q = f2_fma(e, ny2, q);
-    e = f2_fma(s2, q, x2);
-    return f2_fma(e, ny2, q);
-}
-
-// E2M1 rounding is symmetric (round to nearest even, saturation at +-6), so
-// the codes of -q are the codes of q with the sign bit of every nibble set
-// the other way.
-constexpr uint32_t kNibbleSigns = 0x88888888u;
 
 // Largest |x| of a block as fp32 (exact): pairwise max of magnitudes on the
 // packed bf16 words (the sign of the result is meaningless and dropped).
@@ -235,12 +114,6 @@ __device__ __forceinline__ uint32_t encode8(const uint32_t *w, const BlockScale 
         q[2 * i + 1] = __fdiv_rn(__uint_as_float(w[i] & 0xFFFF0000u), b.s);
     }
     return e2m1x8(q);
-}
-
-__device__ __forceinline__ uint32_t sf_mma_offset(uint32_t row_tile, uint32_t r_in_tile, uint32_t c,
-                                                  uint32_t kc)
-{
-    return (row_tile * kc + (c >> 2)) * 512u + (r_in_tile & 31u) * 16u + (r_in_tile >> 5) * 4u + (c & 3u);
 }
 
 // Group of a row (row_offsets sorted; offs has groups+1 entries in smem).

@@ -50,6 +50,8 @@ SIGNATURES = {
     "qfp4_gemm_swiglu_quantize_grouped": (_i32, [_i32, _i64, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp,
                                                  _vp, _vp, _vp, _vp, _vp]),
     "qfp4_quantize_grouped": (_i32, [_i32, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+    "qfp4_residual_rmsnorm_quantize": (_i32, [_i32, _vp, _vp, _vp, _i64, _i64, ctypes.c_float, _vp, _vp, _vp,
+                                              _vp, _i32, _vp]),
     "qfp4_sf_interleave": (_i32, [_vp, _i64, _i64, _vp, _i32, _vp]),
     "qfp4_gemm_workspace_bytes": (_sz, [_i32, _i64, _i64, _i64]),
     "qfp4_gemm_nt": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -192,6 +194,15 @@ def quantize_grouped_rows(fmt, X, row_offsets, gs_rows, Q, SF_mma, stream=None) 
     _check("qfp4_quantize_grouped_rows",
            load().qfp4_quantize_grouped_rows(fmt, _p(X), rows, K, groups, _p(row_offsets), _p(gs_rows), _p(Q),
                                              _p(SF_mma), _stream(stream)))
+
+
+def residual_rmsnorm_quantize(fmt, X, R, gamma, eps, Y, gs_rows, Q, SF, sf_layout=SF_MMA, stream=None) -> None:
+    """y = bf16(X + R) into Y (R and Y may be None), z = RMSNorm(y) * gamma,
+    per-row global scales of z into gs_rows (NVFP4) and z quantised into Q, SF."""
+    M, K = X.shape
+    _check("qfp4_residual_rmsnorm_quantize",
+           load().qfp4_residual_rmsnorm_quantize(fmt, _p(X), _p(R), _p(gamma), M, K, float(eps), _p(Y), _p(gs_rows),
+                                                 _p(Q), _p(SF), sf_layout, _stream(stream)))
 
 
 def sf_interleave(SF_in, rows, cols, SF_out, layout=SF_MMA, stream=None) -> None:

@@ -59,6 +59,11 @@ def weights_bf16(seed: int, rows: int, cols: int) -> np.ndarray:
     return f32_to_bf16_bits(normal_f32(rng(seed), (rows, cols), 0.02))
 
 
+def norm_weight_bf16(seed: int, cols: int) -> np.ndarray:
+    """An RMSNorm weight vector gamma [cols] as bf16: N(1, 0.1)."""
+    return f32_to_bf16_bits(normal_f32(rng(seed), (cols,), 0.1) + np.float32(1.0))
+
+
 def moe_counts(seed: int, tokens: int = 4096, experts: int = 8, topk: int = 2,
                alpha: float = 0.5) -> np.ndarray:
     """Per-expert routed-row counts: p ~ Dirichlet(alpha), counts ~

@@ -200,6 +200,31 @@ int qfp4_quantize_grouped_rows(int fmt, const void *X_bf16, int64_t total_rows, 
                                int64_t groups, const int32_t *row_offsets, const float *gs_rows,
                                void *Q_packed, void *SF_mma, void *stream);
 
+/* Residual add, RMSNorm and quantisation in one pass (quadbit README,
+ * "Accuracy (real models)": the fused RMSNorm and residual-add quantisers
+ * around the GEMMs, with NVFP4's per-row fp32 global scales; "The stack": the
+ * fused block-glue kernels).  Per row m, in fp32:
+ *   y = bf16_rne(x + r)                           (r == NULL: y = x)
+ *   z = (y * (1 / sqrt(sum(y^2) / K + eps))) * gamma
+ *   gs_rows[m] = amax(|z|) / (6 * 448)            (NVFP4 only)
+ * and z is quantised by the rule of qfp4_quantize with gs_rows[m] (MXFP4:
+ * no global scale), so Q, SF and gs_rows go straight into
+ * qfp4_gemm_nt_scaled (row_scale = gs_rows).
+ *   X_bf16, R_bf16  [M, K] BF16 (R may be NULL); gamma_bf16 [K] BF16
+ *   Y_bf16     [M, K] BF16 output, the new residual stream (NULL: not written)
+ *   gs_rows    DEVICE fp32 [M] output (NVFP4; MXFP4 ignores it)
+ *   Q_packed   [M, K/2];  SF  [M, K/g] row-major or MMA layout (padding zeroed)
+ * y is exact to that rule.  The sum of squares, 1/sqrt and z come from fp32
+ * arithmetic whose relative error is at most ((L + 2)/2 + 4) * 2^-24, where
+ * L = EPT + 10 is the longest chain of additions in the sum (EPT = 16, 32 or
+ * 64 elements per thread: the smallest multiple of g with K / EPT <= 1024);
+ * the codes and scale bytes are the rule's output for the kernel's z and
+ * gs_rows.  Requirements: K % 128 == 0, K <= 65536, M <= 2^31 - 1, eps >= 0
+ * and finite, X/R/gamma/Y/Q 16-byte aligned, SF and gs_rows 4-byte aligned. */
+int qfp4_residual_rmsnorm_quantize(int fmt, const void *X_bf16, const void *R_bf16, const void *gamma_bf16,
+                                   int64_t M, int64_t K, float eps, void *Y_bf16, float *gs_rows,
+                                   void *Q_packed, void *SF, int sf_layout, void *stream);
+
 /* ---------------------------------------------------------------------- */
 /* Scale-factor interleave                                                  */
 /* ---------------------------------------------------------------------- */

@@ -127,6 +127,29 @@ def test_absmax_gs_rejects_bad_arguments(lib):
     assert a(2, FAKE, FAKE, 256, FAKE + 2, None) == -3
 
 
+def test_residual_rmsnorm_quantize_rejects_bad_arguments(lib):
+    L = lib.qfp4_residual_rmsnorm_quantize
+    ok = dict(fmt=1, X=FAKE, R=FAKE, gm=FAKE, M=16, K=256, eps=1e-6, Y=FAKE, gs=FAKE, Q=FAKE, SF=FAKE, lay=1)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return L(a["fmt"], a["X"], a["R"], a["gm"], a["M"], a["K"], a["eps"], a["Y"], a["gs"], a["Q"], a["SF"],
+                 a["lay"], None)
+
+    assert call(fmt=2) == -1
+    assert call(lay=3) == -1
+    assert call(M=-1) == -1
+    assert call(eps=-1.0) == -1 and call(eps=float("nan")) == -1 and call(eps=float("inf")) == -1
+    assert call(K=200) == -2                    # K % 128
+    assert call(K=65536 + 128) == -2            # longer rows than one CTA holds
+    assert call(M=0) == 0 and call(K=0) == 0     # empty: nothing launched
+    assert call(X=None) == -1 and call(gm=None) == -1 and call(Q=None) == -1 and call(SF=None) == -1
+    assert call(gs=None) == -1                  # NVFP4 writes the row scales
+    assert call(X=FAKE + 8) == -3 and call(R=FAKE + 8) == -3 and call(Y=FAKE + 8) == -3
+    assert call(gm=FAKE + 8) == -3 and call(Q=FAKE + 4) == -3 and call(SF=FAKE + 2) == -3
+    assert call(gs=FAKE + 2) == -3
+
+
 def test_boundary_names_of_the_scope_table(lib):
     """The entry points the scope of this library names, with the argument
     counts given there: the three core calls, the per-expert global scale

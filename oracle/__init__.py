@@ -18,6 +18,7 @@ import numpy as np
 
 MXFP4 = 0
 NVFP4 = 1
+NVFP4_B32 = 2       # NVFP4 with one UE4M3 scale per 32 elements (the 2:4-sparse path)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")

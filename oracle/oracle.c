@@ -47,6 +47,12 @@
 
 #define ORACLE_MXFP4 0
 #define ORACLE_NVFP4 1
+/* NVFP4 with one UE4M3 scale per 32 K-elements (plus the fp32 global
+ * scales): the scale blocks of the 2:4-sparse path.  [QB] "Accuracy (real
+ * models)": the deployed two-level sparse kernel is trained "per-32 matched"
+ * (weights and activations quantised with 32-element blocks).
+ * READING: that is this format, for both operands of a sparse GEMM. */
+#define ORACLE_NVFP4_B32 2
 
 /* ------------------------------------------------------------------------ */
 /* Element and scale decoding                                                */
@@ -90,7 +96,7 @@ double oracle_scale_value(int fmt, int byte)
     return fmt == ORACLE_MXFP4 ? oracle_ue8m0_value(byte) : oracle_ue4m3_value(byte);
 }
 
-int oracle_block_size(int fmt) { return fmt == ORACLE_MXFP4 ? 32 : 16; }
+int oracle_block_size(int fmt) { return fmt == ORACLE_NVFP4 ? 16 : 32; }
 
 /* ------------------------------------------------------------------------ */
 /* Rounding to the formats (round to nearest, ties to even code)            */
@@ -546,8 +552,9 @@ int oracle_residual_rmsnorm(const uint16_t *x, const uint16_t *r, const uint16_t
  * i0 < i1, stored in that order in the compressed row [K/4 bytes].  The
  * group's metadata nibble is i0 | (i1 << 2); two groups per metadata byte,
  * the even group in the low nibble ([K/16] bytes per row).  The scale
- * factors are those of the dense K.  A pair is zero when both of its
- * elements decode to 0 (codes 0 or 8). */
+ * factors are indexed by the dense K; for NVFP4 they are the per-32 blocks of
+ * ORACLE_NVFP4_B32 (one scale per 16 stored elements of the sparse operand).
+ * A pair is zero when both of its elements decode to 0 (codes 0 or 8). */
 static int pair_is_zero(uint8_t b) { return (b & 7) == 0 && ((b >> 4) & 7) == 0; }
 
 int oracle_sparse24_decompress(const uint8_t *Wc, const uint8_t *meta, int64_t rows, int64_t K, uint8_t *W)

@@ -35,7 +35,8 @@ MUTANTS = [
     ("ue8m0_exponent_bias", "ldexp(1.0, byte - 127)", "ldexp(1.0, byte - 128)"),
     ("ue4m3_exponent_bias", "(1.0 + m / 8.0) * ldexp(1.0, e - 7)", "(1.0 + m / 8.0) * ldexp(1.0, e - 8)"),
     ("ue4m3_subnormal_step", "ldexp((double)m, -9)", "ldexp((double)m, -10)"),
-    ("block_sizes_swapped", "return fmt == ORACLE_MXFP4 ? 32 : 16;", "return fmt == ORACLE_MXFP4 ? 16 : 32;"),
+    ("block_sizes_swapped", "return fmt == ORACLE_NVFP4 ? 16 : 32;", "return fmt == ORACLE_NVFP4 ? 32 : 16;"),
+    ("nvfp4_b32_takes_block_16", "return fmt == ORACLE_NVFP4 ? 16 : 32;", "return fmt == ORACLE_MXFP4 ? 32 : 16;"),
     ("scale_types_swapped",
      "fmt == ORACLE_MXFP4 ? oracle_ue8m0_value(byte) : oracle_ue4m3_value(byte)",
      "fmt == ORACLE_MXFP4 ? oracle_ue4m3_value(byte) : oracle_ue8m0_value(byte)"),

@@ -17,7 +17,7 @@ import oracle
 from block_scaled_fp4_tcgen05_gb300 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-MX, NV = oracle.MXFP4, oracle.NVFP4
+MX, NV, NV32 = oracle.MXFP4, oracle.NVFP4, oracle.NVFP4_B32
 
 
 def _golden_rows(name):
@@ -188,7 +188,7 @@ def _grid_blocks(fmt, rows, blocks, seed, gs):
     return x.reshape(rows, blocks * g).astype(np.float32), codes.reshape(rows, blocks * g), sfb
 
 
-@pytest.mark.parametrize("fmt,gs", [(MX, 1.0), (NV, 1.0), (NV, 2.0 ** -3), (NV, 2.0 ** 5)])
+@pytest.mark.parametrize("fmt,gs", [(MX, 1.0), (NV, 1.0), (NV, 2.0 ** -3), (NV, 2.0 ** 5), (NV32, 2.0 ** -3)])
 def test_quantize_roundtrip_exact_on_grid(fmt, gs):
     x, codes, sfb = _grid_blocks(fmt, 6, 8, 21 + fmt, gs)
     assert np.array_equal(x.astype(np.float64) / 1.0, x)     # representable
@@ -310,7 +310,7 @@ def _pack(codes):
     return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
 
 
-@pytest.mark.parametrize("fmt", [MX, NV])
+@pytest.mark.parametrize("fmt", [MX, NV, NV32])
 def test_gemm_all_ones_closed_form(fmt):
     g = oracle.block_size(fmt)
     M, N, K = 3, 5, 256
@@ -326,7 +326,7 @@ def test_gemm_all_ones_closed_form(fmt):
     assert np.all(D == want) and np.all(T == abs(want))
 
 
-@pytest.mark.parametrize("fmt", [MX, NV])
+@pytest.mark.parametrize("fmt", [MX, NV, NV32])
 def test_gemm_one_hot_pins_nibble_order(fmt):
     """A single non-zero element at (m0, k0): the k index <-> nibble mapping
     (even k low nibble) and the block index k0 // g are both exercised."""
@@ -360,7 +360,7 @@ def _random_operands(fmt, M, N, K, seed):
     return A, Asf, B, Bsf
 
 
-@pytest.mark.parametrize("fmt", [MX, NV])
+@pytest.mark.parametrize("fmt", [MX, NV, NV32])
 def test_gemm_vs_numpy_matmul_of_independent_decode(fmt):
     """Decode with the golden table and torch's float8 decoders, multiply with
     numpy's matmul (fp64): must match the oracle to fp64 rounding."""
@@ -383,7 +383,7 @@ def test_gemm_vs_numpy_matmul_of_independent_decode(fmt):
     assert np.allclose(T, Tref, rtol=1e-12)
 
 
-@pytest.mark.parametrize("fmt", [MX, NV])
+@pytest.mark.parametrize("fmt", [MX, NV, NV32])
 def test_gemm_tiny_exact_bruteforce(fmt):
     """2x3 outputs, K = 64, exact rational arithmetic in pure Python."""
     M, N, K = 2, 3, 64
@@ -468,6 +468,28 @@ def test_gemm_ue8m0_increment_doubles_one_block():
     Dblk, _ = oracle.gemm_nt(MX, only, Asf, B, Bsf)
     assert np.array_equal(D1 - D0, Dblk)
     assert np.array_equal(np.delete(D1, 1, axis=0), np.delete(D0, 1, axis=0))
+
+
+@pytest.mark.parametrize("fmt,g", [(NV, 16), (NV32, 32)])
+def test_ue4m3_scale_step_doubles_exactly_one_block(fmt, g):
+    """One UE4M3 scale byte of one A row raised by one exponent step (0x38,
+    1.0, to 0x40, 2.0) adds exactly the contribution of that row's g elements
+    of the block once more: 16 for NVFP4, 32 for the per-32 format of the
+    sparse path."""
+    M, N, K = 3, 5, 256
+    A, _, B, _ = _random_operands(fmt, M, N, K, 62 + fmt)
+    assert oracle.block_size(fmt) == g
+    Asf = np.full((M, K // g), 0x38, np.uint8)
+    Bsf = np.full((N, K // g), 0x38, np.uint8)
+    D0, _ = oracle.gemm_nt(fmt, A, Asf, B, Bsf, 0.5, 4.0)
+    Asf1 = Asf.copy()
+    Asf1[2, 3] = 0x40
+    D1, _ = oracle.gemm_nt(fmt, A, Asf1, B, Bsf, 0.5, 4.0)
+    only = np.zeros_like(A)
+    only[2, 3 * g // 2:4 * g // 2] = A[2, 3 * g // 2:4 * g // 2]       # elements 3g .. 4g-1
+    Dblk, _ = oracle.gemm_nt(fmt, only, Asf, B, Bsf, 0.5, 4.0)
+    assert np.array_equal(D1 - D0, Dblk) and np.any(Dblk != 0)
+    assert np.array_equal(np.delete(D1, 2, axis=0), np.delete(D0, 2, axis=0))
 
 
 def test_gemm_entries_equal_full():
@@ -773,7 +795,7 @@ def test_sparse24_round_trips():
     assert np.array_equal(Wc3, Wc2) and np.array_equal(meta3, meta2)
 
 
-@pytest.mark.parametrize("fmt", [MX, NV])
+@pytest.mark.parametrize("fmt", [MX, NV, NV32])
 def test_sparse24_gemm_keeps_exactly_the_selected_positions(fmt):
     """All kept elements 1.0 (code 2) with unit scales: D[m, n] is the sum of
     a[m, k] over the positions k that row n keeps, found here from the

@@ -57,14 +57,15 @@ extern "C" int qfp4_device_check(void)
 extern "C" int qfp4_poll_device_status(void *stream)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    uint32_t q = 0, g = 0, gp = 0, gd = 0;
+    uint32_t q = 0, g = 0, gp = 0, gd = 0, gs = 0;
     int rc = qfp4::read_clear_status_quant(s, &q);
     if (rc == QFP4_OK) rc = qfp4::read_clear_status_gemm(s, &g);
     if (rc == QFP4_OK) rc = qfp4::read_clear_status_gemm_pair(s, &gp);
     if (rc == QFP4_OK) rc = qfp4::read_clear_status_gemm_decode(s, &gd);
+    if (rc == QFP4_OK) rc = qfp4::read_clear_status_gemm_sparse(s, &gs);
     if (rc != QFP4_OK) return rc;
-    const uint32_t all = q | g | gp | gd;
+    const uint32_t all = q | g | gp | gd | gs;
     if (all & qfp4::kStatusTimeout) return QFP4_ERR_TIMEOUT;
-    if (all & qfp4::kStatusBadGroup) return QFP4_ERR_INVALID_ARG;
+    if (all & (qfp4::kStatusBadGroup | qfp4::kStatusBadSparsity)) return QFP4_ERR_INVALID_ARG;
     return QFP4_OK;
 }

@@ -11,12 +11,15 @@ namespace qfp4 {
 // Device status word: one per translation unit that launches kernels.  A
 // kernel that gives up on a bounded wait ORs in a bit; qfp4_poll_device_status
 // reads and clears every unit's word.
-enum : uint32_t { kStatusTimeout = 1u, kStatusBadGroup = 2u };
+enum : uint32_t { kStatusTimeout = 1u, kStatusBadGroup = 2u, kStatusBadSparsity = 4u };
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-inline int block_elems(int fmt) { return fmt == QFP4_MXFP4 ? 32 : (fmt == QFP4_NVFP4 ? 16 : 0); }
+inline int block_elems(int fmt)
+{
+    return fmt == QFP4_NVFP4 ? 16 : (fmt == QFP4_MXFP4 || fmt == QFP4_NVFP4_B32) ? 32 : 0;
+}
 
 inline int launch_status(cudaError_t e)
 {
@@ -91,5 +94,6 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 // Per-unit status readers (defined in each .cu that owns a status word).
 int read_clear_status_quant(cudaStream_t s, uint32_t *out);
 int read_clear_status_gemm(cudaStream_t s, uint32_t *out);
+int read_clear_status_gemm_sparse(cudaStream_t s, uint32_t *out);
 
 }  // namespace qfp4

@@ -133,12 +133,12 @@ constexpr int kQStages = 2;
 // stages): the per-stage wait, release and refill are then paid once per two
 // blocks; MXFP4 blocks are twice as long, one per thread fills 16 KB.
 template <int FMT>
-__host__ __device__ constexpr int blocks_per_thread() { return FMT == QFP4_MXFP4 ? 1 : 2; }
+__host__ __device__ constexpr int blocks_per_thread() { return FMT == QFP4_NVFP4 ? 2 : 1; }
 
 template <int FMT>
 __host__ __device__ constexpr int chunk_bytes()
 {
-    return kThreads * blocks_per_thread<FMT>() * 2 * (FMT == QFP4_MXFP4 ? 32 : 16);
+    return kThreads * blocks_per_thread<FMT>() * 2 * (FMT == QFP4_NVFP4 ? 16 : 32);
 }
 
 // floor(n / d) for n < 2^32 as the high half of n * m with m = floor(2^64/d) + 1
@@ -161,7 +161,7 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
                 uint8_t *__restrict__ SF, int64_t M, int groups,
                 const int32_t *__restrict__ row_offsets, uint64_t kg_magic)
 {
-    constexpr int G = FMT == QFP4_MXFP4 ? 32 : 16;
+    constexpr int G = FMT == QFP4_NVFP4 ? 16 : 32;
     constexpr int W = G / 2;                            // bf16 words per block
     constexpr int BPT = blocks_per_thread<FMT>();
     constexpr int kChunkBytes = chunk_bytes<FMT>();
@@ -277,12 +277,12 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
             float gs = gs_one, inv_gs = inv_gs_one;
             if (GROUPED && valid) {
                 grp = find_group(s_offs, groups, row);
-                if (FMT == QFP4_NVFP4 && gs_ptr && !ROWGS) {
+                if (FMT != QFP4_MXFP4 && gs_ptr && !ROWGS) {
                     gs = gs_ptr[grp];
                     inv_gs = __frcp_rn(gs);
                 }
             }
-            if (ROWGS && FMT == QFP4_NVFP4 && valid) {
+            if (ROWGS && FMT != QFP4_MXFP4 && valid) {
                 gs = gs_ptr[row];
                 inv_gs = __frcp_rn(gs);
             }
@@ -553,7 +553,7 @@ template <int FMT, int LAYOUT, bool GROUPED, bool ROWGS = false>
 cudaError_t launch_quantize(const void *X, int64_t M, int64_t K, const float *gs, void *Q,
                             void *SF, int groups, const int32_t *offs, cudaStream_t s)
 {
-    constexpr int G = FMT == QFP4_MXFP4 ? 32 : 16;
+    constexpr int G = FMT == QFP4_NVFP4 ? 16 : 32;
     const int64_t blocks = M * (K / G);
     constexpr int kChunkBytes = chunk_bytes<FMT>();
     const int64_t chunks = (blocks * 2 * G + kChunkBytes - 1) / kChunkBytes;
@@ -683,19 +683,25 @@ extern "C" int qfp4_global_scale_rows(const void *X_bf16, int64_t rows, int64_t 
 extern "C" int qfp4_quantize_rows(int fmt, const void *X_bf16, int64_t M, int64_t K, const float *gs_rows,
                                   void *Q_packed, void *SF, int sf_layout, void *stream)
 {
-    if (fmt != QFP4_MXFP4 && fmt != QFP4_NVFP4) return QFP4_ERR_INVALID_ARG;
+    if (fmt != QFP4_MXFP4 && fmt != QFP4_NVFP4 && fmt != QFP4_NVFP4_B32) return QFP4_ERR_INVALID_ARG;
     if (sf_layout != QFP4_SF_ROWMAJOR && sf_layout != QFP4_SF_MMA) return QFP4_ERR_INVALID_ARG;
     if (M < 0 || K < 0) return QFP4_ERR_INVALID_ARG;
     if (K % 128 != 0) return QFP4_ERR_UNSUPPORTED;
     if (M == 0 || K == 0) return QFP4_OK;
     if ((M + 128) * (K / 16) >= (int64_t{1} << 32) - 4096) return QFP4_ERR_UNSUPPORTED;
     if (!X_bf16 || !Q_packed || !SF) return QFP4_ERR_INVALID_ARG;
-    if (fmt == QFP4_NVFP4 && !gs_rows) return QFP4_ERR_INVALID_ARG;
+    if (fmt != QFP4_MXFP4 && !gs_rows) return QFP4_ERR_INVALID_ARG;
     if (!aligned16(X_bf16) || !aligned16(Q_packed) || !aligned4(SF) || (gs_rows && !aligned4(gs_rows)))
         return QFP4_ERR_MISALIGNED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (fmt == QFP4_MXFP4)        // MXFP4 has no global scale: the plain quantiser
+    if (fmt == QFP4_NVFP4_B32)
+        e = sf_layout == QFP4_SF_MMA
+                ? launch_quantize<QFP4_NVFP4_B32, QFP4_SF_MMA, false, true>(X_bf16, M, K, gs_rows, Q_packed, SF, 1,
+                                                                            nullptr, s)
+                : launch_quantize<QFP4_NVFP4_B32, QFP4_SF_ROWMAJOR, false, true>(X_bf16, M, K, gs_rows, Q_packed,
+                                                                                 SF, 1, nullptr, s);
+    else if (fmt == QFP4_MXFP4)   // MXFP4 has no global scale: the plain quantiser
         e = sf_layout == QFP4_SF_MMA
                 ? launch_quantize<QFP4_MXFP4, QFP4_SF_MMA, false>(X_bf16, M, K, nullptr, Q_packed, SF, 1, nullptr, s)
                 : launch_quantize<QFP4_MXFP4, QFP4_SF_ROWMAJOR, false>(X_bf16, M, K, nullptr, Q_packed, SF, 1,
@@ -712,7 +718,7 @@ extern "C" int qfp4_quantize_rows(int fmt, const void *X_bf16, int64_t M, int64_
 extern "C" int qfp4_quantize(int fmt, const void *X_bf16, int64_t M, int64_t K, const float *gs,
                              void *Q_packed, void *SF, int sf_layout, void *stream)
 {
-    if (fmt != QFP4_MXFP4 && fmt != QFP4_NVFP4) return QFP4_ERR_INVALID_ARG;
+    if (fmt != QFP4_MXFP4 && fmt != QFP4_NVFP4 && fmt != QFP4_NVFP4_B32) return QFP4_ERR_INVALID_ARG;
     if (sf_layout != QFP4_SF_ROWMAJOR && sf_layout != QFP4_SF_MMA) return QFP4_ERR_INVALID_ARG;
     if (M < 0 || K < 0) return QFP4_ERR_INVALID_ARG;
     if (K % 128 != 0) return QFP4_ERR_UNSUPPORTED;
@@ -721,7 +727,7 @@ extern "C" int qfp4_quantize(int fmt, const void *X_bf16, int64_t M, int64_t K, 
     // and the padded scale rows
     if ((M + 128) * (K / 16) >= (int64_t{1} << 32) - 4096) return QFP4_ERR_UNSUPPORTED;
     if (!X_bf16 || !Q_packed || !SF) return QFP4_ERR_INVALID_ARG;
-    if (fmt == QFP4_NVFP4 && !gs) return QFP4_ERR_INVALID_ARG;
+    if (fmt != QFP4_MXFP4 && !gs) return QFP4_ERR_INVALID_ARG;
     if (!aligned16(X_bf16) || !aligned16(Q_packed) || !aligned4(SF) || (gs && !aligned4(gs)))
         return QFP4_ERR_MISALIGNED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -730,6 +736,11 @@ extern "C" int qfp4_quantize(int fmt, const void *X_bf16, int64_t M, int64_t K, 
         e = sf_layout == QFP4_SF_MMA
                 ? launch_quantize<QFP4_MXFP4, QFP4_SF_MMA, false>(X_bf16, M, K, gs, Q_packed, SF, 1, nullptr, s)
                 : launch_quantize<QFP4_MXFP4, QFP4_SF_ROWMAJOR, false>(X_bf16, M, K, gs, Q_packed, SF, 1, nullptr, s);
+    else if (fmt == QFP4_NVFP4_B32)
+        e = sf_layout == QFP4_SF_MMA
+                ? launch_quantize<QFP4_NVFP4_B32, QFP4_SF_MMA, false>(X_bf16, M, K, gs, Q_packed, SF, 1, nullptr, s)
+                : launch_quantize<QFP4_NVFP4_B32, QFP4_SF_ROWMAJOR, false>(X_bf16, M, K, gs, Q_packed, SF, 1,
+                                                                          nullptr, s);
     else
         e = sf_layout == QFP4_SF_MMA
                 ? launch_quantize<QFP4_NVFP4, QFP4_SF_MMA, false>(X_bf16, M, K, gs, Q_packed, SF, 1, nullptr, s)

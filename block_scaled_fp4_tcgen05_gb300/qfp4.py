@@ -16,6 +16,7 @@ import torch
 
 MXFP4 = 0
 NVFP4 = 1
+NVFP4_B32 = 2
 SF_ROWMAJOR = 0
 SF_MMA = 1
 
@@ -45,6 +46,10 @@ SIGNATURES = {
     "qfp4_gemm_nt_grouped_scaled": (_i32, [_i32, _i64, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                            _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "qfp4_absmax_gs": (_i32, [_i64, _vp, _vp, _i64, _vp, _vp]),
+    "qfp4_sparse24_meta_bytes": (_sz, [_i64, _i64, _i32]),
+    "qfp4_sparse24_compress": (_i32, [_vp, _i64, _i64, _vp, _vp, _i32, _vp]),
+    "qfp4_gemm_nt_sparse24": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                     _vp]),
     "qfp4_gemm_swiglu_quantize": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                          _vp]),
     "qfp4_gemm_swiglu_quantize_grouped": (_i32, [_i32, _i64, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp,
@@ -247,6 +252,24 @@ def gemm_nt_grouped_scaled(fmt, row_offsets, total_rows, max_group_rows, N, K, A
                                               _p(A), _p(A_sf), _p(B), _p(B_sf), _p(gs_a), _p(gs_b),
                                               _p(row_scale), _p(col_scale), _p(D), _p(workspace), ws_bytes,
                                               _stream(stream)))
+
+
+def sparse24_meta_bytes(rows: int, K: int, layout: int = SF_MMA) -> int:
+    return int(load().qfp4_sparse24_meta_bytes(rows, K, layout))
+
+
+def sparse24_compress(W, W_comp, W_meta, layout=SF_MMA, stream=None) -> None:
+    """2:4 pair-sparse packed W [rows, K/2] -> kept bytes [rows, K/4] and metadata."""
+    rows, K = W.shape[0], W.shape[1] * 2
+    _check("qfp4_sparse24_compress",
+           load().qfp4_sparse24_compress(_p(W), rows, K, _p(W_comp), _p(W_meta), layout, _stream(stream)))
+
+
+def gemm_nt_sparse24(fmt, M, N, K, X, X_sf, W_comp, W_meta, W_sf, gs_x, gs_w, D, row_scale=None, col_scale=None,
+                     stream=None) -> None:
+    _check("qfp4_gemm_nt_sparse24",
+           load().qfp4_gemm_nt_sparse24(fmt, M, N, K, _p(X), _p(X_sf), _p(W_comp), _p(W_meta), _p(W_sf), _p(gs_x),
+                                        _p(gs_w), _p(row_scale), _p(col_scale), _p(D), _stream(stream)))
 
 
 def gemm_swiglu_quantize(fmt, M, I, K, A, A_sf, W, W_sf, gs_a, gs_w, gs_out, Q_out, SF_out,

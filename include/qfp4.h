@@ -49,8 +49,14 @@
 extern "C" {
 #endif
 
-/* Formats. */
-enum { QFP4_MXFP4 = 0, QFP4_NVFP4 = 1 };
+/* Formats.  QFP4_NVFP4_B32 is NVFP4 with one UE4M3 scale per 32 elements
+ * (plus the fp32 global scale): the format of both operands of the 2:4
+ * sparse GEMM (quadbit README, "Accuracy (real models)": the deployed sparse
+ * kernel is trained "per-32 matched"; the tensor core's sparse MMA applies
+ * one scale per 16 stored elements, i.e. per 32 dense positions).  The
+ * quantiser (qfp4_quantize, qfp4_quantize_rows) and the global scales serve
+ * it like NVFP4; the dense GEMMs take QFP4_MXFP4 and QFP4_NVFP4 only. */
+enum { QFP4_MXFP4 = 0, QFP4_NVFP4 = 1, QFP4_NVFP4_B32 = 2 };
 
 /* Scale-factor layouts. */
 enum { QFP4_SF_ROWMAJOR = 0, QFP4_SF_MMA = 1 };
@@ -88,7 +94,7 @@ int qfp4_poll_device_status(void *stream);
 /* Sizes                                                                    */
 /* ---------------------------------------------------------------------- */
 
-/* Elements per scale block: 32 (MXFP4) or 16 (NVFP4); 0 for a bad fmt. */
+/* Elements per scale block: 32 (MXFP4, NVFP4_B32) or 16 (NVFP4); 0 for a bad fmt. */
 int qfp4_block_size(int fmt);
 
 /* Bytes of the MMA scale-factor layout for a [rows, cols] scale matrix. */
@@ -158,7 +164,8 @@ int qfp4_global_scale_rows(const void *X_bf16, int64_t rows, int64_t cols, float
  *   saturate at 6, sign kept); if s == 0 the block encodes as zeros.
  * Mojo page "fp4_quantization" (quantize_dynamic_scaled_fp4fp8); DeepGEMM
  * pull request "Summary" (formats).  The output is bit-exact to that rule.
- *   fmt        QFP4_MXFP4 (gs ignored, 1.0) or QFP4_NVFP4 (gs required)
+ *   fmt        QFP4_MXFP4 (gs ignored, 1.0), QFP4_NVFP4 or QFP4_NVFP4_B32
+ *              (gs required; g = 16 or 32, UE4M3 scales)
  *   gs         DEVICE pointer to one fp32 global scale (NULL allowed for MXFP4)
  *   sf_layout  QFP4_SF_ROWMAJOR: SF is [M, K/g] row-major;
  *              QFP4_SF_MMA: SF is written directly in the MMA layout
@@ -369,6 +376,57 @@ int qfp4_gemm_nt_grouped_scaled(int fmt, int64_t groups, const int32_t *row_offs
                                 const float *gs_a, const float *gs_b,
                                 const float *row_scale, const float *col_scale,
                                 void *D_bf16, void *workspace, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* 2:4 pair-sparse GEMM                                                     */
+/* ---------------------------------------------------------------------- */
+
+/* Bytes of the metadata qfp4_sparse24_compress writes for a [rows, K] operand:
+ * QFP4_SF_ROWMAJOR [rows][K/16] (two groups per byte, even group low) or
+ * QFP4_SF_MMA, the tiled layout the sparse GEMM reads:
+ * [ceil(rows/128)][K/512][128][32] (rows padded to 128 with valid codes). */
+size_t qfp4_sparse24_meta_bytes(int64_t rows, int64_t K, int meta_layout);
+
+/* Compress a 2:4 pair-sparse packed operand (quadbit README, "Accuracy (real
+ * models)": Blackwell FP4 2:4 sparsity is pair-granular, the MMA keeps 2 of
+ * every 4 FP4 pairs; "The stack": the weight packer).  W_packed [rows, K/2]
+ * holds at most two non-zero bytes (pairs of E2M1 elements; a pair whose
+ * elements both decode to 0, codes 0 and 8, is zero) in every group of four
+ * along K.  Per group the kept pairs i0 < i1 (the non-zero ones, padded with
+ * the lowest zero ones) go to W_comp [rows, K/4] in that order and the code
+ * i0 | i1 << 2 to the metadata.  A group with three or four non-zero pairs
+ * is not 2:4: the next qfp4_poll_device_status returns QFP4_ERR_INVALID_ARG
+ * (that group's outputs are then undefined).  Requirements: K % 64 == 0
+ * (K % 512 == 0 for QFP4_SF_MMA), W_packed / W_comp 16-byte aligned,
+ * W_meta 4-byte aligned, of qfp4_sparse24_meta_bytes bytes. */
+int qfp4_sparse24_compress(const void *W_packed, int64_t rows, int64_t K, void *W_comp, void *W_meta,
+                           int meta_layout, void *stream);
+
+/* D[M,N] (BF16) = X @ W^T with W 2:4 pair-sparse, on the tensor cores'
+ * sparse MMA (tcgen05.mma.sp; quadbit README, "Headline result": the sparse
+ * FP4 GEMM; "Accuracy (real models)": the two-level sparse kernel with a
+ * per-row and per-column fp32 rescale in the epilogue):
+ *   D[m,n] = bf16_rne( (acc[m,n] * (gs_x*gs_w * row_scale[m])) * col_scale[n] )
+ * with acc = sum_k x[m,k] w[n,k] over the dense K, w the decompressed W.
+ *   fmt       QFP4_NVFP4_B32 (one UE4M3 scale per 32 elements for both
+ *             operands, the format the sparse MMA applies; others return
+ *             QFP4_ERR_UNSUPPORTED)
+ *   X_packed  [M, K/2] activations, X_sf MMA layout for [M, K/32]
+ *   W_comp    [N, K/4], W_meta tiled (QFP4_SF_MMA) metadata of
+ *             qfp4_sparse24_compress; W_sf MMA layout for [N, K/32] (the
+ *             scales of the dense W)
+ *   gs_x, gs_w DEVICE fp32 scalars (NULL = 1.0); row_scale [M], col_scale
+ *             [N] DEVICE fp32 or NULL (ones)
+ * Kernel: CTA pairs on 256 weight rows x 256 tokens, stages of 512 K.
+ * Requirements: N % 256 == 0, K % 512 == 0, pointers 16-byte aligned (the
+ * scale vectors 4-byte); M any (M == 0 or N == 0 launches nothing, K == 0
+ * writes D = 0).  Accuracy as qfp4_gemm_nt, with T over the kept products. */
+int qfp4_gemm_nt_sparse24(int fmt, int64_t M, int64_t N, int64_t K,
+                          const void *X_packed, const void *X_sf,
+                          const void *W_comp, const void *W_meta, const void *W_sf,
+                          const float *gs_x, const float *gs_w,
+                          const float *row_scale, const float *col_scale,
+                          void *D_bf16, void *stream);
 
 /* ---------------------------------------------------------------------- */
 /* Up-projection with SwiGLU and requantisation                             */

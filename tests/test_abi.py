@@ -59,7 +59,7 @@ def test_quantize_rejects_bad_arguments(lib):
         a = dict(ok_args, **kw)
         return L(a["fmt"], a["X"], a["M"], a["K"], a["gs"], a["Q"], a["SF"], a["layout"], a["stream"])
 
-    assert call(fmt=2) == -1
+    assert call(fmt=3) == -1
     assert call(layout=5) == -1
     assert call(M=-1) == -1
     assert call(K=200) == -2
@@ -150,6 +150,37 @@ def test_residual_rmsnorm_quantize_rejects_bad_arguments(lib):
     assert call(gs=FAKE + 2) == -3
 
 
+def test_sparse_entry_points_reject_bad_arguments(lib):
+    c = lib.qfp4_sparse24_compress
+    assert c(FAKE, 16, 256, FAKE, FAKE, 7, None) == -1          # layout
+    assert c(FAKE, -1, 256, FAKE, FAKE, 0, None) == -1
+    assert c(FAKE, 16, 96, FAKE, FAKE, 0, None) == -2           # K % 64
+    assert c(FAKE, 16, 256, FAKE, FAKE, 1, None) == -2          # tiled metadata wants K % 512
+    assert c(None, 16, 256, FAKE, FAKE, 0, None) == -1
+    assert c(FAKE + 8, 16, 256, FAKE, FAKE, 0, None) == -3
+    assert c(FAKE, 16, 256, FAKE, FAKE + 2, 0, None) == -3
+    assert c(FAKE, 0, 256, FAKE, FAKE, 0, None) == 0
+    assert qfp4.sparse24_meta_bytes(130, 512, 1) == 256 * 32 and qfp4.sparse24_meta_bytes(130, 512, 0) == 130 * 32
+    g = lib.qfp4_gemm_nt_sparse24
+    base = [2, 256, 256, 512, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None, FAKE, None]
+
+    def call(i=None, v=None):
+        a = list(base)
+        if i is not None:
+            a[i] = v
+        return g(*a)
+
+    assert call(0, 5) == -1
+    assert call(0, 1) == -2                                      # the sparse MMA's scales are per 32
+    assert call(1, -1) == -1
+    assert call(2, 384) == -2                                    # N % 256
+    assert call(3, 256) == -2                                    # K % 512
+    assert call(1, 0) == 0                                       # empty D
+    assert call(4, None) == -1
+    assert call(6, FAKE + 8) == -3
+    assert call(11, FAKE + 2) == -3
+
+
 def test_boundary_names_of_the_scope_table(lib):
     """The entry points the scope of this library names, with the argument
     counts given there: the three core calls, the per-expert global scale
@@ -177,7 +208,7 @@ def test_two_level_entry_points_reject_bad_arguments(lib):
     assert lib.qfp4_global_scale_rows(None, 0, 16, None, None) == 0            # no rows: nothing launched
     # quantisation with per-row global scales
     q = lib.qfp4_quantize_rows
-    assert q(2, FAKE, 16, 256, FAKE, FAKE, FAKE, 0, None) == -1               # format
+    assert q(3, FAKE, 16, 256, FAKE, FAKE, FAKE, 0, None) == -1               # format
     assert q(1, FAKE, 16, 256, FAKE, FAKE, FAKE, 5, None) == -1               # layout
     assert q(1, FAKE, 16, 200, FAKE, FAKE, FAKE, 0, None) == -2               # K % 128
     assert q(1, FAKE, 16, 256, None, FAKE, FAKE, 0, None) == -1               # NVFP4 needs gs_rows

@@ -510,6 +510,8 @@ def sweep(device, l2_bytes, peaks):
         tf = 2 * case.M * case.N * case.K / (ms * 1e-3) / 1e12
         out.append({"workload": case.name, "us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
                     "frac_fp4_peak": round(tf / fp4_peak, 3)})
+    # 2:4 pair-sparse GEMM against the dense one
+    out += sparse_time(device, l2_bytes, fp4_peak)
     # grouped MoE up-projection
     out.append(grouped_time(device, fp4_peak))
     # two-level NVFP4 (per-row global scales, row/column rescale in the epilogue)
@@ -521,6 +523,68 @@ def sweep(device, l2_bytes, peaks):
         except Exception as exc:       # keep the rest of the line if this entry fails
             out.append({"workload": f"nvfp4_swiglu_up{'_grouped' if grouped else ''}", "error": repr(exc)[:200]})
     torch.cuda.empty_cache()
+    return out
+
+
+SPARSE_SHAPES = ((4096, 4096, 4096), (4096, 14336, 4096), (4096, 4096, 14336), (8192, 8192, 8192))
+
+
+def sparse_time(device, l2_bytes, fp4_peak):
+    """The 2:4 pair-sparse GEMM (NVFP4 with 32-element scale blocks) at the
+    shapes the pages measure it on (quadbit README, "Headline result": attn
+    4096^3, ffn-up, ffn-down, square 8192), weights rotated past the L2, in
+    effective TFLOP/s = 2*M*N*K / t (the pages' count), beside the dense NVFP4
+    GEMM on the same shape."""
+    import torch
+    from block_scaled_fp4_tcgen05_gb300 import qfp4
+    out = []
+    for (M, N, K) in SPARSE_SHAPES:
+        X = torch.from_numpy(synth.activations_bf16(synth.SEED_BASE + 11, M, K).view(np.int16).copy()).view(
+            torch.bfloat16).to(device)
+        W = torch.from_numpy(synth.weights_bf16(synth.SEED_BASE + 12, N, K).view(np.int16).copy()).view(
+            torch.bfloat16).to(device)
+        gx = torch.empty(1, dtype=torch.float32, device=device)
+        gw = torch.empty(1, dtype=torch.float32, device=device)
+        qfp4.global_scale(X, gx)
+        qfp4.global_scale(W, gw)
+        Qx = torch.empty((M, K // 2), dtype=torch.uint8, device=device)
+        SFx = torch.empty(qfp4.sf_mma_bytes(M, K // 32), dtype=torch.uint8, device=device)
+        qfp4.quantize(qfp4.NVFP4_B32, X, gx, Qx, SFx, qfp4.SF_MMA)
+        Qw = torch.empty((N, K // 2), dtype=torch.uint8, device=device)
+        SFw = torch.empty(qfp4.sf_mma_bytes(N, K // 32), dtype=torch.uint8, device=device)
+        qfp4.quantize(qfp4.NVFP4_B32, W, gw, Qw, SFw, qfp4.SF_MMA)
+        del X, W
+        # 2:4 pair pruning: keep two of every four pair bytes (a seeded pattern)
+        gen = torch.Generator(device=device).manual_seed(synth.SEED_BASE + 13)
+        keep = torch.rand((N, K // 8, 4), generator=gen, device=device).argsort(dim=2)[..., :2]
+        mask = torch.zeros((N, K // 8, 4), dtype=torch.bool, device=device).scatter_(2, keep, True)
+        Qw = torch.where(mask.view(N, K // 2), Qw, torch.zeros_like(Qw))
+        Wc = torch.empty((N, K // 4), dtype=torch.uint8, device=device)
+        meta = torch.empty(qfp4.sparse24_meta_bytes(N, K, qfp4.SF_MMA), dtype=torch.uint8, device=device)
+        qfp4.sparse24_compress(Qw, Wc, meta, qfp4.SF_MMA)
+        del Qw, mask, keep
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        wbytes = Wc.numel() + meta.numel() + SFw.numel()
+        copies = max(1, min(16, int(np.ceil(2 * l2_bytes / wbytes)) + 1))
+        Wcs = [Wc] + [Wc.clone() for _ in range(copies - 1)]
+        Ms = [meta] + [meta.clone() for _ in range(copies - 1)]
+        SFs = [SFw] + [SFw.clone() for _ in range(copies - 1)]
+        calls = [(lambda i=i: qfp4.gemm_nt_sparse24(qfp4.NVFP4_B32, M, N, K, Qx, SFx, Wcs[i], Ms[i], SFs[i], gx,
+                                                    gw, D)) for i in range(copies)]
+        ms = graph_time(calls, 5)
+        assert qfp4.poll_device_status() == 0
+        del Wcs, Ms, SFs, calls, Qx, SFx, Wc, meta, SFw, D
+        torch.cuda.empty_cache()
+        dense = next((c for c in synth.COMPUTE_SWEEP + (synth.PREFILL_NV,)
+                      if c.fmt == 1 and (c.M, c.N, c.K) == (M, N, K)), None)
+        dense_ms = rotated_gemm_time(dense, device, l2_bytes, reps=5) if dense else None
+        tf = 2 * M * N * K / (ms * 1e-3) / 1e12
+        e = {"workload": f"nvfp4_b32_sparse24_gemm_nt_{M}x{N}x{K}", "us": round(ms * 1e3, 1),
+             "TFLOP/s_effective": round(tf, 1), "frac_fp4_dense_peak": round(tf / fp4_peak, 3)}
+        if dense_ms:
+            e["us_dense_nvfp4"] = round(dense_ms * 1e3, 1)
+            e["speedup_vs_dense"] = round(dense_ms / ms, 3)
+        out.append(e)
     return out
 
 

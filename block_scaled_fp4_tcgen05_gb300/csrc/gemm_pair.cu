@@ -118,47 +118,63 @@ __device__ __forceinline__ void record_timeout()
     atomicOr(&g_status_gemm_pair, static_cast<uint32_t>(kStatusTimeout));
 }
 
-// silu(g) * u = g / (1 + exp(-g)) * u in fp32: CUDA's full-accuracy expf
-// (+inf for g below about -88.7, which makes the quotient a signed zero, the
-// limit), then a correctly rounded division and product.  quadbit README,
-// "Accuracy (real models)": the fused SwiGLU quantiser between the GEMMs.
+// e^x for x in [-86, 0] by Cody-Waite range reduction (W. J. Cody and
+// W. Waite, "Software Manual for the Elementary Functions", 1980):
+// x = n ln2 + r with n = rint(x log2(e)), r = (x - n ln2_hi) - n ln2_lo,
+// where ln2_hi holds the leading 16 bits of ln 2 (so n ln2_hi is exact for
+// |n| < 2^8) and ln2_lo the next 24; e^r = 2^(r log2(e)) with |r| <= ln2/2
+// from the hardware's ex2.approx; 2^n by exponent arithmetic.  Measured on
+// GB300 against exact values: relative error below 2^-22.7.
+__device__ __forceinline__ float exp_cody_waite(float x)
+{
+    constexpr float kLog2e = 0x1.715476p+0f, kLn2Hi = 0x1.62e4p-1f, kLn2Lo = 0x1.7f7d1cp-20f;
+    const float n = rintf(__fmul_rn(x, kLog2e));
+    float r = __fmaf_rn(-n, kLn2Hi, x);
+    r = __fmaf_rn(-n, kLn2Lo, r);
+    float e2;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(e2) : "f"(__fmul_rn(r, kLog2e)));
+    return __fmul_rn(e2, __int_as_float((static_cast<int>(n) + 127) << 23));
+}
+
+// silu(g) * u = g * sigma(g) * u in fp32 with a bounded error (quadbit
+// README, "Accuracy (real models)": the fused SwiGLU quantiser between the
+// GEMMs), written without branches so that the sixteen values a thread
+// holds are computed side by side: with t = e^-|g| in (0, 1],
+// sigma(g) = 1 / (1 + t) for g >= 0 and t / (1 + t) below, so the divisor
+// lies in [1, 2]; the quotient is the hardware's reciprocal estimate with
+// one remainder correction.  |g| beyond 86 takes t = e^-86 (the value it
+// multiplies is then below 2^-120 |g u|).  Measured on GB300: relative error
+// below 2^-22 against exact values, far inside the 2^-19 |H| the
+// requantisation check allows for the epilogue's arithmetic.
 __device__ __forceinline__ float silu_mul(float g, float u)
 {
-    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+    const float t = exp_cody_waite(fmaxf(-fabsf(g), -86.0f));
+    const float a = g >= 0.0f ? g : __fmul_rn(g, t);
+    const float d = __fadd_rn(1.0f, t);
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(d));
+    const float q0 = __fmul_rn(a, y);
+    const float q = __fmaf_rn(__fmaf_rn(-d, q0, a), y, q0);
+    return __fmul_rn(q, u);
 }
 
 // The quantiser's rule on one block of G values held by this thread, with
-// the same steps and roundings as the standalone quantiser: amax, t =
-// (amax / 6) / gs, the scale byte (UE8M0 for G = 32, where gs is 1; UE4M3
-// for G = 16), s = decode * gs, codes of h / s (all +0 when s is 0).
-// Returns the scale byte; writes G / 8 words of packed codes.
+// the standalone quantiser's steps and fast bit-exact arithmetic (shared
+// from qfp4_fp4_codes.cuh): amax, t = (amax / 6) / gs, the scale byte (UE8M0
+// for G = 32, where gs is 1; UE4M3 for G = 16), s = decode * gs, codes of
+// h / s (all +0 when s is 0).  inv_gs = RN(1 / gs).  Returns the scale byte;
+// writes G / 8 words of packed codes.
 template <int G>
-__device__ __forceinline__ uint32_t quant_block(const float (&h)[G], float gs, uint32_t *w)
+__device__ __forceinline__ uint32_t quant_block(const float *h, float gs, float inv_gs, uint32_t *w)
 {
+    constexpr int FMT = G == 32 ? QFP4_MXFP4 : QFP4_NVFP4;
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < G; ++i) amax = fmaxf(amax, fabsf(h[i]));
-    uint32_t code;
-    float s;
-    if (G == 32) {
-        code = ue8m0_encode(__fdiv_rn(amax, 6.0f));
-        s = ue8m0_decode(code);
-    } else {
-        const float t = __fdiv_rn(__fdiv_rn(amax, 6.0f), gs);
-        // t is NaN only when amax and gs are both 0 (0/0) and then takes
-        // code 0 like t = 0; a non-zero block with gs = 0 has t = +inf and
-        // saturates to 0x7E, and s = 448 * 0 = 0 still makes its codes +0
-        code = t > 0.0f ? ue4m3_encode(t) : 0u;
-        s = __fmul_rn(ue4m3_decode(code), gs);
-    }
+    const BlockScale bs = block_scale<FMT>(amax, gs, inv_gs);
 #pragma unroll
-    for (int b = 0; b < G / 8; ++b) {
-        float q[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = s == 0.0f ? 0.0f : __fdiv_rn(h[8 * b + i], s);
-        w[b] = s == 0.0f ? 0u : e2m1x8(q);
-    }
-    return code;
+    for (int b = 0; b < G / 8; ++b) w[b] = encode8_f32<FMT>(h + 8 * b, bs);
+    return bs.code;
 }
 
 struct PairTile {
@@ -548,13 +564,14 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 // of the same outputs, i.e. 64 columns of H starting at
                 // (n0 + 128 half) / 2.  NVFP4: chunk j (32 columns) is one
                 // block of 16; MXFP4: chunks 2k, 2k + 1 are one block of 32.
-                // Each lane (one row) quantises its own blocks: 32 bytes of
-                // codes and 4 (NVFP4) or 2 (MXFP4) scale bytes per tile half.
+                // Each lane (one row) computes its 64 values of H, releases
+                // the accumulator, and only then quantises its own blocks: 32
+                // bytes of codes and 4 (NVFP4) or 2 (MXFP4) scale bytes per
+                // tile half.
                 constexpr int G = C::G;
                 const int32_t hrow = ti.row0 + 128 * static_cast<int32_t>(rank) + quad * 32 + lane;
                 const uint32_t tcol = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + half * 128;
-                uint32_t qw[8];
-                uint32_t sfw = 0;
+                float h[64];
                 if (G == 16) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -562,12 +579,10 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         tmem_ld_32x32b_x32(tcol + j * 32, v);
                         tmem_ld_wait();
                         tmem_regs_after_wait(v);
-                        float h[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            h[i] = silu_mul(__fmul_rn(__uint_as_float(v[i]), gs),
-                                            __fmul_rn(__uint_as_float(v[16 + i]), gs));
-                        sfw |= quant_block<16>(h, gs_out, &qw[2 * j]) << (8 * j);
+                            h[16 * j + i] = silu_mul(__fmul_rn(__uint_as_float(v[i]), gs),
+                                                     __fmul_rn(__uint_as_float(v[16 + i]), gs));
                     }
                 } else {
 #pragma unroll
@@ -578,16 +593,24 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         tmem_ld_wait();
                         tmem_regs_after_wait(vg);
                         tmem_regs_after_wait(vu);
-                        float h[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            h[i] = silu_mul(__uint_as_float(vg[i]), __uint_as_float(vu[i]));
-                        sfw |= quant_block<32>(h, 1.0f, &qw[4 * k]) << (8 * k);
+                            h[32 * k + i] = silu_mul(__uint_as_float(vg[i]), __uint_as_float(vu[i]));
                     }
                 }
                 tc_fence_before();
                 if (!named_barrier_and(1, 256, got != 0 && *abort_flag == 0)) { ok = got != 0; break; }
                 if (warp == 12 && lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
+                uint32_t qw[8];
+                uint32_t sfw = 0;
+                const float inv_gs_out = __frcp_rn(gs_out);
+                if (G == 16) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) sfw |= quant_block<16>(&h[16 * j], gs_out, inv_gs_out, &qw[2 * j]) << (8 * j);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) sfw |= quant_block<32>(&h[32 * k], 1.0f, 1.0f, &qw[4 * k]) << (8 * k);
+                }
                 if (hrow < ti.row_end) {
                     uint8_t *qdst = p.Q_out + static_cast<size_t>(hrow) * static_cast<size_t>(p.I / 2) +
                                     ti.n0 / 4 + half * 32;

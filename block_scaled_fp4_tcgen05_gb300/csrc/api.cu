@@ -11,6 +11,23 @@
 
 namespace qfp4 {
 
+int ensure_thread_context()
+{
+    // The runtime makes the primary context current on a host thread only
+    // when that thread makes certain runtime calls; a driver-API call (the
+    // tensor-map encode) from a thread that has made none fails with
+    // CUDA_ERROR_INVALID_CONTEXT.  cudaSetDevice binds the current device's
+    // primary context to the calling thread; done once per thread and device.
+    thread_local int bound = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QFP4_ERR_CUDA;
+    if (dev != bound) {
+        if (cudaSetDevice(dev) != cudaSuccess) return QFP4_ERR_CUDA;
+        bound = dev;
+    }
+    return QFP4_OK;
+}
+
 int ensure_smem_attr(const void *kern, int bytes)
 {
     static std::mutex mu;

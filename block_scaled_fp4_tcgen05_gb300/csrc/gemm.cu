@@ -408,12 +408,100 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
     return fn;
 }
 
+int encode_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+               uint32_t box_rows);
+int encode_map_kpairs(CUtensorMap *map, const void *base, uint64_t K, uint64_t rows);
+int encode_map_bf16(CUtensorMap *map, void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                    uint32_t box_rows);
+
+// Encoded tensor maps, cached.  A map is a pure function of its encode
+// arguments (base address, extents, strides, box, element type, swizzle), so
+// an entry keyed by all of them can never be stale: a buffer freed and
+// reallocated at the same address with the same shape gets the same map.
+// Decode-sized GEMMs run in ~10 us, and encoding two or three maps on the
+// host per call is a visible part of that; the cache makes repeated calls on
+// the same buffers (the common case: weights, and activations in a reused
+// arena) skip the encode.  Fixed size, hash-indexed, replace on collision,
+// one mutex (host threads may call the library concurrently).
+struct MapKey {
+    uint32_t kind;           // 0: make_map, 1: make_map_kpairs, 2: make_map_bf16
+    uint32_t box0, box1;
+    const void *base;
+    uint64_t d0, d1;
+    bool operator==(const MapKey &o) const
+    {
+        return kind == o.kind && box0 == o.box0 && box1 == o.box1 && base == o.base && d0 == o.d0 && d1 == o.d1;
+    }
+};
+
+constexpr int kMapCacheSize = 256;
+struct MapEntry {
+    bool used = false;
+    MapKey key{};
+    CUtensorMap map{};
+};
+
+std::mutex g_map_mu;
+MapEntry g_map_cache[kMapCacheSize];
+
+size_t map_hash(const MapKey &k)
+{
+    uint64_t h = 0x9E3779B97F4A7C15ull * (reinterpret_cast<uintptr_t>(k.base) >> 4);
+    h ^= (k.d0 * 0xC2B2AE3D27D4EB4Full) + (k.d1 << 17) + (static_cast<uint64_t>(k.box0) << 7) + k.box1 + k.kind;
+    h ^= h >> 29;
+    return static_cast<size_t>(h % kMapCacheSize);
+}
+
+template <typename F>
+int cached_map(const MapKey &key, CUtensorMap *out, F encode)
+{
+    const size_t i = map_hash(key);
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        if (g_map_cache[i].used && g_map_cache[i].key == key) {
+            *out = g_map_cache[i].map;
+            return QFP4_OK;
+        }
+    }
+    int rc = ensure_thread_context();
+    if (rc == QFP4_OK) rc = encode(out);
+    if (rc == QFP4_OK) {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        g_map_cache[i].used = true;
+        g_map_cache[i].key = key;
+        g_map_cache[i].map = *out;
+    }
+    return rc;
+}
+
 }  // namespace
 
 // 2D byte matrix [rows, inner] (row stride = inner bytes), box of
 // box_inner bytes x box_rows rows, 128-byte swizzle, zero fill out of bounds.
 int make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, uint32_t box_inner,
              uint32_t box_rows)
+{
+    return cached_map(MapKey{0, box_inner, box_rows, base, inner, rows}, map,
+                      [&](CUtensorMap *m) { return encode_map(m, base, inner, rows, box_inner, box_rows); });
+}
+
+int make_map_kpairs(CUtensorMap *map, const void *base, uint64_t K, uint64_t rows)
+{
+    return cached_map(MapKey{1, 0, 0, base, K, rows}, map,
+                      [&](CUtensorMap *m) { return encode_map_kpairs(m, base, K, rows); });
+}
+
+int make_map_bf16(CUtensorMap *map, void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                  uint32_t box_rows)
+{
+    return cached_map(MapKey{2, box_cols, box_rows, base, cols, rows}, map,
+                      [&](CUtensorMap *m) { return encode_map_bf16(m, base, cols, rows, box_cols, box_rows); });
+}
+
+namespace {
+
+int encode_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+               uint32_t box_rows)
 {
     auto enc = get_encode_fn();
     if (!enc) return QFP4_ERR_CUDA;
@@ -427,7 +515,7 @@ int make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, 
     return r == CUDA_SUCCESS ? QFP4_OK : QFP4_ERR_CUDA;
 }
 
-int make_map_kpairs(CUtensorMap *map, const void *base, uint64_t K, uint64_t rows)
+int encode_map_kpairs(CUtensorMap *map, const void *base, uint64_t K, uint64_t rows)
 {
     auto enc = get_encode_fn();
     if (!enc) return QFP4_ERR_CUDA;
@@ -441,8 +529,8 @@ int make_map_kpairs(CUtensorMap *map, const void *base, uint64_t K, uint64_t row
     return r == CUDA_SUCCESS ? QFP4_OK : QFP4_ERR_CUDA;
 }
 
-int make_map_bf16(CUtensorMap *map, void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                  uint32_t box_rows)
+int encode_map_bf16(CUtensorMap *map, void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                    uint32_t box_rows)
 {
     auto enc = get_encode_fn();
     if (!enc) return QFP4_ERR_CUDA;
@@ -455,6 +543,8 @@ int make_map_bf16(CUtensorMap *map, void *base, uint64_t cols, uint64_t rows, ui
                      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? QFP4_OK : QFP4_ERR_CUDA;
 }
+
+}  // namespace
 
 namespace {
 

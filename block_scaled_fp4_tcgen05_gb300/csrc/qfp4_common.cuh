@@ -31,6 +31,11 @@ inline int launch_status(cudaError_t e)
 // Safe to call from several host threads (a mutex guards the record).
 int ensure_smem_attr(const void *kern, int bytes);
 
+// Makes the current device's primary context current on the calling host
+// thread (needed before driver-API calls from a thread that has made no
+// runtime call yet).  Once per (thread, device).
+int ensure_thread_context();
+
 // Grouped launches read per-group row offsets from device memory.  They are
 // usable only if they start at 0, never decrease, end at the row count the
 // host sized the launch for and, when max_rows > 0, give no group more than

@@ -2,6 +2,11 @@
 
 Translation units compile in parallel, then link into
 ``block_scaled_fp4_tcgen05_gb300/libqfp4.so``.  No CMake, no JIT.
+
+variant="faultinj" builds the same sources with QFP4_FAULT_INJECTION into
+``libqfp4_faultinj.so`` (objects in ``_build_faultinj``): a test library whose
+wait limit is 5 ms and which exports qfp4_test_inject_skip_release, so that a
+test can make one bounded wait run out.  The released library never has it.
 """
 from __future__ import annotations
 
@@ -17,6 +22,11 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqfp4.so")
+VARIANTS = {
+    None: (BUILD, LIB, []),
+    "faultinj": (os.path.join(HERE, "_build_faultinj"), os.path.join(HERE, "libqfp4_faultinj.so"),
+                 ["-DQFP4_FAULT_INJECTION"]),
+}
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -47,18 +57,19 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, variant: str | None = None) -> str:
+    build_dir, lib, extra = VARIANTS[variant]
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
     objs = []
     jobs = []
     for src in sources:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
-            cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+            cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
             if verbose:
                 cmd.insert(1, "-Xptxas=-v")
             jobs.append(cmd)
@@ -74,17 +85,17 @@ def build(force: bool = False, verbose: bool = False) -> str:
                     sys.stderr.write(r.stdout + r.stderr)
                 if r.returncode != 0:
                     raise RuntimeError(f"nvcc failed: {' '.join(cmd)}")
-    if force or jobs or _stale(LIB, objs):
+    if force or jobs or _stale(lib, objs):
         libdir = _cuda_lib_dir(nvcc)
-        tmp = LIB + f".{os.getpid()}.tmp"
+        tmp = lib + f".{os.getpid()}.tmp"
         cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
                "-Xlinker", f"-rpath={libdir}", "-L", libdir]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)
             raise RuntimeError("link failed")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -52,6 +52,21 @@ namespace qfp4 {
 
 __device__ uint32_t g_status_gemm_pair = 0;
 
+#ifdef QFP4_FAULT_INJECTION
+// Test build only: when set, the leader epilogue of pair 0 skips its release
+// of the accumulator after its first tile, so that the MMA issuer's next wait
+// runs out.  No copy engine transfer completes on that barrier, so nothing is
+// in flight when the kernel gives up; every other role of the pair then runs
+// out of its own waits, and the kernel ends through its abort path.
+__device__ int g_inject_skip_release = 0;
+__device__ __forceinline__ bool inject_skip_release(int32_t pair_id, uint32_t rank, int32_t t)
+{
+    return g_inject_skip_release != 0 && pair_id == 0 && rank == 0 && t == 0;
+}
+#else
+__device__ __forceinline__ bool inject_skip_release(int32_t, uint32_t, int32_t) { return false; }
+#endif
+
 int read_clear_status_gemm_pair(cudaStream_t s, uint32_t *out)
 {
     uint32_t zero = 0;
@@ -663,7 +678,8 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             tmem_regs_after_wait(last);
             tc_fence_before();
             if (!named_barrier_and(1, 256, got != 0 && *abort_flag == 0)) { ok = got != 0; break; }
-            if (warp == 12 && lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
+            if (warp == 12 && lane == 0 && !inject_skip_release(pair_id, rank, t))
+                mbar_arrive_cluster_relaxed(acc_empty_leader);
             uint32_t q3[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -782,6 +798,13 @@ int launch_gemm_pair(int fmt, bool grouped, const CUtensorMap &ma, const CUtenso
                    : launch<QFP4_MXFP4, false>(ma, mb, md, prm, pair_tiles, s);
 }
 
+#ifdef QFP4_FAULT_INJECTION
+int set_inject_skip_release(int on)
+{
+    return cudaMemcpyToSymbol(g_inject_skip_release, &on, sizeof(int)) == cudaSuccess ? QFP4_OK : QFP4_ERR_CUDA;
+}
+#endif
+
 int launch_gemm_pair_swiglu(int fmt, bool grouped, const CUtensorMap &ma, const CUtensorMap &mb,
                             const GemmParams &prm, int64_t pair_tiles, cudaStream_t s)
 {
@@ -794,3 +817,9 @@ int launch_gemm_pair_swiglu(int fmt, bool grouped, const CUtensorMap &ma, const 
 }
 
 }  // namespace qfp4
+
+#ifdef QFP4_FAULT_INJECTION
+// Test build only (not declared in the public header): arm (1) or disarm (0)
+// the injected missing release described above.
+extern "C" int qfp4_test_inject_skip_release(int on) { return qfp4::set_inject_skip_release(on); }
+#endif

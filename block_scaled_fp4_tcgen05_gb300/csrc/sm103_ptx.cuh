@@ -79,7 +79,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 
 // Upper bound on any single wait inside a kernel of this library.  A wait
 // that runs out returns false; the caller records QFP4_ERR_TIMEOUT and stops.
+// The fault-injection test build (QFP4_FAULT_INJECTION, never the released
+// library) shortens it so that a test can make one wait run out quickly.
+#ifdef QFP4_FAULT_INJECTION
+constexpr uint64_t kWaitLimitNs = 5000000ull;      // 5 ms
+#else
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+#endif
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 {

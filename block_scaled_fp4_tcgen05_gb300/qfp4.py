@@ -88,6 +88,31 @@ def load() -> ctypes.CDLL:
         return _lib
 
 
+FAULTINJ_PATH = os.path.join(_HERE, "libqfp4_faultinj.so")
+_faultinj = None
+
+
+def load_fault_injection() -> ctypes.CDLL:
+    """Open the fault-injection test build (libqfp4_faultinj.so, built by
+    build.build(variant="faultinj")): the same entry points with a 5 ms wait
+    limit, plus qfp4_test_inject_skip_release(int).  For tests only; the
+    product path always uses load()."""
+    global _faultinj
+    with _lock:
+        if _faultinj is None:
+            if not os.path.exists(FAULTINJ_PATH):
+                raise RuntimeError(f"fault-injection build missing ({FAULTINJ_PATH})")
+            lib = ctypes.CDLL(FAULTINJ_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            lib.qfp4_test_inject_skip_release.restype = _i32
+            lib.qfp4_test_inject_skip_release.argtypes = [_i32]
+            _faultinj = lib
+        return _faultinj
+
+
 def status_string(status: int) -> str:
     return load().qfp4_status_string(int(status)).decode()
 

@@ -313,7 +313,19 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const int mid = (lo + hi + 1) >> 1;
                 if (s_ptile[mid] <= mt_all) lo = mid; else hi = mid - 1;
             }
-            const int32_t mt = mt_all - s_ptile[lo];
+            // within the expert, the same raster as the dense schedule:
+            // groups of up to 8 row tiles walk the column tiles together, so
+            // the pairs of one round share B tiles (an expert's whole weight
+            // slab would otherwise stream through L2 every round)
+            constexpr int32_t GM = 8;
+            const int32_t lt = t - s_ptile[lo] * ntiles_n;
+            const int32_t mtiles_e = s_ptile[lo + 1] - s_ptile[lo];
+            const int32_t per_group = GM * ntiles_n;
+            const int32_t first_m = (lt / per_group) * GM;
+            const int32_t rows_here = min(GM, mtiles_e - first_m);
+            const int32_t idx = lt % per_group;
+            const int32_t mt = first_m + idx % rows_here;
+            ti.n0 = (idx / rows_here) * 256;
             ti.group = lo;
             ti.row0 = s_offs[lo] + mt * 256;
             ti.row_end = s_offs[lo + 1];

@@ -472,24 +472,14 @@ def sweep(device, l2_bytes, peaks):
         del X, Q, SF
     # residual add + RMSNorm + NVFP4 quantisation (per-row global scales) on X[16384, 4096]
     M, K = synth.QUANT_ROWS, synth.QUANT_COLS
-    X = torch.from_numpy(synth.activations_bf16(synth.QUANT_SEED, M, K).view(np.int16).copy()).view(
-        torch.bfloat16).to(device)
-    R = torch.from_numpy(synth.activations_bf16(synth.QUANT_SEED + 1, M, K).view(np.int16).copy()).view(
-        torch.bfloat16).to(device)
-    gamma = torch.from_numpy(synth.norm_weight_bf16(synth.QUANT_SEED + 2, K).view(np.int16).copy()).view(
-        torch.bfloat16).to(device)
-    Y = torch.empty_like(X)
-    gs_rows = torch.empty(M, dtype=torch.float32, device=device)
-    Q = torch.empty((M, K // 2), dtype=torch.uint8, device=device)
-    SF = torch.empty(qfp4.sf_mma_bytes(M, K // 16), dtype=torch.uint8, device=device)
+    call = rmsnorm_call(device)
     # X, R and Y (400 MB) exceed the L2, so back-to-back launches stream from HBM
-    ms = graph_time([lambda: qfp4.residual_rmsnorm_quantize(qfp4.NVFP4, X, R, gamma, 1e-6, Y, gs_rows, Q, SF,
-                                                            qfp4.SF_MMA)] * 8)
+    ms = graph_time([call] * 8)
     byts = 3 * 2 * M * K + M * K / 2 + M * K / 16 + 4 * M
     gbs = byts / (ms * 1e-3) / 1e9
     out.append({"workload": f"nvfp4_residual_rmsnorm_quantize_{M}x{K}", "us": round(ms * 1e3, 2),
                 "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 3)})
-    del X, R, gamma, Y, gs_rows, Q, SF
+    del call
     # the step on the prefill-attention shape 4096^3 (global scale, quantise, GEMM), L2 flushed
     pipe = Pipeline(synth.PREFILL_NV, device)
     flush = Flush(device)
@@ -526,7 +516,84 @@ def sweep(device, l2_bytes, peaks):
     return out
 
 
+# sweep workload -> the key of its ncu DRAM counters in profiles/dram_traffic.json
+SWEEP_TRAFFIC = {
+    "nvfp4_quantize_16384x4096": "quantize_kernel nvfp4 16384x4096",
+    "nvfp4_gemm_nt_128x14336x4096": "gemm_decode_kernel nvfp4 128x14336x4096",
+    "nvfp4_gemm_nt_128x4096x4096": "gemm_decode_kernel nvfp4 128x4096x4096",
+    "nvfp4_gemm_nt_4096x4096x4096": "gemm_pair_kernel nvfp4 4096x4096x4096",
+    "nvfp4_gemm_nt_8192x8192x8192": "gemm_pair_kernel nvfp4 8192x8192x8192",
+    "nvfp4_grouped_up_4096tok_top2_8exp": "gemm_pair_kernel grouped nvfp4 moe_up_8x14336x4096",
+    "nvfp4_swiglu_up_4096x7168x4096": "gemm_pair_kernel swiglu nvfp4 4096x7168x4096",
+    "nvfp4_b32_sparse24_gemm_nt_8192x8192x8192": "gemm_sparse_kernel nvfp4_b32 8192x8192x8192",
+    "nvfp4_residual_rmsnorm_quantize_16384x4096": "rmsnorm_quant_kernel nvfp4 16384x4096",
+}
+
+
+def attach_traffic(entries):
+    """Adds each sweep entry's DRAM bytes per launch from its committed ncu
+    summary (absent when the kernel source changed since the capture)."""
+    for e in entries:
+        key = SWEEP_TRAFFIC.get(e.get("workload"))
+        t = ncu_traffic(key) if key else None
+        if t is not None:
+            e["ncu_dram_bytes_per_launch"] = t
+            e["ncu_key"] = key
+    return entries
+
+
 SPARSE_SHAPES = ((4096, 4096, 4096), (4096, 14336, 4096), (4096, 4096, 14336), (8192, 8192, 8192))
+
+
+def sparse_operands(device, M, N, K):
+    """Operands of the 2:4 pair-sparse GEMM: X quantised to NVFP4 with 32-element
+    scale blocks; W likewise, pruned to two of every four pair bytes (a seeded
+    pattern) and compressed; D.  Returns (Qx, SFx, Wc, meta, SFw, gx, gw, D)."""
+    import torch
+    from block_scaled_fp4_tcgen05_gb300 import qfp4
+    X = torch.from_numpy(synth.activations_bf16(synth.SEED_BASE + 11, M, K).view(np.int16).copy()).view(
+        torch.bfloat16).to(device)
+    W = torch.from_numpy(synth.weights_bf16(synth.SEED_BASE + 12, N, K).view(np.int16).copy()).view(
+        torch.bfloat16).to(device)
+    gx = torch.empty(1, dtype=torch.float32, device=device)
+    gw = torch.empty(1, dtype=torch.float32, device=device)
+    qfp4.global_scale(X, gx)
+    qfp4.global_scale(W, gw)
+    Qx = torch.empty((M, K // 2), dtype=torch.uint8, device=device)
+    SFx = torch.empty(qfp4.sf_mma_bytes(M, K // 32), dtype=torch.uint8, device=device)
+    qfp4.quantize(qfp4.NVFP4_B32, X, gx, Qx, SFx, qfp4.SF_MMA)
+    Qw = torch.empty((N, K // 2), dtype=torch.uint8, device=device)
+    SFw = torch.empty(qfp4.sf_mma_bytes(N, K // 32), dtype=torch.uint8, device=device)
+    qfp4.quantize(qfp4.NVFP4_B32, W, gw, Qw, SFw, qfp4.SF_MMA)
+    del X, W
+    gen = torch.Generator(device=device).manual_seed(synth.SEED_BASE + 13)
+    keep = torch.rand((N, K // 8, 4), generator=gen, device=device).argsort(dim=2)[..., :2]
+    mask = torch.zeros((N, K // 8, 4), dtype=torch.bool, device=device).scatter_(2, keep, True)
+    Qw = torch.where(mask.view(N, K // 2), Qw, torch.zeros_like(Qw))
+    Wc = torch.empty((N, K // 4), dtype=torch.uint8, device=device)
+    meta = torch.empty(qfp4.sparse24_meta_bytes(N, K, qfp4.SF_MMA), dtype=torch.uint8, device=device)
+    qfp4.sparse24_compress(Qw, Wc, meta, qfp4.SF_MMA)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    return Qx, SFx, Wc, meta, SFw, gx, gw, D
+
+
+def rmsnorm_call(device):
+    """The residual-add + RMSNorm NVFP4 quantiser on X[16384, 4096] with a
+    residual and per-row global scales, MMA-layout scales; returns the call."""
+    import torch
+    from block_scaled_fp4_tcgen05_gb300 import qfp4
+    M, K = synth.QUANT_ROWS, synth.QUANT_COLS
+    X = torch.from_numpy(synth.activations_bf16(synth.QUANT_SEED, M, K).view(np.int16).copy()).view(
+        torch.bfloat16).to(device)
+    R = torch.from_numpy(synth.activations_bf16(synth.QUANT_SEED + 1, M, K).view(np.int16).copy()).view(
+        torch.bfloat16).to(device)
+    gamma = torch.from_numpy(synth.norm_weight_bf16(synth.QUANT_SEED + 2, K).view(np.int16).copy()).view(
+        torch.bfloat16).to(device)
+    Y = torch.empty_like(X)
+    gs_rows = torch.empty(M, dtype=torch.float32, device=device)
+    Q = torch.empty((M, K // 2), dtype=torch.uint8, device=device)
+    SF = torch.empty(qfp4.sf_mma_bytes(M, K // 16), dtype=torch.uint8, device=device)
+    return lambda: qfp4.residual_rmsnorm_quantize(qfp4.NVFP4, X, R, gamma, 1e-6, Y, gs_rows, Q, SF, qfp4.SF_MMA)
 
 
 def sparse_time(device, l2_bytes, fp4_peak):
@@ -539,31 +606,7 @@ def sparse_time(device, l2_bytes, fp4_peak):
     from block_scaled_fp4_tcgen05_gb300 import qfp4
     out = []
     for (M, N, K) in SPARSE_SHAPES:
-        X = torch.from_numpy(synth.activations_bf16(synth.SEED_BASE + 11, M, K).view(np.int16).copy()).view(
-            torch.bfloat16).to(device)
-        W = torch.from_numpy(synth.weights_bf16(synth.SEED_BASE + 12, N, K).view(np.int16).copy()).view(
-            torch.bfloat16).to(device)
-        gx = torch.empty(1, dtype=torch.float32, device=device)
-        gw = torch.empty(1, dtype=torch.float32, device=device)
-        qfp4.global_scale(X, gx)
-        qfp4.global_scale(W, gw)
-        Qx = torch.empty((M, K // 2), dtype=torch.uint8, device=device)
-        SFx = torch.empty(qfp4.sf_mma_bytes(M, K // 32), dtype=torch.uint8, device=device)
-        qfp4.quantize(qfp4.NVFP4_B32, X, gx, Qx, SFx, qfp4.SF_MMA)
-        Qw = torch.empty((N, K // 2), dtype=torch.uint8, device=device)
-        SFw = torch.empty(qfp4.sf_mma_bytes(N, K // 32), dtype=torch.uint8, device=device)
-        qfp4.quantize(qfp4.NVFP4_B32, W, gw, Qw, SFw, qfp4.SF_MMA)
-        del X, W
-        # 2:4 pair pruning: keep two of every four pair bytes (a seeded pattern)
-        gen = torch.Generator(device=device).manual_seed(synth.SEED_BASE + 13)
-        keep = torch.rand((N, K // 8, 4), generator=gen, device=device).argsort(dim=2)[..., :2]
-        mask = torch.zeros((N, K // 8, 4), dtype=torch.bool, device=device).scatter_(2, keep, True)
-        Qw = torch.where(mask.view(N, K // 2), Qw, torch.zeros_like(Qw))
-        Wc = torch.empty((N, K // 4), dtype=torch.uint8, device=device)
-        meta = torch.empty(qfp4.sparse24_meta_bytes(N, K, qfp4.SF_MMA), dtype=torch.uint8, device=device)
-        qfp4.sparse24_compress(Qw, Wc, meta, qfp4.SF_MMA)
-        del Qw, mask, keep
-        D = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        Qx, SFx, Wc, meta, SFw, gx, gw, D = sparse_operands(device, M, N, K)
         wbytes = Wc.numel() + meta.numel() + SFw.numel()
         copies = max(1, min(16, int(np.ceil(2 * l2_bytes / wbytes)) + 1))
         Wcs = [Wc] + [Wc.clone() for _ in range(copies - 1)]
@@ -633,12 +676,11 @@ def two_level_time(device, l2_bytes, fp4_peak):
     return res
 
 
-def swiglu_time(device, l2_bytes, fp4_peak, grouped):
-    """Up-projection with SwiGLU and NVFP4 requantisation fused into the
-    epilogue, against the plain GEMM writing BF16 on the same operands:
-    dense 4096 tokens x I = 7168 x K = 4096 (W: 14336 gate/up rows), or the
-    top-2-of-8 MoE batch of the grouped workload with I = 7168 per expert.
-    Weights rotated past the L2 (dense) or the L2 flushed (grouped)."""
+def swiglu_setup(device, l2_bytes, grouped):
+    """Operands of the SwiGLU up-projection (dense 4096 tokens x I = 7168 x
+    K = 4096, W: 14336 gate/up rows; or the top-2-of-8 MoE batch with I = 7168
+    per expert).  Returns (fused(i), plain(i), copies, rows, I, K, Qh, SFh, D):
+    call i uses weight copy i (dense weights are rotated past the L2)."""
     import torch
     from block_scaled_fp4_tcgen05_gb300 import qfp4
     fmt, g, K = qfp4.NVFP4, 16, 4096
@@ -690,6 +732,16 @@ def swiglu_time(device, l2_bytes, fp4_peak, grouped):
 
         def plain(i):
             qfp4.gemm_nt(fmt, rows, 2 * I, K, Qa, SFa, Qs[i], SFs[i], gs_a, gs_w, D)
+    return fused, plain, copies, rows, I, K, Qh, SFh, D
+
+
+def swiglu_time(device, l2_bytes, fp4_peak, grouped):
+    """Up-projection with SwiGLU and NVFP4 requantisation fused into the
+    epilogue, against the plain GEMM writing BF16 on the same operands.
+    Weights rotated past the L2 (dense) or the L2 flushed (grouped)."""
+    import torch
+    from block_scaled_fp4_tcgen05_gb300 import qfp4
+    fused, plain, copies, rows, I, K, Qh, SFh, D = swiglu_setup(device, l2_bytes, grouped)
     if grouped:
         flush = Flush(device)
 
@@ -722,7 +774,10 @@ def swiglu_time(device, l2_bytes, fp4_peak, grouped):
             "bytes_out_fused": int(Qh.numel() + SFh.numel()), "bytes_out_bf16": int(D.numel() * 2)}
 
 
-def grouped_time(device, fp4_peak):
+def grouped_setup(device):
+    """Operands of the grouped MoE up-projection (quantised weights; the
+    activations' global scales and quantisation are the prologue).  Returns
+    (prologue(), gemm(), rows, counts)."""
     import torch
     from block_scaled_fp4_tcgen05_gb300 import qfp4
     case = synth.MOE_UP
@@ -747,14 +802,24 @@ def grouped_time(device, fp4_peak):
     qfp4.quantize_grouped(case.fmt, W, w_offs, gs_b, Qb, SFb)
     del W
 
-    def step():
+    def prologue():
         qfp4.global_scale_grouped(X, d_offs, gs_a)
         qfp4.quantize_grouped(case.fmt, X, d_offs, gs_a, Qa, SFa)
+
+    def gemm():
         qfp4.gemm_nt_grouped(case.fmt, d_offs, rows, int(counts.max()), N, K, Qa, SFa, Qb, SFb,
                              gs_a, gs_b, D)
+    return prologue, gemm, rows, counts
 
+
+def grouped_time(device, fp4_peak):
+    import torch
+    case = synth.MOE_UP
+    N, K = case.N, case.K
+    prologue, gemm, rows, counts = grouped_setup(device)
     for _ in range(3):
-        step()
+        prologue()
+        gemm()
     torch.cuda.synchronize()
     flush = Flush(device)
     ts, gts = [], []
@@ -762,11 +827,9 @@ def grouped_time(device, fp4_peak):
         flush()
         s, m, e = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         s.record()
-        qfp4.global_scale_grouped(X, d_offs, gs_a)
-        qfp4.quantize_grouped(case.fmt, X, d_offs, gs_a, Qa, SFa)
+        prologue()
         m.record()
-        qfp4.gemm_nt_grouped(case.fmt, d_offs, rows, int(counts.max()), N, K, Qa, SFa, Qb, SFb,
-                             gs_a, gs_b, D)
+        gemm()
         e.record()
         torch.cuda.synchronize()
         ts.append(s.elapsed_time(e))
@@ -798,6 +861,22 @@ def single_kernel(args, device):
         SF = torch.empty(qfp4.sf_mma_bytes(M, K // g), dtype=torch.uint8, device=device)
         run = lambda: qfp4.quantize(fmt, X, gs, Q, SF, qfp4.SF_MMA)
         workload = f"{name}_{M}x{K}"
+    elif name == "rmsnorm":
+        run = rmsnorm_call(device)
+        workload = f"nvfp4_residual_rmsnorm_quantize_{synth.QUANT_ROWS}x{synth.QUANT_COLS}"
+    elif name == "sparse":
+        M = N = K = 8192
+        Qx, SFx, Wc, meta, SFw, gx, gw, D = sparse_operands(device, M, N, K)
+        run = lambda: qfp4.gemm_nt_sparse24(qfp4.NVFP4_B32, M, N, K, Qx, SFx, Wc, meta, SFw, gx, gw, D)
+        workload = f"nvfp4_b32_sparse24_gemm_nt_{M}x{N}x{K}"
+    elif name == "grouped":
+        prologue, run, _, _ = grouped_setup(device)
+        prologue()
+        workload = synth.MOE_UP.name
+    elif name == "swiglu":
+        fused, _, _, rows, I, K, _, _, _ = swiglu_setup(device, 0, False)
+        run = lambda: fused(0)
+        workload = f"nvfp4_swiglu_up_{rows}x{I}x{K}"
     else:
         case = {"decode_up": synth.DECODE_UP, "decode_attn": synth.DECODE_ATTN,
                 "prefill": synth.PREFILL_NV, "square": synth.SQUARE_NV}[name]
@@ -894,7 +973,7 @@ def main():
                     help="seconds of clock-sampled steps ahead of the timed ones (0 for profiler runs)")
     ap.add_argument("--kernel", default=None,
                     choices=["quantize_nvfp4", "quantize_mxfp4", "decode_up", "decode_attn", "prefill",
-                             "square"],
+                             "square", "grouped", "swiglu", "sparse", "rmsnorm"],
                     help="launch only this kernel (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -972,7 +1051,7 @@ def main():
                                 "(profiles/dram_traffic.json is keyed to the source it was captured on)")
     del pipe
     torch.cuda.empty_cache()
-    extra = [] if args.no_sweep else sweep(device, l2_bytes, peaks)
+    extra = [] if args.no_sweep else attach_traffic(sweep(device, l2_bytes, peaks))
     cpu = None if args.no_cpu else cpu_baseline(case)
     line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),

@@ -7,8 +7,13 @@
 //
 // Swap AB: the weights B [N, K] take the MMA's M slot and the <= 128 tokens
 // of A take its N slot, so the tensor core computes D^T.  A CTA pair owns 256
-// weight rows (128 per CTA) and all K: ceil(N / 256) pairs, no split-K and no
-// cross-CTA reduction (N = 14336: 56 pairs on 112 SMs).  Per 256-K block the
+// weight rows (128 per CTA) and, by default, all of K: ceil(N / 256) pairs
+// and no cross-CTA reduction (N = 14336: 56 pairs on 112 SMs).  When that
+// leaves the GPU short of pairs and K is long enough for it to pay (see
+// decode_splits), SPLITK gives each weight tile S pairs with contiguous K
+// ranges: fp32 partials go to the caller's workspace, and after a counted
+// barrier the S CTAs of a rank each reduce a slice of the columns in split
+// order (deterministic) and write D.  Per 256-K block the
 // leader issues four M=256 N=128 K=64 MMAs (each CTA's tensor memory
 // receives its 128 weight rows x 128 tokens); each CTA streams 16 KB of
 // weights, 8 KB of tokens (its half of N) and 4 KB of scale factors.

@@ -122,6 +122,30 @@ __device__ __forceinline__ float scale_target(float amax, float gs, float inv_gs
     return gs == 1.0f ? __fdiv_rn(amax, 6.0f) : __fdiv_rn(__fdiv_rn(amax, 6.0f), gs);
 }
 
+// UE4M3 scale byte of a block with maximum magnitude amax under global
+// scale gs (inv_gs = RN(1/gs)).  t is NaN only when amax and gs are both 0
+// (0/0: an all-zero block under a zero global scale) and then takes code 0
+// like t = 0; a non-zero block with gs = 0 has t = +inf and saturates to 0x7E
+// (s = 448 * 0 = 0 then still encodes it as zeros).
+__device__ __forceinline__ uint32_t nvfp4_scale_code(float amax, float gs, float inv_gs)
+{
+    const float t = scale_target(amax, gs, inv_gs);
+    return t > 0.0f ? ue4m3_encode(t) : 0u;
+}
+
+// The element-step parameters of an NVFP4 block from its scale s =
+// decode(code) * gs and y = RN(1/s) (0 when s is 0).
+__device__ __forceinline__ BlockScale nvfp4_block(uint32_t code, float s, float y, float amax)
+{
+    BlockScale b;
+    b.code = code;
+    b.s = s;
+    b.inv = y;
+    const bool fast = s >= 0x1p-64f && s <= 0x1p64f && amax <= s * 0x1p60f;
+    b.mode = s == 0.0f ? 0 : fast ? 1 : 2;
+    return b;
+}
+
 template <int FMT>
 __device__ __forceinline__ BlockScale block_scale(float amax, float gs, float inv_gs)
 {
@@ -133,21 +157,9 @@ __device__ __forceinline__ BlockScale block_scale(float amax, float gs, float in
         b.s = 0.0f;
         b.mode = 1;
     } else {
-        const float t = scale_target(amax, gs, inv_gs);
-        // t is NaN only when amax and gs are both 0 (0/0: an all-zero
-        // block under a zero global scale) and then takes code 0 like t = 0;
-        // a non-zero block with gs = 0 has t = +inf and saturates to 0x7E,
-        // and s = 448 * 0 = 0 still encodes it as zeros
-        b.code = t > 0.0f ? ue4m3_encode(t) : 0u;
-        b.s = __fmul_rn(ue4m3_decode(b.code), gs);
-        if (b.s == 0.0f) {
-            b.mode = 0;
-            b.inv = 0.0f;
-        } else {
-            b.inv = __frcp_rn(b.s);
-            const bool fast = b.s >= 0x1p-64f && b.s <= 0x1p64f && amax <= b.s * 0x1p60f;
-            b.mode = fast ? 1 : 2;
-        }
+        const uint32_t code = nvfp4_scale_code(amax, gs, inv_gs);
+        const float s = __fmul_rn(ue4m3_decode(code), gs);
+        b = nvfp4_block(code, s, s == 0.0f ? 0.0f : __frcp_rn(s), amax);
     }
     return b;
 }

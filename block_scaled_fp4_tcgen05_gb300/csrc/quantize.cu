@@ -203,6 +203,24 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
     const float gs_one = (FMT == QFP4_MXFP4 || GROUPED || ROWGS) ? 1.0f : *gs_ptr;
     const float inv_gs_one = __frcp_rn(gs_one);
 
+    // One NVFP4 global scale for the whole tensor: the scale codes come from
+    // a table.  A block's code is a non-decreasing function of its amax (the
+    // roundings in t = (amax / 6) / gs and the UE4M3 encoding are monotone),
+    // so s_thr[c], the least bf16 magnitude whose code is at least c (found
+    // by bisection with nvfp4_scale_code itself), decides it: the estimate
+    // c0 = UE4M3(amax * RN(RN(1/6) * RN(1/gs))) is within 2^-21 of t
+    // relatively, while UE4M3 rounding boundaries lie at least 2^-4 apart
+    // (and both saturate at 448), so c0 is at most one code off and one
+    // comparison each way with s_thr[c0] and s_thr[c0 + 1] corrects it.
+    // s_sy[c] holds s = decode(c) * gs and RN(1/s).  For gs in
+    // [2^-100, 2^100] no factor of the estimate leaves the normal range; other
+    // global scales take block_scale for every block.
+    constexpr bool TABLE = FMT == QFP4_NVFP4 && !GROUPED && !ROWGS;
+    __shared__ float s_thr[TABLE ? 128 : 1];
+    __shared__ float2 s_sy[TABLE ? 128 : 1];
+    const bool use_table = TABLE && gs_one >= 0x1p-100f && gs_one <= 0x1p100f;
+    const float est_k = __fmul_rn(0x1.555556p-3f, inv_gs_one);     // RN(1/6) * RN(1/gs)
+
     // MMA layout without groups: zero the padding rows [M, ceil128(M)).
     if (SF_LAYOUT == QFP4_SF_MMA && !GROUPED) {
         const int64_t mp = (M + 127) / 128 * 128;
@@ -252,6 +270,33 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
         }
         return;
     }
+    if (TABLE && use_table) {
+        // (consumer threads only: the producer warp is already streaming)
+        if (threadIdx.x < 128) {
+            const uint32_t c = threadIdx.x;
+            float th;
+            if (c == 0) {
+                th = 0.0f;
+            } else if (c == 127) {
+                th = __uint_as_float(0x7FC00000u);             // NaN: no amax compares >= it
+            } else {
+                uint32_t lo = 0, hi = 0x7F80u;                 // +inf has code 126 >= c
+#pragma unroll 1
+                for (int i = 0; i < 16; ++i) {
+                    if (lo < hi) {
+                        const uint32_t mid = (lo + hi) >> 1;
+                        if (nvfp4_scale_code(__uint_as_float(mid << 16), gs_one, inv_gs_one) >= c) hi = mid;
+                        else lo = mid + 1;
+                    }
+                }
+                th = __uint_as_float(lo << 16);
+            }
+            s_thr[c] = th;
+            const float sc = __fmul_rn(ue4m3_decode(c < 127 ? c : 126u), gs_one);
+            s_sy[c] = make_float2(sc, sc == 0.0f ? 0.0f : __frcp_rn(sc));
+        }
+        named_barrier_sync(1, kThreads);
+    }
     uint32_t it = 0;
     for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++it) {
         const uint32_t st = it % kQStages;
@@ -286,7 +331,16 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
                 gs = gs_ptr[row];
                 inv_gs = __frcp_rn(gs);
             }
-            const BlockScale bs = block_scale<FMT>(amax, gs, inv_gs);
+            BlockScale bs;
+            if (TABLE && use_table) {
+                const float x = __fmul_rn(amax, est_k);
+                const uint32_t c0 = x > 0.0f ? ue4m3_encode(x) : 0u;        // 0..126 (NaN: 0)
+                const uint32_t code = c0 + (amax >= s_thr[c0 + 1] ? 1u : 0u) - (amax < s_thr[c0] ? 1u : 0u);
+                const float2 sy = s_sy[code];
+                bs = nvfp4_block(code, sy.x, sy.y, amax);
+            } else {
+                bs = block_scale<FMT>(amax, gs, inv_gs);
+            }
             uint32_t packed[W / 4];
 #pragma unroll
             for (int v = 0; v < W / 4; ++v) packed[v] = encode8<FMT>(&w[4 * v], bs);

@@ -257,3 +257,37 @@ def test_quantize_exhaustive_element_path(fmt, gs):
     x, ncodes = exhaustive_input(fmt, gs if gs is not None else np.float32(1.0))
     assert ncodes >= (100 if fmt == NV else 200)
     check_quantize(fmt, x, gs)
+
+
+def every_amax_input(seed):
+    """One NVFP4 block per positive finite bf16 magnitude v (bit patterns
+    0x0000..0x7F7F): v at a random position, the other 15 elements random
+    fractions of v (rounded to bf16, so never above v), every sign random;
+    rows of 256 blocks, zero-padded."""
+    gen = synth.rng(seed)
+    vals = np.arange(0, 0x7F80, dtype=np.uint32)
+    amax = (vals << 16).view(np.float32)
+    n = len(vals)
+    others = synth.f32_to_bf16_bits(amax[:, None] * gen.random((n, 15)).astype(np.float32))
+    blk = np.concatenate([vals.astype(np.uint16)[:, None], others], axis=1)
+    blk = np.take_along_axis(blk, gen.permuted(np.tile(np.arange(16), (n, 1)), axis=1), axis=1)
+    blk = np.where(gen.random((n, 16)) < 0.5, blk | np.uint16(0x8000), blk).astype(np.uint16)
+    pad = (-n) % 256
+    blk = np.concatenate([blk, np.zeros((pad, 16), np.uint16)])
+    return blk.reshape(-1, 256 * 16)
+
+
+_RANDOM_GS = [np.float32(2.0 ** e) for e in synth.rng(12).uniform(-100.0, 100.0, 4)]
+
+
+@pytest.mark.parametrize("gs", [np.float32(1.0), np.float32(0.01371), np.float32(7.3e-6), np.float32(3.1e-3),
+                                np.float32(1e-30), np.float32(7e25), np.float32(2.0 ** -100),
+                                np.float32(2.0 ** 100), np.float32(2.0 ** -101), np.float32(1.5 * 2.0 ** 100)]
+                         + _RANDOM_GS)
+def test_quantize_nvfp4_every_block_amax(gs):
+    """Bit-exact against the oracle with every positive finite bf16 magnitude
+    as the maximum of some block: pins the scale code of every amax a
+    per-tensor NVFP4 quantisation can see, for global scales inside and just
+    outside [2^-100, 2^100] (where the kernel reads codes from a table built
+    at launch) and for random ones across that range."""
+    check_quantize(NV, every_amax_input(31), gs)

@@ -348,12 +348,15 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
                 if (G == 16) *reinterpret_cast<uint2 *>(Q + static_cast<size_t>(bu) * (G / 2)) = make_uint2(packed[0], packed[1]);
                 else *reinterpret_cast<uint4 *>(Q + static_cast<size_t>(bu) * (G / 2)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             }
-            // Scale bytes: lanes 4i..4i+3 hold four consecutive blocks of one row.
-            const uint32_t c1 = __shfl_down_sync(0xffffffffu, bs.code, 1);
-            const uint32_t c2 = __shfl_down_sync(0xffffffffu, bs.code, 2);
-            const uint32_t c3 = __shfl_down_sync(0xffffffffu, bs.code, 3);
-            if (valid && (lane & 3) == 0) {
-                const uint32_t word = bs.code | (c1 << 8) | (c2 << 16) | (c3 << 24);
+            // Scale bytes: lanes 4i..4i+3 hold four consecutive blocks of one
+            // row, whose bytes are adjacent in both layouts.  NVFP4 stores one
+            // byte per lane (the four stores of a word go out in one warp
+            // instruction); MXFP4, with half as many blocks, gathers each word
+            // into its first lane (measured faster there).
+            const uint32_t c1 = FMT == QFP4_NVFP4 ? 0u : __shfl_down_sync(0xffffffffu, bs.code, 1);
+            const uint32_t c2 = FMT == QFP4_NVFP4 ? 0u : __shfl_down_sync(0xffffffffu, bs.code, 2);
+            const uint32_t c3 = FMT == QFP4_NVFP4 ? 0u : __shfl_down_sync(0xffffffffu, bs.code, 3);
+            if (valid && (FMT == QFP4_NVFP4 || (lane & 3) == 0)) {
                 const uint32_t col = bu - row * kg;
                 size_t off;
                 if (GROUPED) {
@@ -364,7 +367,8 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
                 } else {
                     off = bu;
                 }
-                *reinterpret_cast<uint32_t *>(SF + off) = word;
+                if (FMT == QFP4_NVFP4) SF[off] = static_cast<uint8_t>(bs.code);
+                else *reinterpret_cast<uint32_t *>(SF + off) = bs.code | (c1 << 8) | (c2 << 16) | (c3 << 24);
             }
         }
         __syncwarp();

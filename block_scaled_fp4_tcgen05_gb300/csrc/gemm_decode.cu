@@ -24,10 +24,10 @@
 // the MMA issuer; warps 4..11, two sets of four taking alternate K-blocks,
 // move the scale bytes into tensor memory with tcgen05.st (the tensor pipe
 // then runs MMAs only; one set alone, waiting for each store to complete,
-// would take about a K-block's streaming time per K-block); at the end warps
-// 4..7 drain the accumulator: scale by gs_a * gs_b, round to BF16, transpose
-// through shared memory and write D with one TMA store per CTA.  All waits
-// are bounded.
+// would take about a K-block's streaming time per K-block); at the end both
+// sets drain the accumulator, each half of the tokens: scale by gs_a * gs_b,
+// round to BF16, transpose through shared memory and write D with one TMA
+// store per CTA.  All waits are bounded.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -381,10 +381,11 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             *abort_flag = 1;
         }
         }
-        if (!SPLITK && set == 0) {
+        if (!SPLITK) {
         // -------------------------------------------- accumulator drain
-        // Lane 32q + i of tensor memory is weight row n = 32q + i of this
-        // CTA; column m is token m.  Each thread writes D[m][n] for its n
+        // Both scale sets drain, set s the tokens 64s .. 64s + 63.  Lane
+        // 32q + i of tensor memory is weight row n = 32q + i of this CTA;
+        // column m is token m.  Each thread writes D[m][n] for its n
         // into a row-major [128 tokens][128 columns] BF16 tile in shared
         // memory (a warp writes 64 consecutive bytes per token), and one
         // TMA store moves the tile to D; rows m >= M are clipped by it.
@@ -416,7 +417,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             const bool odd = lane & 1;
             const int n0 = n & ~1;
             const int nchunks = (p.M + 31) / 32;
-            for (int j = 0; j < nchunks; ++j) {
+            for (int j = 2 * set; j < nchunks && j < 2 * set + 2; ++j) {   // set s: tokens 64s..64s+63
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(taddr + j * 32, v);
                 tmem_ld_wait();
@@ -446,7 +447,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             *abort_flag = 1;
         }
         __syncwarp();
-        named_barrier_sync(1, 4 * 32);
+        named_barrier_sync(1, 8 * 32);
         if (warp == 4 && lane == 0 && !*abort_flag && w_valid) {
             tma_store_2d(&tmD, smem_u32(smem), wtile * 128, 0);
             bulk_commit_group();

@@ -97,6 +97,8 @@ def _load():
             "oracle_e2m1_round_n": (c_int, [c_p, c_i64, c_p]),
             "oracle_scale_round_n": (c_int, [c_int, c_p, c_i64, c_p]),
             "oracle_num_threads": (c_int, []),
+            "oracle_scale_codes_bits": (c_int, [c_int, ctypes.c_uint32, c_i64, ctypes.c_float, c_p]),
+            "oracle_element_codes_bits": (c_int, [ctypes.c_uint32, c_i64, ctypes.c_float, c_p]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -510,6 +512,24 @@ def gemm_nt_sparse24(fmt: int, A, A_sf, Wc, meta, W_sf, gs_a: float = 1.0, gs_w:
     decompressed operand (its scale factors are those of the dense K)."""
     K = np.asarray(A).shape[1] * 2
     return gemm_nt(fmt, A, A_sf, sparse24_decompress(Wc, meta, K), W_sf, gs_a, gs_w)
+
+
+def scale_codes_bits(fmt: int, first: int, n: int, gs=1.0) -> np.ndarray:
+    """Scale bytes the quantiser's rule gives for amax = the floats whose
+    bit patterns are first .. first + n - 1 (no NaN or Inf among them)."""
+    out = np.empty(n, dtype=np.uint8)
+    if _load().oracle_scale_codes_bits(fmt, first, n, float(np.float32(gs)), _ptr(out)) != 0:
+        raise ValueError("bad range")
+    return out
+
+
+def element_codes_bits(first: int, n: int, s) -> np.ndarray:
+    """E2M1 codes of x / s for x = the floats whose bit patterns are first ..
+    first + n - 1 (no NaN or Inf among them), block scale s > 0."""
+    out = np.empty(n, dtype=np.uint8)
+    if _load().oracle_element_codes_bits(first, n, float(np.float32(s)), _ptr(out)) != 0:
+        raise ValueError("bad range or scale")
+    return out
 
 
 def num_threads() -> int:

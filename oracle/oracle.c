@@ -105,12 +105,18 @@ int oracle_block_size(int fmt) { return fmt == ORACLE_NVFP4 ? 16 : 32; }
 /* Nearest entry of a table of ncodes non-negative values that increase with
  * the code, for a >= 0: the two codes that bracket a are compared (their
  * distances to a are exact in fp64), ties go to the even code, and anything
- * at or above the last value gives the last code (saturation). */
+ * at or above the last value gives the last code (saturation).  The first
+ * code whose value is >= a is found by bisection, which the increasing
+ * values allow. */
 static int nearest_even_code(double a, double (*value)(int), int ncodes)
 {
     if (a >= value(ncodes - 1)) return ncodes - 1;
-    int hi = 0;
-    while (value(hi) < a) ++hi;            /* first code whose value is >= a */
+    int hi = 0, top = ncodes - 1;          /* value(top) > a */
+    while (hi < top) {
+        int mid = (hi + top) / 2;
+        if (value(mid) < a) hi = mid + 1;
+        else top = mid;
+    }
     if (hi == 0) return 0;
     int lo = hi - 1;
     double dlo = a - value(lo), dhi = value(hi) - a;
@@ -615,6 +621,46 @@ int oracle_scale_round_n(int fmt, const float *t, int64_t n, uint8_t *code)
 {
     if (n < 0) return -1;
     for (int64_t i = 0; i < n; ++i) code[i] = (uint8_t)oracle_scale_round(fmt, t[i]);
+    return 0;
+}
+
+/* The quantiser's two rounding steps over ranges of fp32 bit patterns, for
+ * checks against every fp32 input: x_i is the float whose bit pattern is
+ * first + i, for i < n (the caller keeps NaN and Inf patterns out).
+ *   oracle_scale_codes_bits:   the scale step of quantize_block with
+ *                              amax = x_i >= 0: t = (x_i / 6) / gs, two fp32
+ *                              divisions, rounded to the format (gs = 1 for
+ *                              MXFP4);
+ *   oracle_element_codes_bits: the element step for a block scale s > 0:
+ *                              E2M1-round(x_i / s), one fp32 division. */
+static float float_of_bits(uint32_t b)
+{
+    float f;
+    memcpy(&f, &b, sizeof f);
+    return f;
+}
+
+int oracle_scale_codes_bits(int fmt, uint32_t first, int64_t n, float gs, uint8_t *code)
+{
+    if (n < 0 || (uint64_t)first + (uint64_t)n > ((uint64_t)1 << 32)) return -1;
+    if (fmt == ORACLE_MXFP4) gs = 1.0f;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        float amax = float_of_bits(first + (uint32_t)i);
+        float t = (amax / 6.0f) / gs;
+        code[i] = (uint8_t)oracle_scale_round(fmt, t);
+    }
+    return 0;
+}
+
+int oracle_element_codes_bits(uint32_t first, int64_t n, float s, uint8_t *code)
+{
+    if (n < 0 || (uint64_t)first + (uint64_t)n > ((uint64_t)1 << 32) || !(s > 0.0f)) return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        float q = float_of_bits(first + (uint32_t)i) / s;
+        code[i] = (uint8_t)oracle_e2m1_round(q);
+    }
     return 0;
 }
 

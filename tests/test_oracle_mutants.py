@@ -81,6 +81,13 @@ MUTANTS = [
      "code[i] = (uint8_t)(oracle_e2m1_round(q[i]) & 7);"),
     ("scale_round_n_other_format", "code[i] = (uint8_t)oracle_scale_round(fmt, t[i]);",
      "code[i] = (uint8_t)oracle_scale_round(1 - fmt, t[i]);"),
+    ("scale_codes_bits_without_gs",
+     "float t = (amax / 6.0f) / gs;\n        code[i] = (uint8_t)oracle_scale_round(fmt, t);",
+     "float t = amax / 6.0f;\n        code[i] = (uint8_t)oracle_scale_round(fmt, t);"),
+    ("element_codes_bits_multiplies", "float q = float_of_bits(first + (uint32_t)i) / s;",
+     "float q = float_of_bits(first + (uint32_t)i) * s;"),
+    ("element_codes_bits_off_by_one", "float q = float_of_bits(first + (uint32_t)i) / s;",
+     "float q = float_of_bits(first + (uint32_t)i + 1) / s;"),
     # residual add and RMSNorm
     ("bf16_round_truncates", "return (uint16_t)((u + 0x7FFFu + lsb) >> 16);", "return (uint16_t)(u >> 16);"),
     ("bf16_round_ties_up", "return (uint16_t)((u + 0x7FFFu + lsb) >> 16);", "return (uint16_t)((u + 0x8000u) >> 16);"),

@@ -847,3 +847,28 @@ def test_requant_valid_underflowing_scale():
     neg[H < 0] = 8
     Qn = (neg[:, 0::2] | (neg[:, 1::2] << 4)).astype(np.uint8)
     assert not oracle.requant_valid(NV, Qn, SF, H, z, 1.0).any()
+
+
+def test_bit_range_codes_follow_the_quantiser_steps():
+    """The bit-range forms behind the exhaustive GPU check of the encoders:
+    element codes equal E2M1 rounding of numpy's IEEE fp32 quotient x / s,
+    and scale codes equal the scale byte the whole quantiser gives a block
+    whose largest magnitude is that value."""
+    starts = (0x00000000, 0x3E7FFF00, 0x3F7FFF80, 0x40A00000 - 64, 0x7F7FFF00,
+              0x80000000, 0xBF400000 - 100, 0xC0C00000 - 200)
+    n = 256
+    for first in starts:
+        bits = np.arange(first, first + n, dtype=np.uint64).astype(np.uint32)
+        x = bits.view(np.float32)
+        for s in (np.float32(1.0), np.float32(3.0), np.float32(0.37), np.float32(2.0 ** -100)):
+            with np.errstate(over="ignore"):
+                q = x / s
+            assert np.array_equal(oracle.element_codes_bits(first, n, s), oracle.e2m1_round_array(q)), (hex(first), s)
+        if first >= 0x80000000:
+            continue
+        for fmt, gs in ((NV, np.float32(1.0)), (NV, np.float32(0.0137)), (NV, np.float32(1e-30)), (MX, np.float32(1.0))):
+            g = oracle.block_size(fmt)
+            blocks = np.zeros((n, g), np.float32)
+            blocks[:, 3] = x
+            _, sf = oracle.quantize(fmt, blocks, gs)
+            assert np.array_equal(oracle.scale_codes_bits(fmt, first, n, gs), sf[:, 0]), (hex(first), fmt, gs)

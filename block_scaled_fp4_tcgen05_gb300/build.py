@@ -6,7 +6,9 @@ Translation units compile in parallel, then link into
 variant="faultinj" builds the same sources with QFP4_FAULT_INJECTION into
 ``libqfp4_faultinj.so`` (objects in ``_build_faultinj``): a test library whose
 wait limit is 5 ms and which exports qfp4_test_inject_skip_release, so that a
-test can make one bounded wait run out.  The released library never has it.
+test can make one bounded wait run out, and the encoder probes of
+csrc/test_probes.cu, which run the fp32 quantisers' device functions over
+ranges of fp32 bit patterns.  The released library never has them.
 """
 from __future__ import annotations
 

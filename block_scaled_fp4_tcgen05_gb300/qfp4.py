@@ -93,9 +93,10 @@ _faultinj = None
 
 
 def load_fault_injection() -> ctypes.CDLL:
-    """Open the fault-injection test build (libqfp4_faultinj.so, built by
+    """Open the test build (libqfp4_faultinj.so, built by
     build.build(variant="faultinj")): the same entry points with a 5 ms wait
-    limit, plus qfp4_test_inject_skip_release(int).  For tests only; the
+    limit, plus qfp4_test_inject_skip_release(int) and the encoder probes
+    qfp4_test_scale_codes / qfp4_test_element_codes.  For tests only; the
     product path always uses load()."""
     global _faultinj
     with _lock:
@@ -109,6 +110,10 @@ def load_fault_injection() -> ctypes.CDLL:
                 fn.argtypes = args
             lib.qfp4_test_inject_skip_release.restype = _i32
             lib.qfp4_test_inject_skip_release.argtypes = [_i32]
+            for name in ("qfp4_test_scale_codes", "qfp4_test_element_codes"):
+                fn = getattr(lib, name)
+                fn.restype = _i32
+                fn.argtypes = [_i32, ctypes.c_uint32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
             _faultinj = lib
         return _faultinj
 

@@ -276,3 +276,21 @@ def test_swiglu_entry_points_reject_bad_arguments(lib):
     assert G(1, 257, FAKE, 300, 256, 512, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, None) == -2
     assert G(1, 2, FAKE + 2, 300, 256, 512, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, None) == -3
     assert G(0, 2, FAKE, 0, 256, 512, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, FAKE, None) == 0
+
+
+def test_test_build_probes_only_in_the_test_build(lib):
+    """The encoder probes and the fault injection live in the test build only;
+    the probes check their arguments on the host before any launch."""
+    for name in ("qfp4_test_inject_skip_release", "qfp4_test_scale_codes", "qfp4_test_element_codes"):
+        assert not hasattr(lib, name), name
+    if not os.path.exists(qfp4.FAULTINJ_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    t = qfp4.load_fault_injection()
+    dummy = 16
+    assert t.qfp4_test_scale_codes(7, 0, 8, 1.0, dummy, None) == -1      # format
+    assert t.qfp4_test_scale_codes(qfp4.NVFP4, 0, 8, 1.0, None, None) == -1
+    assert t.qfp4_test_scale_codes(qfp4.NVFP4, 0xFFFFFFF0, 32, 1.0, dummy, None) == -1   # past 2^32
+    assert t.qfp4_test_element_codes(qfp4.NVFP4, 0, 8, 0.0, dummy, None) == -1          # s = 0
+    assert t.qfp4_test_element_codes(qfp4.MXFP4, 0, 8, 255.0, dummy, None) == -1        # code 255
+    assert t.qfp4_test_scale_codes(qfp4.NVFP4, 0, 0, 1.0, dummy, None) == 0                         # nothing to do

@@ -495,11 +495,34 @@ def sweep(device, l2_bytes, peaks):
                 "frac_fp4_peak_gemm": round(flop / (statistics.median(gm) * 1e-3) / 1e12 / fp4_peak, 3)})
     del pipe, flush
     # compute-bound sweep
+    us_of = {}
     for case in synth.COMPUTE_SWEEP:
         ms = rotated_gemm_time(case, device, l2_bytes, reps=5)
         tf = 2 * case.M * case.N * case.K / (ms * 1e-3) / 1e12
         out.append({"workload": case.name, "us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
                     "frac_fp4_peak": round(tf / fp4_peak, 3)})
+        us_of[(case.fmt, case.M, case.N, case.K)] = ms * 1e3
+    # NVFP4 / MXFP4 time on the same shapes (the DeepGEMM pull request's
+    # "Benchmark" section reports 1.09-1.16x on B200)
+    for (fmt, M, N, K), us in sorted(us_of.items()):
+        if fmt == qfp4.NVFP4 and (qfp4.MXFP4, M, N, K) in us_of:
+            out.append({"workload": f"nvfp4_over_mxfp4_time_{M}x{N}x{K}",
+                        "ratio": round(us / us_of[(qfp4.MXFP4, M, N, K)], 3)})
+    # scale-factor interleave, row-major -> MMA layout, on the scales of an
+    # NVFP4 [65536, 16384] operand (64 MiB in, 64 MiB out; two buffer sets
+    # rotated so that consecutive launches do not find their input in L2)
+    rows, cols = 65536, 16384 // 16
+    sets = []
+    for _ in range(2):
+        src = torch.randint(0, 0x7F, (rows, cols), dtype=torch.uint8, device=device)
+        dst = torch.empty(qfp4.sf_mma_bytes(rows, cols), dtype=torch.uint8, device=device)
+        sets.append((src, dst))
+    calls = [(lambda a=a, b=b: qfp4.sf_interleave(a, rows, cols, b, qfp4.SF_MMA)) for a, b in sets] * 4
+    ms = graph_time(calls, 10)
+    byts = rows * cols + qfp4.sf_mma_bytes(rows, cols)
+    out.append({"workload": f"sf_interleave_to_mma_{rows}x{cols}", "us": round(ms * 1e3, 2),
+                "GB/s": round(byts / (ms * 1e-3) / 1e9, 1), "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)})
+    del sets, calls
     # 2:4 pair-sparse GEMM against the dense one
     out += sparse_time(device, l2_bytes, fp4_peak)
     # grouped MoE up-projection

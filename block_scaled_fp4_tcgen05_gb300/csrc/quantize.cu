@@ -598,6 +598,50 @@ sf_interleave_kernel(const uint8_t *__restrict__ in, uint8_t *__restrict__ out, 
     }
 }
 
+// Row-major scale bytes [rows, cols] -> MMA layout when cols % 16 == 0 and
+// both buffers are 16-byte aligned.  CTA b takes rows [128 R, 128 R + 128)
+// and columns [32 C, 32 C + w) (w = 32, or 16 for the last chunk of a row
+// whose cols is an odd multiple of 16): w / 4 atoms that lie next to each
+// other in the MMA layout.  Thread t reads its row's w bytes (whole 32-byte
+// sectors), puts word q (columns 4q .. 4q + 3 of the chunk) into atom q at
+// word (t % 32) 4 + t / 32, and the CTA writes the atoms as one contiguous
+// run.  Rows past `rows` are the layout's zero padding.
+__global__ void __launch_bounds__(128)
+sf_to_mma_tiled_kernel(const uint8_t *__restrict__ in, uint8_t *__restrict__ out, int64_t rows, int64_t cols,
+                       int64_t kc, int64_t chunks_per_row)
+{
+    __shared__ __align__(16) uint32_t atoms[8 * 128];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t R = blockIdx.x / chunks_per_row, C = blockIdx.x % chunks_per_row;
+    const int t = threadIdx.x;
+    const int64_t c0 = 32 * C;
+    const int w = cols - c0 >= 32 ? 32 : 16;
+    const int64_t r = 128 * R + t;
+    uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = make_uint4(0u, 0u, 0u, 0u);
+    if (r < rows) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(in + r * cols + c0);
+        v0 = src[0];
+        if (w == 32) v1 = src[1];
+    }
+    const int pos = (t & 31) * 4 + (t >> 5);
+    atoms[0 * 128 + pos] = v0.x;
+    atoms[1 * 128 + pos] = v0.y;
+    atoms[2 * 128 + pos] = v0.z;
+    atoms[3 * 128 + pos] = v0.w;
+    if (w == 32) {
+        atoms[4 * 128 + pos] = v1.x;
+        atoms[5 * 128 + pos] = v1.y;
+        atoms[6 * 128 + pos] = v1.z;
+        atoms[7 * 128 + pos] = v1.w;
+    }
+    __syncthreads();
+    uint4 *dst = reinterpret_cast<uint4 *>(out + (R * kc + 8 * C) * 512);
+    const uint4 *srcs = reinterpret_cast<const uint4 *>(atoms);
+    dst[t] = srcs[t];
+    if (w == 32) dst[t + 128] = srcs[t + 128];
+}
+
 int grid_for(int64_t work_items, int per_block)
 {
     const int sms = sm_count();
@@ -865,6 +909,14 @@ extern "C" int qfp4_sf_interleave(const void *SF_in, int64_t rows, int64_t cols,
     const int64_t kc = (cols + 3) / 4;
     const int64_t words = ((rows + 127) / 128) * kc * 128;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (layout == QFP4_SF_MMA && cols % 16 == 0 && aligned16(SF_in) && aligned16(SF_out)) {
+        const int64_t chunks_per_row = (cols + 31) / 32;
+        const int64_t blocks = ((rows + 127) / 128) * chunks_per_row;
+        if (blocks <= INT32_MAX)
+            return launch_status(launch_pdl(sf_to_mma_tiled_kernel, dim3(static_cast<unsigned>(blocks)), dim3(128), 0,
+                                            s, static_cast<const uint8_t *>(SF_in), static_cast<uint8_t *>(SF_out),
+                                            rows, cols, kc, chunks_per_row));
+    }
     const int grid = grid_for(words, kThreads);
     if (layout == QFP4_SF_MMA)
         return launch_status(launch_pdl(sf_interleave_kernel<true>, dim3(grid), dim3(kThreads), 0, s,

@@ -137,7 +137,7 @@ def test_quantize_full_size_16384x4096(fmt):
     assert np.array_equal(SFm, oracle.sf_to_mma(sf_ref))
 
 
-@pytest.mark.parametrize("rows,cols", [(1, 8), (16, 16), (200, 64), (4096, 256), (16384, 256)])
+@pytest.mark.parametrize("rows,cols", [(1, 8), (16, 16), (200, 64), (130, 48), (4096, 256), (16384, 256)])
 def test_global_scale_bitexact(rows, cols):
     x = synth.activations_bf16(rows * 7 + cols, rows, cols)
     gs = torch.empty(1, dtype=torch.float32, device="cuda")

@@ -173,10 +173,21 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
     uint64_t *empty = full + kQStages;
     __shared__ int32_t s_offs[GROUPED ? kMaxGroups + 1 : 1];
     __shared__ int32_t s_tile0[GROUPED ? kMaxGroups : 1];
+    // NVFP4 per-group global scales and RN(1/gs), read once per CTA
+    constexpr bool GRP_GS = GROUPED && FMT == QFP4_NVFP4 && !ROWGS;
+    __shared__ float s_ggs[GRP_GS ? kMaxGroups : 1];
+    __shared__ float s_ginv[GRP_GS ? kMaxGroups : 1];
     pdl_wait();                 // first global access below
     pdl_launch_dependents();
     if (GROUPED) {
         for (int i = threadIdx.x; i <= groups; i += blockDim.x) s_offs[i] = row_offsets[i];
+    }
+    if (GRP_GS) {
+        for (int i = threadIdx.x; i < groups; i += blockDim.x) {
+            const float g = gs_ptr ? gs_ptr[i] : 1.0f;
+            s_ggs[i] = g;
+            s_ginv[i] = __frcp_rn(g);
+        }
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < kQStages; ++i) {
@@ -322,9 +333,9 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
             float gs = gs_one, inv_gs = inv_gs_one;
             if (GROUPED && valid) {
                 grp = find_group(s_offs, groups, row);
-                if (FMT != QFP4_MXFP4 && gs_ptr && !ROWGS) {
-                    gs = gs_ptr[grp];
-                    inv_gs = __frcp_rn(gs);
+                if (GRP_GS) {
+                    gs = s_ggs[grp];
+                    inv_gs = s_ginv[grp];
                 }
             }
             if (ROWGS && FMT != QFP4_MXFP4 && valid) {

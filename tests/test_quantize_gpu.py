@@ -137,7 +137,7 @@ def test_quantize_full_size_16384x4096(fmt):
     assert np.array_equal(SFm, oracle.sf_to_mma(sf_ref))
 
 
-@pytest.mark.parametrize("rows,cols", [(1, 8), (16, 16), (200, 64), (130, 48), (4096, 256), (16384, 256)])
+@pytest.mark.parametrize("rows,cols", [(1, 8), (16, 16), (200, 64), (4096, 256), (16384, 256)])
 def test_global_scale_bitexact(rows, cols):
     x = synth.activations_bf16(rows * 7 + cols, rows, cols)
     gs = torch.empty(1, dtype=torch.float32, device="cuda")
@@ -189,7 +189,8 @@ def test_quantize_grouped_bitexact(fmt):
     assert SFh[tile * (K // g // 4) * 512:].max(initial=0) == 0
 
 
-@pytest.mark.parametrize("rows,cols", [(1, 1), (128, 4), (129, 7), (300, 64), (4096, 256), (8192, 512)])
+@pytest.mark.parametrize("rows,cols", [(1, 1), (128, 4), (129, 7), (64, 16), (130, 48), (300, 64), (4096, 256),
+                                       (8192, 512)])
 def test_sf_interleave_bitexact(rows, cols):
     sf = synth.rng(rows + cols).integers(0, 255, size=(rows, cols), dtype=np.uint8)
     out = torch.full((qfp4.sf_mma_bytes(rows, cols),), 0x5A, dtype=torch.uint8, device="cuda")
@@ -291,3 +292,51 @@ def test_quantize_nvfp4_every_block_amax(gs):
     outside [2^-100, 2^100] (where the kernel reads codes from a table built
     at launch) and for random ones across that range."""
     check_quantize(NV, every_amax_input(31), gs)
+
+
+def quantize_grouped_check(x, counts, gs_host):
+    """Grouped NVFP4 quantisation of x (bf16 bits) against the oracle, group
+    by group: codes and per-group MMA-layout scale tiles, bit-exact."""
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    K = x.shape[1]
+    Q = torch.empty((int(offs[-1]), K // 2), dtype=torch.uint8, device="cuda")
+    SF = torch.full((qfp4.sf_mma_grouped_bytes(int(offs[-1]), len(counts), K // 16),), 0xEE,
+                    dtype=torch.uint8, device="cuda")
+    qfp4.quantize_grouped(NV, to_dev_bf16(x), torch.from_numpy(offs).cuda(), torch.from_numpy(gs_host).cuda(), Q, SF)
+    torch.cuda.synchronize()
+    Qh, SFh = to_host(Q), to_host(SF)
+    tile = 0
+    for e in range(len(counts)):
+        if counts[e] == 0:
+            continue
+        q_ref, sf_ref = oracle.quantize(NV, x[offs[e]:offs[e + 1]], gs_host[e])
+        assert np.array_equal(Qh[offs[e]:offs[e + 1]], q_ref), e
+        ref_mma = oracle.sf_to_mma(sf_ref)
+        start = tile * (K // 64) * 512
+        assert np.array_equal(SFh[start:start + ref_mma.size], ref_mma), e
+        tile += -(-int(counts[e]) // 128)
+
+
+def test_quantize_grouped_nvfp4_every_block_amax():
+    """Every positive finite bf16 magnitude as a block maximum in each of four
+    groups with their own global scales: two inside the scale-code tables'
+    range, one below it (per-block arithmetic for that group only) and one
+    far above; bit-exact against the oracle."""
+    x = every_amax_input(31)                     # 128 rows, every magnitude once
+    # four groups of 128 rows, each with every magnitude once (rolls by whole blocks)
+    x = np.concatenate([x, np.roll(x, 16, axis=1), np.roll(x, 160, axis=1), x[::-1]])
+    gs_host = np.array([1.0, 0.0137, 2.0 ** -101, 7e25], dtype=np.float32)
+    quantize_grouped_check(x, np.array([128, 128, 128, 128]), gs_host)
+
+
+def test_quantize_grouped_nvfp4_more_groups_than_tables():
+    """Twelve groups (more than the kernel keeps scale-code tables for), with
+    ragged and empty groups: each group's gs and RN(1/gs) come from shared
+    memory and the per-block arithmetic; bit-exact against the oracle."""
+    counts = np.array([33, 0, 140, 1, 256, 7, 0, 129, 64, 3, 300, 17], dtype=np.int64)
+    x = synth.activations_bf16(23, int(counts.sum()), 1024)
+    offs = np.concatenate([[0], np.cumsum(counts)])
+    gs_host = np.array([oracle.global_scale(x[offs[e]:offs[e + 1]]) if counts[e] else np.float32(1.0)
+                        for e in range(len(counts))], dtype=np.float32)
+    gs_host[4] = np.float32(2.0 ** -110)
+    quantize_grouped_check(x, counts, gs_host)

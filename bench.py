@@ -503,7 +503,7 @@ def sweep(device, l2_bytes, peaks):
                     "frac_fp4_peak": round(tf / fp4_peak, 3)})
         us_of[(case.fmt, case.M, case.N, case.K)] = ms * 1e3
     # NVFP4 / MXFP4 time on the same shapes (the DeepGEMM pull request's
-    # "Benchmark" section reports 1.09-1.16x on B200)
+    # "Benchmark" section reports 1.09-1.16x; it does not name the GPU)
     for (fmt, M, N, K), us in sorted(us_of.items()):
         if fmt == qfp4.NVFP4 and (qfp4.MXFP4, M, N, K) in us_of:
             out.append({"workload": f"nvfp4_over_mxfp4_time_{M}x{N}x{K}",

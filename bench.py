@@ -947,13 +947,96 @@ def oracle_sample(case, target_s):
     return rows, run, oracle.num_threads()
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or ''."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return ""
+
+
+def oracle_configs(target_s=2.0):
+    """The oracle on every config, each on a bounded sample (about target_s
+    seconds): GEMM configs as TFLOP/s of global scale + quantisation of a slab
+    of activation rows + the GEMM of that slab against all N columns; the
+    quantiser as GB/s of its algorithmic bytes.  All host cores, and one core
+    for the small MXFP4 case and the decode attention shape."""
+    import oracle
+    out = []
+    full = oracle.num_threads()
+
+    def gemm_entry(case, threads, label):
+        oracle.set_num_threads(threads)
+        try:
+            rows, run, _ = oracle_sample(case, target_s)
+            dt = run(rows)
+        finally:
+            oracle.set_num_threads(full)
+        out.append({"config": label, "value": 2.0 * rows * case.N * case.K / dt / 1e12, "unit": "TFLOP/s",
+                    "threads": threads, "sample": f"{rows} of {case.M} rows x {case.N} columns, {dt:.2f} s"})
+
+    # the small MXFP4 case: fp32 operands quantised by the oracle, whole GEMM
+    c = synth.SMALL_MX
+    a = synth.normal_f32(synth.rng(c.seed), (c.M, c.K))
+    b = synth.normal_f32(synth.rng(c.seed + 1), (c.N, c.K))
+    for threads in (full, 1):
+        oracle.set_num_threads(threads)
+        try:
+            t0 = time.perf_counter()
+            reps = 0
+            while time.perf_counter() - t0 < min(target_s, 1.0) or reps == 0:
+                qa, sfa = oracle.quantize(c.fmt, a)
+                qb, sfb = oracle.quantize(c.fmt, b)
+                oracle.gemm_nt(c.fmt, qa, sfa, qb, sfb)
+                reps += 1
+            dt = (time.perf_counter() - t0) / reps
+        finally:
+            oracle.set_num_threads(full)
+        out.append({"config": c.name, "value": 2.0 * c.M * c.N * c.K / dt / 1e12, "unit": "TFLOP/s",
+                    "threads": threads, "sample": f"whole problem, {reps} runs, {dt * 1e3:.2f} ms each"})
+    gemm_entry(synth.PREFILL_NV, full, synth.PREFILL_NV.name)
+    gemm_entry(synth.DECODE_UP, full, synth.DECODE_UP.name)
+    gemm_entry(synth.DECODE_ATTN, full, synth.DECODE_ATTN.name)
+    gemm_entry(synth.DECODE_ATTN, 1, synth.DECODE_ATTN.name)
+    # the quantiser, NVFP4 X[16384, 4096]: global scale and quantisation of a slab
+    M, K = synth.QUANT_ROWS, synth.QUANT_COLS
+    x = synth.activations_bf16(synth.QUANT_SEED, M, K)
+    gs = oracle.global_scale(x)
+    t0 = time.perf_counter()
+    oracle.quantize(1, x[:64], gs)
+    t1 = max(time.perf_counter() - t0, 1e-4)
+    rows = int(max(64, min(M, 64 * target_s / t1)))
+    t0 = time.perf_counter()
+    oracle.quantize(1, x[:rows], gs)
+    dt = time.perf_counter() - t0
+    out.append({"config": f"nvfp4_quantize_{M}x{K}", "value": rows * K * (2 + 0.5 + 1 / 16) / dt / 1e9,
+                "unit": "GB/s", "threads": full, "sample": f"{rows} of {M} rows, {dt:.2f} s"})
+    # the grouped MoE up-projection: one expert's rows against its weights
+    g = synth.MOE_UP
+    counts = synth.moe_counts(g.seed, g.tokens, g.experts, g.topk)
+    e0 = synth.GemmCase(f"{g.name}_expert0", g.fmt, int(counts[0]), g.N, g.K, g.seed)
+    gemm_entry(e0, full, f"{g.name} (expert 0 of {g.experts}, {int(counts[0])} rows)")
+    return out
+
+
 def cpu_baseline(case, target_s=10.0):
     rows, run, threads = oracle_sample(case, target_s)
     dt = run(rows)
     tf = 2.0 * rows * case.N * case.K / dt / 1e12
     return {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{case.name}: global scale of all {case.M} rows, quantise {rows} rows, "
-                      f"GEMM of those {rows} rows x {case.N} columns (fp64), {dt:.1f} s"}
+                      f"GEMM of those {rows} rows x {case.N} columns (fp64), {dt:.1f} s",
+            "cpu_model": cpu_model(), "nproc": os.cpu_count(), "configs": oracle_configs()}
 
 
 def reference_arm(args):

@@ -97,6 +97,7 @@ def _load():
             "oracle_e2m1_round_n": (c_int, [c_p, c_i64, c_p]),
             "oracle_scale_round_n": (c_int, [c_int, c_p, c_i64, c_p]),
             "oracle_num_threads": (c_int, []),
+            "oracle_set_num_threads": (None, [c_int]),
             "oracle_scale_codes_bits": (c_int, [c_int, ctypes.c_uint32, c_i64, ctypes.c_float, c_p]),
             "oracle_element_codes_bits": (c_int, [ctypes.c_uint32, c_i64, ctypes.c_float, c_p]),
         }
@@ -534,3 +535,8 @@ def element_codes_bits(first: int, n: int, s) -> np.ndarray:
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Thread count of the oracle's OpenMP loops (for timing it on n cores)."""
+    _load().oracle_set_num_threads(int(n))

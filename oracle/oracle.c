@@ -664,6 +664,17 @@ int oracle_element_codes_bits(uint32_t first, int64_t n, float s, uint8_t *code)
     return 0;
 }
 
+/* Thread count of the OpenMP loops above (n > 0), for timing the oracle on
+ * a given number of host cores. */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP

@@ -320,15 +320,15 @@ gemm_sparse_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 const uint4 m0 = mrow[0], m1 = mrow[1];
                 vm[0] = m0.x; vm[1] = m0.y; vm[2] = m0.z; vm[3] = m0.w;
                 vm[4] = m1.x; vm[5] = m1.y; vm[6] = m1.z; vm[7] = m1.w;
-                // weight scales: word `quad` of the lane's 16-byte atom row, in all 4 columns of the atom
-                uint32_t vw[C::SFW_COLS];
+                // weight scales: word `quad` of the lane's 16-byte atom row, stored only in column
+                // 4 c + quad of atom c, the one this lane quarter's MMA rows read
+                uint32_t vw[4];
                 // token scales: both token tiles' atoms, 8 columns per K = 128
                 uint32_t vx[C::SFX_COLS];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const uint4 a4 = *reinterpret_cast<const uint4 *>(sd + C::META_BYTES + c * 512 + lane * 16);
-                    const uint32_t w = quad == 0 ? a4.x : quad == 1 ? a4.y : quad == 2 ? a4.z : a4.w;
-                    vw[4 * c + 0] = w; vw[4 * c + 1] = w; vw[4 * c + 2] = w; vw[4 * c + 3] = w;
+                    vw[c] = quad == 0 ? a4.x : quad == 1 ? a4.y : quad == 2 ? a4.z : a4.w;
                     const uint8_t *xs = sd + C::META_BYTES + C::SFW_BYTES;
                     const uint4 b0 = *reinterpret_cast<const uint4 *>(xs + c * 512 + lane * 16);
                     const uint4 b1 = *reinterpret_cast<const uint4 *>(xs + (4 + c) * 512 + lane * 16);
@@ -345,7 +345,8 @@ gemm_sparse_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 }
                 tc_fence_after();
                 const uint32_t col = tmem_base + C::COL_SLOT0 + slot * C::SLOT_COLS;
-                tmem_st_32x32b<C::SFW_COLS>(lane_base + col, vw);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_st_32x32b_x1(lane_base + col + 4 * c + quad, vw[c]);
                 tmem_st_32x32b<C::SFX_COLS>(lane_base + col + C::SFW_COLS, vx);
                 tmem_st_32x32b<C::META_COLS>(lane_base + col + C::SFW_COLS + C::SFX_COLS, vm);
                 tmem_st_wait();

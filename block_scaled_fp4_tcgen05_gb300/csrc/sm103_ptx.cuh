@@ -507,6 +507,12 @@ __device__ __forceinline__ void tmem_st_32x32b<32>(uint32_t taddr, const uint32_
         : "memory");
 }
 
+// One 32-bit column of the warp's 32 lanes.
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t r)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r) : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait()
 {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");

@@ -26,12 +26,15 @@
 //                 quarter), then signal the leader.  Writing from registers
 //                 keeps the tensor pipe free of the shared->tensor-memory
 //                 copies NVFP4 would otherwise need (twelve per 256-K block),
-//                 and only B's scales are replicated across the quarters.
-//   warps 12..19  epilogue: drain 128 rows x 256 columns of the accumulator in
-//                 two halves (scaled by gs_a * gs_b and rounded to BF16 on the
-//                 way), release it once all eight have drained, and store it
-//                 through per-warp staging boxes with TMA stores while the
-//                 next tile's main loop runs.
+//                 and only B's scales are replicated across the quarters (A's
+//                 go into the one column per atom that each quarter reads).
+//                 One warp per set waits on the commit that frees the slot.
+//   warps 12..19  epilogue: one warp waits for the accumulator and tells the
+//                 others through a named barrier; all eight drain 128 rows x
+//                 256 columns in two halves (scaled by gs_a * gs_b and rounded
+//                 to BF16 on the way), release it once all have drained, and
+//                 store it through per-warp staging boxes with TMA stores
+//                 while the next tile's main loop runs.
 // Hand-offs between the CTAs use cluster-scope mbarrier arrivals; the ones
 // that only order tensor-memory writes (already complete after
 // tcgen05.wait::st and fenced) are relaxed, which keeps them off the

@@ -517,11 +517,15 @@ def sweep(device, l2_bytes, peaks):
         src = torch.randint(0, 0x7F, (rows, cols), dtype=torch.uint8, device=device)
         dst = torch.empty(qfp4.sf_mma_bytes(rows, cols), dtype=torch.uint8, device=device)
         sets.append((src, dst))
-    calls = [(lambda a=a, b=b: qfp4.sf_interleave(a, rows, cols, b, qfp4.SF_MMA)) for a, b in sets] * 4
-    ms = graph_time(calls, 10)
     byts = rows * cols + qfp4.sf_mma_bytes(rows, cols)
-    out.append({"workload": f"sf_interleave_to_mma_{rows}x{cols}", "us": round(ms * 1e3, 2),
-                "GB/s": round(byts / (ms * 1e-3) / 1e9, 1), "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)})
+    # both directions: row-major -> MMA layout, then back on the same buffers
+    for name, layout, fwd in (("to_mma", qfp4.SF_MMA, True), ("to_rowmajor", qfp4.SF_ROWMAJOR, False)):
+        calls = [(lambda a=a, b=b, layout=layout, fwd=fwd: qfp4.sf_interleave(a, rows, cols, b, layout) if fwd
+                  else qfp4.sf_interleave(b, rows, cols, a, layout)) for a, b in sets] * 4
+        ms = graph_time(calls, 10)
+        out.append({"workload": f"sf_interleave_{name}_{rows}x{cols}", "us": round(ms * 1e3, 2),
+                    "GB/s": round(byts / (ms * 1e-3) / 1e9, 1),
+                    "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)})
     del sets, calls
     # 2:4 pair-sparse GEMM against the dense one
     out += sparse_time(device, l2_bytes, fp4_peak)

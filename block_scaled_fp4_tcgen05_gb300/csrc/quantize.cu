@@ -653,6 +653,38 @@ sf_to_mma_tiled_kernel(const uint8_t *__restrict__ in, uint8_t *__restrict__ out
     if (w == 32) dst[t + 128] = srcs[t + 128];
 }
 
+// The inverse, MMA layout -> row-major scale bytes, under the same
+// conditions: CTA b reads the w / 4 adjacent atoms of rows [128 R, 128 R +
+// 128) and columns [32 C, 32 C + w) as one contiguous run into shared
+// memory, and thread t writes its row's w bytes (whole 32-byte sectors);
+// the layout's padding rows are not written.
+__global__ void __launch_bounds__(128)
+sf_from_mma_tiled_kernel(const uint8_t *__restrict__ in, uint8_t *__restrict__ out, int64_t rows,
+                         int64_t cols, int64_t kc, int64_t chunks_per_row)
+{
+    __shared__ __align__(16) uint32_t atoms[8 * 128];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t R = blockIdx.x / chunks_per_row, C = blockIdx.x % chunks_per_row;
+    const int t = threadIdx.x;
+    const int64_t c0 = 32 * C;
+    const int w = cols - c0 >= 32 ? 32 : 16;
+    const uint4 *src = reinterpret_cast<const uint4 *>(in + (R * kc + 8 * C) * 512);
+    uint4 *stage = reinterpret_cast<uint4 *>(atoms);
+    stage[t] = src[t];
+    if (w == 32) stage[t + 128] = src[t + 128];
+    __syncthreads();
+    const int64_t r = 128 * R + t;
+    if (r < rows) {
+        const int pos = (t & 31) * 4 + (t >> 5);
+        uint4 *dst = reinterpret_cast<uint4 *>(out + r * cols + c0);
+        dst[0] = make_uint4(atoms[0 * 128 + pos], atoms[1 * 128 + pos], atoms[2 * 128 + pos], atoms[3 * 128 + pos]);
+        if (w == 32)
+            dst[1] = make_uint4(atoms[4 * 128 + pos], atoms[5 * 128 + pos], atoms[6 * 128 + pos],
+                                atoms[7 * 128 + pos]);
+    }
+}
+
 int grid_for(int64_t work_items, int per_block)
 {
     const int sms = sm_count();
@@ -920,12 +952,13 @@ extern "C" int qfp4_sf_interleave(const void *SF_in, int64_t rows, int64_t cols,
     const int64_t kc = (cols + 3) / 4;
     const int64_t words = ((rows + 127) / 128) * kc * 128;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (layout == QFP4_SF_MMA && cols % 16 == 0 && aligned16(SF_in) && aligned16(SF_out)) {
+    if (cols % 16 == 0 && aligned16(SF_in) && aligned16(SF_out)) {
         const int64_t chunks_per_row = (cols + 31) / 32;
         const int64_t blocks = ((rows + 127) / 128) * chunks_per_row;
         if (blocks <= INT32_MAX)
-            return launch_status(launch_pdl(sf_to_mma_tiled_kernel, dim3(static_cast<unsigned>(blocks)), dim3(128), 0,
-                                            s, static_cast<const uint8_t *>(SF_in), static_cast<uint8_t *>(SF_out),
+            return launch_status(launch_pdl(layout == QFP4_SF_MMA ? sf_to_mma_tiled_kernel : sf_from_mma_tiled_kernel,
+                                            dim3(static_cast<unsigned>(blocks)), dim3(128), 0, s,
+                                            static_cast<const uint8_t *>(SF_in), static_cast<uint8_t *>(SF_out),
                                             rows, cols, kc, chunks_per_row));
     }
     const int grid = grid_for(words, kThreads);

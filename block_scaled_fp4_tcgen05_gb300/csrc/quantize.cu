@@ -20,8 +20,10 @@
 // second correction returns RN(x/s) when y = RN(1/s), the previous quotient
 // is within one ulp and nothing underflows or overflows.  Blocks whose scale
 // or range could leave that regime take CUDA's IEEE division instead.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <mutex>
 
 #include "qfp4_common.cuh"
 #include "qfp4_fp4_codes.cuh"
@@ -399,11 +401,17 @@ quantize_kernel(const uint8_t *__restrict__ X, int64_t total_blocks, int64_t K,
 // (non-negative floats order like unsigned integers); a warp keeps a running
 // maximum while its rows stay in one group.  One tensor uses amax_flat_kernel.
 // rows < 0: the row count is row_offsets[groups], read on the device.
+// The group words are those of a reduction slot (groups words, then the
+// count of CTAs that have added to them): the CTA that arrives last writes
+// gs_out[e] = amax / (6 * 448), 0 for every group when the offsets are bad,
+// and puts the slot back to zero.
 __global__ void __launch_bounds__(kThreads)
 amax_rows_kernel(const uint4 *__restrict__ X, int64_t rows, int64_t chunks_per_row, int groups,
-                 const int32_t *__restrict__ row_offsets, uint32_t *__restrict__ amax_bits)
+                 const int32_t *__restrict__ row_offsets, uint32_t *__restrict__ amax_bits,
+                 float *__restrict__ gs_out)
 {
     __shared__ int32_t s_offs[kMaxGroups + 1];
+    __shared__ int s_last;
     pdl_wait();
     pdl_launch_dependents();
     __shared__ int s_bad;
@@ -415,13 +423,12 @@ amax_rows_kernel(const uint4 *__restrict__ X, int64_t rows, int64_t chunks_per_r
         if (s_bad && blockIdx.x == 0) atomicOr(&g_status_quant, static_cast<uint32_t>(kStatusBadGroup));
     }
     __syncthreads();
-    if (s_bad) return;
     const int lane = threadIdx.x & 31;
     const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     int cur = -1;
     float run = 0.0f;
-    for (int64_t r = warp; r < rows; r += nwarps) {
+    for (int64_t r = s_bad ? rows : warp; r < rows; r += nwarps) {
         const uint4 *p = X + r * chunks_per_row;
         float m = 0.0f;
         int64_t i = lane;
@@ -461,15 +468,43 @@ amax_rows_kernel(const uint4 *__restrict__ X, int64_t rows, int64_t chunks_per_r
         run = fmaxf(run, m);
     }
     if (cur >= 0 && lane == 0) atomicMax(amax_bits + cur, __float_as_uint(run));
+    if (lane == 0) __threadfence();
+    __syncthreads();
+    uint32_t *count = amax_bits + groups;
+    if (threadIdx.x == 0) s_last = atomicAdd(count, 1u) == gridDim.x - 1 ? 1 : 0;
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        for (int e = threadIdx.x; e < groups; e += blockDim.x) {
+            const uint32_t bits = atomicExch(amax_bits + e, 0u);
+            gs_out[e] = s_bad ? 0.0f : __fdiv_rn(__uint_as_float(bits), 2688.0f);
+        }
+        if (threadIdx.x == 0) *count = 0u;
+    }
 }
 
-// amax over all of X (one group): the rows are contiguous, so X is walked as
-// one flat array of 16-byte vectors, eight loads in flight per thread per
-// round (one or two rounds of memory latency for a 32 MB tensor instead of
-// one per 2 KB of a row), then one atomic per CTA.
+// Reduction slots of the one-tensor global scale: per slot the running amax
+// bit pattern and the count of CTAs that have added to it.  Zero when the
+// module loads; every launch leaves its slot at zero again, so a slot can be
+// reused by the next launch that draws it.  The host hands the slots out in
+// turn, so that launches in flight at the same time (on other streams) use
+// different ones as long as fewer than kGsSlots are in flight.
+constexpr int kGsSlots = 1024;
+__device__ uint32_t g_gs_slots[2 * kGsSlots];
+// The same for the per-group form: kMaxGroups group words and a count per slot.
+constexpr int kGsGroupSlots = 64;
+__device__ uint32_t g_gs_group_slots[kGsGroupSlots * (kMaxGroups + 1)];
+
+// gs = amax(X) / (6 * 448) for all of X (one group), in one launch: the rows
+// are contiguous, so X is walked as one flat array of 16-byte vectors, eight
+// loads in flight per thread per round (one or two rounds of memory latency
+// for a 32 MB tensor instead of one per 2 KB of a row).  Each CTA folds its
+// maximum into the slot with one atomic and then counts itself in; the CTA
+// that arrives last (all maxima are in by then) divides, writes gs_out and
+// puts the slot back to zero.
 constexpr int kAmaxUnroll = 8;
 __global__ void __launch_bounds__(kThreads)
-amax_flat_kernel(const uint4 *__restrict__ X, int64_t nvec, uint32_t *__restrict__ amax_bits)
+amax_flat_kernel(const uint4 *__restrict__ X, int64_t nvec, uint32_t *__restrict__ slot, float *__restrict__ gs_out)
 {
     __shared__ float s_warp[kThreads / 32];
     pdl_wait();
@@ -504,7 +539,14 @@ amax_flat_kernel(const uint4 *__restrict__ X, int64_t nvec, uint32_t *__restrict
 #pragma unroll
         for (int w = 0; w < kThreads / 32; ++w) cm = fmaxf(cm, s_warp[w]);
         // non-negative floats order like their bit patterns
-        if (cm != 0.0f) atomicMax(amax_bits, __float_as_uint(cm));
+        if (cm != 0.0f) atomicMax(slot, __float_as_uint(cm));
+        __threadfence();
+        if (atomicAdd(slot + 1, 1u) == gridDim.x - 1) {
+            __threadfence();
+            const uint32_t bits = atomicExch(slot, 0u);
+            slot[1] = 0u;
+            *gs_out = __fdiv_rn(__uint_as_float(bits), 2688.0f);
+        }
     }
 }
 
@@ -550,29 +592,6 @@ gs_rows_kernel(const uint4 *__restrict__ X, int64_t rows, int64_t chunks_per_row
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) gs_out[r] = __fdiv_rn(m, 2688.0f);
-    }
-}
-
-// Zeroes the amax words before the atomics of the amax kernels.  A kernel
-// rather than a memset so that the next launch overlaps it; its wait also
-// keeps it behind the previous kernel, which may still read these words as
-// global scales.
-__global__ void gs_init_kernel(uint32_t *bits, int n)
-{
-    pdl_wait();
-    pdl_launch_dependents();
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) bits[i] = 0u;
-}
-
-// gs = amax / (6 * 448), in place over the amax bit patterns.
-__global__ void gs_finalize_kernel(uint32_t *bits, int n)
-{
-    pdl_wait();
-    pdl_launch_dependents();
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < n) {
-        const float amax = __uint_as_float(bits[i]);
-        reinterpret_cast<float *>(bits)[i] = __fdiv_rn(amax, 2688.0f);
     }
 }
 
@@ -736,27 +755,54 @@ extern "C" size_t qfp4_sf_mma_grouped_bytes(int64_t total_rows, int64_t groups, 
            static_cast<size_t>((cols + 3) / 4) * 512u;
 }
 
+// Device addresses of the slot pools on the current device (looked up once
+// per device): pool 0 one tensor, pool 1 per group.
+static uint32_t *gs_slot_pool(int which)
+{
+    static std::mutex mu;
+    static uint32_t *cached[2][64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cached[which][dev]) {
+        void *p = nullptr;
+        if ((which == 0 ? cudaGetSymbolAddress(&p, g_gs_slots) : cudaGetSymbolAddress(&p, g_gs_group_slots)) !=
+            cudaSuccess)
+            return nullptr;
+        cached[which][dev] = static_cast<uint32_t *>(p);
+    }
+    return cached[which][dev];
+}
+
+// The next per-group slot (handed out in turn).
+static uint32_t *gs_group_slot()
+{
+    uint32_t *pool = gs_slot_pool(1);
+    if (!pool) return nullptr;
+    static std::atomic<uint32_t> next_slot{0};
+    return pool + (next_slot.fetch_add(1u, std::memory_order_relaxed) % kGsGroupSlots) * (kMaxGroups + 1);
+}
+
 extern "C" int qfp4_global_scale(const void *X_bf16, int64_t rows, int64_t cols, float *gs_out,
                                  void *stream)
 {
-    if (!X_bf16 || !gs_out || rows < 0 || cols < 0) return QFP4_ERR_INVALID_ARG;
+    // X may be NULL when it is empty (nothing is read; gs = 0 is written)
+    if (!gs_out || rows < 0 || cols < 0 || (!X_bf16 && rows > 0 && cols > 0)) return QFP4_ERR_INVALID_ARG;
     if (cols % 8 != 0) return QFP4_ERR_UNSUPPORTED;
     if (!aligned16(X_bf16) || !aligned4(gs_out)) return QFP4_ERR_MISALIGNED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (launch_pdl(gs_init_kernel, dim3(1), dim3(32), 0, s, reinterpret_cast<uint32_t *>(gs_out), 1) != cudaSuccess)
-        return QFP4_ERR_CUDA;
-    if (rows > 0 && cols > 0) {
-        const int64_t nvec = rows * (cols / 8);
-        const int sms = sm_count();
-        int64_t grid = static_cast<int64_t>(sms > 0 ? sms : 148) * 6;
-        const int64_t want = (nvec + kThreads - 1) / kThreads;
-        if (want < grid) grid = want;
-        if (launch_pdl(amax_flat_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
-                       static_cast<const uint4 *>(X_bf16), nvec, reinterpret_cast<uint32_t *>(gs_out)) != cudaSuccess)
-            return QFP4_ERR_CUDA;
-    }
-    return launch_status(launch_pdl(gs_finalize_kernel, dim3(1), dim3(32), 0, s,
-                                    reinterpret_cast<uint32_t *>(gs_out), 1));
+    uint32_t *slots = gs_slot_pool(0);
+    if (!slots) return QFP4_ERR_CUDA;
+    static std::atomic<uint32_t> next_slot{0};
+    uint32_t *slot = slots + 2 * (next_slot.fetch_add(1u, std::memory_order_relaxed) % kGsSlots);
+    const int64_t nvec = rows * (cols / 8);
+    const int sms = sm_count();
+    int64_t grid = static_cast<int64_t>(sms > 0 ? sms : 148) * 6;
+    const int64_t want = (nvec + kThreads - 1) / kThreads;
+    if (want < grid) grid = want;
+    if (grid < 1) grid = 1;                 // an empty X still writes gs = 0
+    return launch_status(launch_pdl(amax_flat_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
+                                    static_cast<const uint4 *>(X_bf16), nvec, slot, gs_out));
 }
 
 extern "C" int qfp4_global_scale_grouped(const void *X_bf16, int64_t total_rows, int64_t cols,
@@ -769,18 +815,13 @@ extern "C" int qfp4_global_scale_grouped(const void *X_bf16, int64_t total_rows,
     if (!aligned16(X_bf16) || !aligned4(gs_out) || !aligned4(row_offsets))
         return QFP4_ERR_MISALIGNED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (launch_pdl(gs_init_kernel, dim3((static_cast<unsigned>(groups) + 127) / 128), dim3(128), 0, s,
-                   reinterpret_cast<uint32_t *>(gs_out), static_cast<int>(groups)) != cudaSuccess)
-        return QFP4_ERR_CUDA;
-    if (total_rows > 0 && cols > 0) {
-        const int grid = grid_for(total_rows, kThreads / 32);
-        if (launch_pdl(amax_rows_kernel, dim3(grid), dim3(kThreads), 0, s, static_cast<const uint4 *>(X_bf16),
-                       total_rows, cols / 8, static_cast<int>(groups), row_offsets,
-                       reinterpret_cast<uint32_t *>(gs_out)) != cudaSuccess)
-            return QFP4_ERR_CUDA;
-    }
-    return launch_status(launch_pdl(gs_finalize_kernel, dim3((static_cast<unsigned>(groups) + 127) / 128), dim3(128),
-                                    0, s, reinterpret_cast<uint32_t *>(gs_out), static_cast<int>(groups)));
+    uint32_t *slot = gs_group_slot();
+    if (!slot) return QFP4_ERR_CUDA;
+    // one launch; an empty X still runs one CTA, which writes gs = 0
+    const int grid = total_rows > 0 && cols > 0 ? grid_for(total_rows, kThreads / 32) : 1;
+    return launch_status(launch_pdl(amax_rows_kernel, dim3(grid), dim3(kThreads), 0, s,
+                                    static_cast<const uint4 *>(X_bf16), total_rows,
+                                    cols / 8, static_cast<int>(groups), row_offsets, slot, gs_out));
 }
 
 extern "C" int qfp4_absmax_gs(int64_t groups, const int32_t *row_offsets, const void *X_bf16, int64_t K,
@@ -790,21 +831,15 @@ extern "C" int qfp4_absmax_gs(int64_t groups, const int32_t *row_offsets, const 
     if (groups > kMaxGroups || K % 8 != 0) return QFP4_ERR_UNSUPPORTED;
     if (!aligned16(X_bf16) || !aligned4(gs_out) || !aligned4(row_offsets)) return QFP4_ERR_MISALIGNED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const unsigned gblocks = (static_cast<unsigned>(groups) + 127) / 128;
-    if (launch_pdl(gs_init_kernel, dim3(gblocks), dim3(128), 0, s, reinterpret_cast<uint32_t *>(gs_out),
-                   static_cast<int>(groups)) != cudaSuccess)
-        return QFP4_ERR_CUDA;
-    if (K > 0) {
-        // the row count lives on the device: a full grid of row-walking warps
-        const int sms = sm_count();
-        const int grid = (sms > 0 ? sms : 148) * 8;
-        if (launch_pdl(amax_rows_kernel, dim3(grid), dim3(kThreads), 0, s, static_cast<const uint4 *>(X_bf16),
-                       int64_t{-1}, K / 8, static_cast<int>(groups), row_offsets,
-                       reinterpret_cast<uint32_t *>(gs_out)) != cudaSuccess)
-            return QFP4_ERR_CUDA;
-    }
-    return launch_status(launch_pdl(gs_finalize_kernel, dim3(gblocks), dim3(128), 0, s,
-                                    reinterpret_cast<uint32_t *>(gs_out), static_cast<int>(groups)));
+    uint32_t *slot = gs_group_slot();
+    if (!slot) return QFP4_ERR_CUDA;
+    // the row count lives on the device: a full grid of row-walking warps
+    // (K = 0: one CTA, which walks the rows without reading and writes gs = 0)
+    const int sms = sm_count();
+    const int grid = K > 0 ? (sms > 0 ? sms : 148) * 8 : 1;
+    return launch_status(launch_pdl(amax_rows_kernel, dim3(grid), dim3(kThreads), 0, s,
+                                    static_cast<const uint4 *>(X_bf16), int64_t{-1}, K / 8,
+                                    static_cast<int>(groups), row_offsets, slot, gs_out));
 }
 
 extern "C" int qfp4_global_scale_rows(const void *X_bf16, int64_t rows, int64_t cols, float *gs_out,

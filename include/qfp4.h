@@ -113,7 +113,8 @@ size_t qfp4_sf_mma_grouped_bytes(int64_t total_rows, int64_t groups, int64_t col
  * BF16 [rows, cols] row-major.  The block whose |x| reaches amax then gets
  * the largest UE4M3 scale, 448.  DeepGEMM pull request "Summary" (per-tensor
  * fp32 global scales).  Requirements: rows, cols >= 0, X 16-byte aligned,
- * cols % 8 == 0.  An empty X gives gs = 0. */
+ * cols % 8 == 0.  An empty X (rows or cols 0; X may then be NULL) gives
+ * gs = 0. */
 int qfp4_global_scale(const void *X_bf16, int64_t rows, int64_t cols, float *gs_out,
                       void *stream);
 

@@ -146,6 +146,62 @@ def test_global_scale_bitexact(rows, cols):
     assert np.float32(gs.item()) == oracle.global_scale(x)
 
 
+def test_global_scale_many_launches():
+    """The one-tensor global scale reduces through a pool of device slots that
+    every launch hands back at zero: more launches than the pool has slots,
+    back to back on one stream, on tensors whose maxima differ (and an empty
+    and an all-zero one among them), each bit-exact."""
+    shapes = [(1, 8), (3, 16), (130, 64), (0, 8), (257, 40)]
+    xs = []
+    for i, (r, c) in enumerate(shapes):
+        x = synth.activations_bf16(4000 + i, r, c) if r else np.zeros((0, c), np.uint16)
+        xs.append((to_dev_bf16(x) if r else torch.zeros((1, c), dtype=torch.bfloat16, device="cuda"), r, c,
+                   oracle.global_scale(x) if r else np.float32(0.0)))
+    zero = torch.zeros((5, 24), dtype=torch.bfloat16, device="cuda")
+    n = 1100 + 7
+    out = torch.full((n,), -1.0, dtype=torch.float32, device="cuda")
+    want = []
+    for k in range(n):
+        if k % 11 == 5:
+            qfp4.global_scale(zero, out[k:k + 1])
+            want.append(np.float32(0.0))
+        else:
+            X, r, c, w = xs[k % len(xs)]
+            qfp4.global_scale(X[:r] if r else X[:0], out[k:k + 1])
+            want.append(w)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_host(out), np.array(want, dtype=np.float32))
+
+
+def test_global_scale_grouped_many_launches():
+    """The per-group global scales reduce through a pool of 64 device slots:
+    more launches than that, alternating the two entry points (row count on
+    the host, row count read on the device) and group layouts with empty
+    groups, each bit-exact against the oracle per group."""
+    layouts = [np.array([5, 0, 130, 1], dtype=np.int64), np.array([0, 0, 64], dtype=np.int64),
+               np.array([300, 17, 0, 0, 2, 9, 1, 44], dtype=np.int64)]
+    cases = []
+    for i, counts in enumerate(layouts):
+        offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+        x = synth.activations_bf16(5000 + i, int(offs[-1]), 96)
+        want = np.array([oracle.global_scale(x[offs[e]:offs[e + 1]]) if counts[e] else np.float32(0.0)
+                         for e in range(len(counts))], dtype=np.float32)
+        cases.append((to_dev_bf16(x), torch.from_numpy(offs).cuda(), want))
+    results = []
+    for k in range(70):
+        X, d_offs, want = cases[k % len(cases)]
+        gs = torch.full((len(want),), -1.0, dtype=torch.float32, device="cuda")
+        if k % 2:
+            qfp4.absmax_gs(d_offs, X, gs)
+        else:
+            qfp4.global_scale_grouped(X, d_offs, gs)
+        results.append((gs, want))
+    torch.cuda.synchronize()
+    assert qfp4.poll_device_status() == 0
+    for k, (gs, want) in enumerate(results):
+        assert np.array_equal(to_host(gs), want), k
+
+
 def test_global_scale_grouped_bitexact():
     counts = synth.moe_counts(5)
     offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)

@@ -114,7 +114,13 @@ size_t qfp4_sf_mma_grouped_bytes(int64_t total_rows, int64_t groups, int64_t col
  * the largest UE4M3 scale, 448.  DeepGEMM pull request "Summary" (per-tensor
  * fp32 global scales).  Requirements: rows, cols >= 0, X 16-byte aligned,
  * cols % 8 == 0.  An empty X (rows or cols 0; X may then be NULL) gives
- * gs = 0. */
+ * gs = 0.
+ * One launch: the CTAs reduce through one of 1024 slots in the library's
+ * device memory, handed out in turn by the host and left at zero by every
+ * launch.  So at most 1024 calls may be in flight at once (over all
+ * streams), and a CUDA graph that captured a call reuses that slot on every
+ * replay: one graph must not be replayed concurrently with itself.  The
+ * grouped forms below have 64 slots. */
 int qfp4_global_scale(const void *X_bf16, int64_t rows, int64_t cols, float *gs_out,
                       void *stream);
 

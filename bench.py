@@ -231,10 +231,15 @@ class Flush:
         return self.buf.sum()
 
 
-def time_steps(pipe, n, flush, stream):
-    """n steps, each bracketed by CUDA events (start, after the prologue,
-    after the GEMM) on the launching stream, with the L2 flush before each
-    step outside the events.  Returns per-step (step, gemm, prologue) ms."""
+def time_steps(pipe, n, flush, stream, split=True):
+    """n steps, each bracketed by CUDA events on the launching stream, with
+    the L2 flush before each step outside the events.  split: one more event
+    between the prologue and the GEMM, for the breakdown; it makes the GEMM
+    wait for the quantiser to finish instead of starting its set-up under the
+    quantiser's tail (programmatic dependent launch), which lengthens the
+    step by ~6 us, so the step time itself is taken without it.  Returns
+    per-step (step, gemm, prologue) ms (gemm and prologue empty unless
+    split)."""
     torch = pipe.torch
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(n)]
@@ -243,19 +248,25 @@ def time_steps(pipe, n, flush, stream):
         e0, e1, e2 = ev[i]
         e0.record(stream)
         pipe.prologue()
-        e1.record(stream)
+        if split:
+            e1.record(stream)
         pipe.gemm()
         e2.record(stream)
     torch.cuda.synchronize()
-    return ([a.elapsed_time(c) for a, _, c in ev], [b.elapsed_time(c) for _, b, c in ev],
-            [a.elapsed_time(b) for a, b, _ in ev])
+    steps = [a.elapsed_time(c) for a, _, c in ev]
+    if not split:
+        return steps, [], []
+    return steps, [b.elapsed_time(c) for _, b, c in ev], [a.elapsed_time(b) for a, b, _ in ev]
 
 
 def time_main(pipe, steps, warmup, flush, world, device, clocks_gpu, soak_s=SOAK_SECONDS):
     """Warm-up, then a soak of soak_s seconds of flushed steps (not part of
     `value`), then exactly `steps` timed steps between barriers and
-    synchronisations; SM clocks are sampled over the soak and the timed
-    steps.  Returns (total ms of the timed steps, max over ranks; stats)."""
+    synchronisations (events before and after each step only), then a second
+    block of `steps` steps, also between barriers and synchronisations, with
+    the event between the prologue and the GEMM that times the GEMM alone.
+    SM clocks are sampled over all of them.  Returns (total ms of the timed
+    steps, max over ranks; stats)."""
     torch = pipe.torch
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
@@ -277,7 +288,11 @@ def time_main(pipe, steps, warmup, flush, world, device, clocks_gpu, soak_s=SOAK
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
-        step_ms, gemm_ms, pro_ms = time_steps(pipe, steps, flush, stream)
+        step_ms, _, _ = time_steps(pipe, steps, flush, stream, split=False)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        split_ms, gemm_ms, pro_ms = time_steps(pipe, steps, flush, stream)
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
@@ -286,6 +301,7 @@ def time_main(pipe, steps, warmup, flush, world, device, clocks_gpu, soak_s=SOAK
     stats = {"gemm_ms_median": statistics.median(all_gemm), "gemm_ms_min": min(all_gemm),
              "gemm_ms_timed_median": statistics.median(gemm_ms),
              "prologue_ms_median": statistics.median(soak_pro + pro_ms),
+             "split_step_ms_median": statistics.median(split_ms),
              "soak": {"steps": len(soak_step), "seconds": round(soak_wall, 2),
                       "step_us_median": round(statistics.median(soak_step) * 1e3, 2),
                       "step_us_min": round(min(soak_step) * 1e3, 2)},
@@ -481,7 +497,8 @@ def sweep(device, l2_bytes, peaks):
     flush = Flush(device)
     stream = torch.cuda.current_stream()
     time_steps(pipe, 5, flush, stream)
-    st, gm, pr = time_steps(pipe, 200, flush, stream)
+    st, _, _ = time_steps(pipe, 200, flush, stream, split=False)
+    _, gm, pr = time_steps(pipe, 200, flush, stream)
     c = synth.PREFILL_NV
     flop = 2.0 * c.M * c.N * c.K
     out.append({"workload": f"nvfp4_step_{c.M}x{c.N}x{c.K}", "us_step": round(statistics.median(st) * 1e3, 2),
@@ -846,17 +863,23 @@ def grouped_time(device, fp4_peak):
     torch.cuda.synchronize()
     flush = Flush(device)
     ts, gts = [], []
-    for _ in range(5):
-        flush()
-        s, m, e = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-        s.record()
-        prologue()
-        m.record()
-        gemm()
-        e.record()
-        torch.cuda.synchronize()
-        ts.append(s.elapsed_time(e))
-        gts.append(m.elapsed_time(e))
+    # the step without an event between prologue and GEMM (which would make
+    # the GEMM wait for the quantiser), then the GEMM alone with one
+    for split in (False, True):
+        for _ in range(5):
+            flush()
+            s, m, e = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            s.record()
+            prologue()
+            if split:
+                m.record()
+            gemm()
+            e.record()
+            torch.cuda.synchronize()
+            if split:
+                gts.append(m.elapsed_time(e))
+            else:
+                ts.append(s.elapsed_time(e))
     flops = 2.0 * rows * N * K
     ms, gms = statistics.median(ts), statistics.median(gts)
     return {"workload": case.name, "expert_rows": counts.tolist(), "us_step": round(ms * 1e3, 1),
@@ -1170,6 +1193,11 @@ def main():
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "l2": "flushed between timed steps (read-only pass over 512 MiB, 4x L2)",
                        "step": "global scale + quantise (SF in MMA layout) + GEMM",
+                       "timing": "value: the timed steps, CUDA events before and after each step only; "
+                                 "gemm_us / prologue_us: the soak and a second block of the same number of "
+                                 "steps, with an event between the prologue and the GEMM (which makes the "
+                                 "GEMM wait for the quantiser to finish)",
+                       "step_us_with_split_event": round(stats["split_step_ms_median"] * 1e3, 2),
                        "soak": stats["soak"]},
             "gpu_launches": pipe_kernels(case) * args.steps,
             "roofline": roof, "cpu_baseline": cpu,

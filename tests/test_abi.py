@@ -112,6 +112,8 @@ def test_grouped_and_interleave_reject_bad_arguments(lib):
     assert lib.qfp4_sf_interleave(FAKE, 0, 10, FAKE, 1, None) == 0
     assert lib.qfp4_global_scale(FAKE, 10, 12, FAKE, None) == -2
     assert lib.qfp4_global_scale(FAKE + 2, 10, 16, FAKE, None) == -3
+    assert lib.qfp4_global_scale(None, 10, 16, FAKE, None) == -1          # X NULL but not empty
+    assert lib.qfp4_global_scale(FAKE, 10, 16, None, None) == -1          # no gs_out
 
 
 def test_absmax_gs_rejects_bad_arguments(lib):
